@@ -1,0 +1,417 @@
+"""Benchmark of one paged decode step on GB300.
+
+A step is one pass of the device path over one batch: kv_append of one new
+token per sequence into its slot, then paged decode attention over every
+sequence's context (split-context reduction included when the context is
+partitioned).  Copy-on-write (block_copy) is part of the path but this batch
+shares no blocks, so its step has no pairs to copy.
+
+Workload (default): an OPT-13B-shaped attention layer — 40 heads of 128 (MHA),
+fp16, blocks of 16 tokens, 64 sequences with lognormal context lengths
+(median 500, sigma 1, clipped to [16, 2048]) whose blocks are shuffled
+through a pool 1.3x the size needed; q/K/V ~ N(0, 1), seeded.  Each step
+rewrites the token at the last position (the step's new token) and attends
+over the whole context, so every step does the same work.
+
+Prints one JSON line: value = algorithmic HBM bytes of the step / step time
+(GB/s, summed over ranks), plus decode seqs/s, the roofline of the decode
+call, an end-to-end figure through the C ABI with host buffers, the oracle
+timed on host cores, and SM clocks sampled during the timed region.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged decode attention HBM GB/s (% of GB300 peak) and decode seqs/s per layer"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="opt13b", choices=["opt13b", "gqa4k"])
+    ap.add_argument("--partition", type=int, default=0, help="tokens per partition (0 = library)")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------- utilities --
+
+def peak_hbm():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def source_hash(*names):
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "paged_kv_cache_247_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel_key, workload):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)[workload][kernel_key]
+    except (OSError, KeyError, ValueError):
+        return None
+    if rec.get("source_hash") != source_hash("decode.cu", "common.cuh"):
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi sampling every 200 ms in the background."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.file.flush()
+        with open(self.file.name) as f:
+            rows = [r.strip().split(", ") for r in f if r.strip()]
+        os.unlink(self.file.name)
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                mx = float(r[2])
+            except ValueError:
+                continue
+            for name, val in zip(names, r[5:9]):
+                if val.strip().lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# -------------------------------------------------------------- workload --
+
+def make_workload(name, device):
+    from paged_kv_cache_247_gb300 import workloads as W
+    if name == "opt13b":
+        case = W.opt13b_layer_decode(device=device)
+        desc = dict(W.OPT13B_LAYER)
+        label = "OPT-13B-shaped layer decode + kv_append"
+    else:
+        case = W.gqa_4k_decode(device=device)
+        desc = dict(W.GQA_4K)
+        label = "GQA 32q/8kv decode, ctx 4096 + kv_append"
+    S, Hq, D = case.q.shape
+    Hkv = case.k_cache.shape[1]
+    k_new, v_new = W.new_tokens(11, S, Hkv, D, desc["dtype"], device=device)
+    slots = W.last_position_slots(case).to(device)
+    return case, k_new, v_new, slots, desc, label
+
+
+def step_bytes(case):
+    """Algorithmic HBM bytes of one step: decode reads each context's K and V
+    once plus q, the table and the lengths, and writes out; the append reads
+    and writes one K and one V row per sequence (plus its slot)."""
+    S, Hq, D = case.q.shape
+    Hkv, B = case.k_cache.shape[1], case.block_size
+    e = case.q.element_size()
+    lens = case.context_lens.cpu().numpy().astype(np.int64)
+    kv = int(lens.sum()) * 2 * Hkv * D * e
+    decode = kv + 2 * S * Hq * D * e + int((-(-lens // B)).sum()) * 4 + S * 4
+    append = 2 * 2 * S * Hkv * D * e + S * 8
+    return decode, append
+
+
+# ------------------------------------------------------------- CPU legs --
+
+def oracle_sample_rate(case, k_new, v_new, slots, seconds, max_seqs=None):
+    """Time the fp64 oracle (append + decode) on whole sequences of the
+    workload until `seconds` pass; returns (GB/s, sequences done, elapsed)."""
+    import oracle
+    S, Hq, D = case.q.shape
+    Hkv, B = case.k_cache.shape[1], case.block_size
+    e = case.q.element_size()
+    tables = case.block_tables.cpu().numpy()
+    lens = case.context_lens.cpu().numpy()
+    order = np.random.default_rng(0).permutation(S)
+    done, nbytes, t_total = 0, 0, 0.0
+    i = 0
+    while t_total < seconds and (max_seqs is None or done < max_seqs):
+        s = int(order[i % S])
+        i += 1
+        nb = -(-int(lens[s]) // B)
+        ids = torch.from_numpy(tables[s, :nb].astype(np.int64)).to(case.k_cache.device)
+        kc = case.k_cache.index_select(0, ids).float().cpu().numpy()
+        vc = case.v_cache.index_select(0, ids).float().cpu().numpy()
+        q = case.q[s:s + 1].double().cpu().numpy()
+        kn = k_new[s:s + 1].float().cpu().numpy()
+        vn = v_new[s:s + 1].float().cpu().numpy()
+        # the sequence's blocks, relabelled 0..nb-1 in table order
+        phys, off = divmod(int(slots[s]), B)
+        local_slot = np.array([int(np.nonzero(tables[s, :nb] == phys)[0][0]) * B + off])
+        t0 = time.perf_counter()
+        kc2, vc2 = oracle.kv_append(kn, vn, kc, vc, local_slot)
+        oracle.paged_decode_attention(q, kc2.astype(np.float64), vc2.astype(np.float64),
+                                      np.arange(nb)[None, :], [int(lens[s])], case.scale)
+        t_total += time.perf_counter() - t0
+        done += 1
+        nbytes += int(lens[s]) * 2 * Hkv * D * e + 2 * Hq * D * e + 4 * Hkv * D * e
+    return nbytes / t_total / 1e9, done, t_total
+
+
+def cores_used():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+# ------------------------------------------------------------------ arms --
+
+def run_reference(args, rank, world):
+    """The oracle timed on host cores as the reference arm (rank 0 only)."""
+    if rank != 0:
+        return
+    from paged_kv_cache_247_gb300 import workloads as W
+    case, k_new, v_new, slots, desc, label = make_workload(args.workload, "cpu")
+    per_step = max(0.5, min(6.0, 150.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        oracle_sample_rate(case, k_new, v_new, slots, per_step / 4, max_seqs=1)
+    total_bytes_t, seqs, elapsed = 0.0, 0, 0.0
+    rates = []
+    for _ in range(args.steps):
+        rate, n, t = oracle_sample_rate(case, k_new, v_new, slots, per_step)
+        rates.append(rate)
+        total_bytes_t += rate * t
+        seqs += n
+        elapsed += t
+    value = total_bytes_t / elapsed
+    S = case.q.shape[0]
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * elapsed / args.steps, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": label, "num_seqs": S, "sample": "whole sequences, random order"},
+        "decode_seqs_per_s": round(seqs / elapsed, 3),
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores_used(),
+                         "kind": "oracle",
+                         "sample": f"{seqs} sequences of the workload (append + decode), "
+                                   f"~{per_step:.1f} s per step"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, rank, world, local_rank):
+    import paged_kv_cache_247_gb300 as pkv
+    from paged_kv_cache_247_gb300 import build as _build
+    if rank == 0 or not os.path.exists(_build.LIB):
+        _build.build_library()
+    if world > 1:
+        torch.distributed.barrier()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    case, k_new, v_new, slots, desc, label = make_workload(args.workload, dev)
+    S, Hq, D = case.q.shape
+    Hkv = case.k_cache.shape[1]
+    out = torch.empty_like(case.q)
+    ws_bytes = pkv.decode_workspace_size(S, Hq, Hkv, D, case.max_context_len, args.partition)
+    workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+    part = args.partition or pkv.decode_partition_size(S, Hq, Hkv, D, case.max_context_len)
+    split = -(-case.max_context_len // part) > 1
+    launches_per_step = 2 + (1 if split else 0)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        pkv.kv_append(k_new, v_new, case.k_cache, case.v_cache, slots)
+        pkv.paged_attn_decode(out, case.q, case.k_cache, case.v_cache, case.block_tables,
+                              case.context_lens, case.scale, case.max_context_len,
+                              partition_size=args.partition, workspace=workspace)
+
+    pkv.device_status(clear=True)
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(dev.index if dev.index is not None else 0)
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(K)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)  # let the sampler start before the timed region
+    start.record(stream)
+    for i in range(K):
+        pkv.kv_append(k_new, v_new, case.k_cache, case.v_cache, slots)
+        ev[i][0].record(stream)
+        pkv.paged_attn_decode(out, case.q, case.k_cache, case.v_cache, case.block_tables,
+                              case.context_lens, case.scale, case.max_context_len,
+                              partition_size=args.partition, workspace=workspace)
+        ev[i][1].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    clock_rec = clocks.stop()
+    if world > 1:
+        torch.distributed.barrier()
+    elapsed_ms = start.elapsed_time(end)
+    decode_ms = [a.elapsed_time(b) for a, b in ev]
+    flags = pkv.device_status(clear=True)
+    if flags:
+        raise RuntimeError(f"device status flags {flags} during the bench")
+
+    t = torch.tensor([elapsed_ms], dtype=torch.float64)
+    if world > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    elapsed_ms = float(t.item())
+
+    # End to end through the C ABI with host buffers: every step copies its
+    # inputs (q, new K/V, slots, tables, lengths) from pinned host memory and
+    # reads the output back.
+    host = {n: x.cpu().pin_memory() for n, x in (("q", case.q), ("k", k_new), ("v", v_new),
+                                                  ("slots", slots), ("tables", case.block_tables),
+                                                  ("lens", case.context_lens))}
+    out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    dev_in = {n: torch.empty_like(x, device=dev) for n, x in host.items()}
+    h2d = sum(x.numel() * x.element_size() for x in host.values())
+    d2h = out_host.numel() * out_host.element_size()
+    K_e2e = max(10, K // 4)
+
+    def e2e_step():
+        for n, x in host.items():
+            dev_in[n].copy_(x, non_blocking=True)
+        pkv.kv_append(dev_in["k"], dev_in["v"], case.k_cache, case.v_cache, dev_in["slots"])
+        pkv.paged_attn_decode(out, dev_in["q"], case.k_cache, case.v_cache, dev_in["tables"],
+                              dev_in["lens"], case.scale, case.max_context_len,
+                              partition_size=args.partition, workspace=workspace)
+        out_host.copy_(out, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(K_e2e):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / K_e2e
+
+    decode_b, append_b = step_bytes(case)
+    ms_step = elapsed_ms / K
+    value = (decode_b + append_b) * world / (ms_step * 1e-3) / 1e9
+    peak, peak_kind = peak_hbm()
+    dec_ms = float(np.mean(decode_ms))
+    achieved = decode_b / (dec_ms * 1e-3) / 1e9
+    traffic = ncu_traffic("paged_decode_kernel", args.workload)
+
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp16"
+        if case.q.dtype == torch.float16 else "bf16", "data": "synthetic",
+        "config": {"workload": label, "num_seqs": S, "num_q_heads": Hq, "num_kv_heads": Hkv,
+                   "head_dim": D, "block_size": case.block_size,
+                   "context_tokens": int(case.context_lens.sum().item()),
+                   "max_context_len": case.max_context_len, "partition_size": part,
+                   "split": split, "l2": f"inputs larger than L2: {decode_b / 1e9:.2f} GB of "
+                   "K/V per step vs 129 MB L2, no flush", "parallelism": f"replicas x{world}"},
+        "pct_of_peak": round(100.0 * value / world / peak, 2),
+        "decode_seqs_per_s": round(S * world / (ms_step * 1e-3), 1),
+        "roofline": {"kernel": "paged_attn_decode call (decode kernel"
+                     + (" + split reduction)" if split else ")"),
+                     "bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
+                     "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
+                     if peak_kind == "measured" else "fallback",
+                     "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "algorithmic_bytes_per_launch": decode_b,
+                     "avg_launch_ms": round(dec_ms, 5)},
+        "e2e": {"value": round((decode_b + append_b) * world / (e2e_ms * 1e-3) / 1e9, 2),
+                "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": round(e2e_ms, 5)},
+        "gpu_launches": K * launches_per_step,
+        "clocks": clock_rec,
+    }
+    if rank == 0 and world == 1:
+        rate, n, secs = oracle_sample_rate(case, k_new, v_new, slots, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": round(rate, 4), "unit": "GB/s", "cores": cores_used(),
+                                "kind": "oracle",
+                                "sample": f"{n} whole sequences of this workload (append + decode "
+                                          f"in fp64), {secs:.1f} s"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        torch.distributed.init_process_group("gloo")
+    try:
+        if args.impl == "reference":
+            run_reference(args, rank, world)
+        else:
+            run_ours(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

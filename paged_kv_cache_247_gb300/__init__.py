@@ -1,0 +1,24 @@
+"""Paged KV-cache decode for GB300 (sm_103a): the hot path of PagedAttention.
+
+Device calls (hand-written CUDA behind the C ABI of ``libpagedkv.so``):
+
+* :func:`paged_attn_decode` — single-query decode attention walking each
+  sequence's block table, with split-context partitions and GQA grouping;
+* :func:`kv_append` — scatter of each step's new K/V into its slot;
+* :func:`block_copy` — block-granular copy-on-write.
+
+Host: :class:`BlockAllocator`, the refcounted block allocator that decides
+slots and copy-on-write pairs.  The library is loaded on first use and there
+is no fallback: a missing library raises.
+"""
+
+from ._lib import PagedKVError, load as load_library  # noqa: F401
+from .ops import (  # noqa: F401
+    paged_attn_decode,
+    kv_append,
+    block_copy,
+    device_status,
+    decode_workspace_size,
+    decode_partition_size,
+)
+from .allocator import BlockAllocator, OutOfBlocks  # noqa: F401

@@ -1,0 +1,271 @@
+// The C ABI: argument checks, launch planning, and the device status word.
+// Nothing here allocates device memory.
+
+#include <cuda_runtime.h>
+
+#include <math.h>
+#include <mutex>
+
+#include "kernels.h"
+#include "pagedkv.h"
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int kDefaultPartition = 512;  // tokens per split-context partition
+constexpr int kPartitionQuantum = 32;   // partitions are whole pipeline stages
+
+// Sticky per-device record of problems the kernels saw (PKV_DEV_* bits).
+__device__ unsigned int g_device_status;
+
+thread_local int g_last_cuda_error = 0;
+
+std::mutex g_mutex;
+unsigned int* g_status_ptr[kMaxDevices] = {};
+int g_sm_count[kMaxDevices] = {};
+
+pkv_status_t cuda_fail(cudaError_t err) {
+  g_last_cuda_error = static_cast<int>(err);
+  return PKV_ERR_CUDA;
+}
+
+// Device address of the status word on the current device (host code may not
+// take the symbol's address directly: that is a host-side shadow).
+cudaError_t status_word(unsigned int** out) {
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  if (!g_status_ptr[dev]) {
+    void* p = nullptr;
+    err = cudaGetSymbolAddress(&p, g_device_status);
+    if (err != cudaSuccess) return err;
+    g_status_ptr[dev] = static_cast<unsigned int*>(p);
+  }
+  *out = g_status_ptr[dev];
+  return cudaSuccess;
+}
+
+[[maybe_unused]] int sm_count() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  if (!g_sm_count[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    g_sm_count[dev] = n;
+  }
+  return g_sm_count[dev];
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool supported_block_size(int b) { return b == 8 || b == 16 || b == 32 || b == 64 || b == 128; }
+
+int log2_int(int x) {
+  int r = 0;
+  while ((1 << r) < x) ++r;
+  return r;
+}
+
+bool decode_shape_ok(int num_seqs, int num_q_heads, int num_kv_heads, int max_context_len) {
+  return num_seqs >= 0 && num_q_heads > 0 && num_kv_heads > 0 &&
+         num_q_heads % num_kv_heads == 0 && max_context_len >= 0;
+}
+
+int round_partition(int tokens) {
+  const int t = tokens < 1 ? 1 : tokens;
+  return ((t + kPartitionQuantum - 1) / kPartitionQuantum) * kPartitionQuantum;
+}
+
+int auto_partition(int max_context_len) {
+  // Contexts up to one partition run unsplit; longer ones are cut into
+  // fixed partitions so that every CTA streams a bounded, similar amount of
+  // K/V (even for a batch of one) and a reduction merges them.
+  if (max_context_len <= kDefaultPartition) return round_partition(max_context_len);
+  return kDefaultPartition;
+}
+
+long long num_parts_for(int max_context_len, int partition) {
+  if (max_context_len <= 0) return 1;
+  return (max_context_len + (long long)partition - 1) / partition;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* pkv_status_string(pkv_status_t status) {
+  switch (status) {
+    case PKV_OK: return "ok";
+    case PKV_ERR_INVALID_ARG: return "invalid argument";
+    case PKV_ERR_UNSUPPORTED: return "unsupported configuration";
+    case PKV_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case PKV_ERR_OUT_OF_BLOCKS: return "out of blocks";
+    case PKV_ERR_CUDA: return "CUDA error";
+    case PKV_ERR_UNKNOWN_SEQ: return "unknown sequence";
+    case PKV_ERR_SEQ_EXISTS: return "sequence exists";
+    case PKV_ERR_TABLE_TOO_SMALL: return "block table row too small";
+  }
+  return "unknown status";
+}
+
+int pkv_last_cuda_error(void) { return g_last_cuda_error; }
+
+int pkv_version(void) { return 1; }
+
+int pkv_decode_partition_size(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                              int max_context_len) {
+  if (!decode_shape_ok(num_seqs, num_q_heads, num_kv_heads, max_context_len)) return -1;
+  if (head_dim != 64 && head_dim != 128) return -1;
+  return auto_partition(max_context_len);
+}
+
+size_t pkv_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                 int max_context_len, int partition_size) {
+  if (!decode_shape_ok(num_seqs, num_q_heads, num_kv_heads, max_context_len)) return (size_t)-1;
+  if (head_dim != 64 && head_dim != 128) return (size_t)-1;
+  if (partition_size < 0 || partition_size % kPartitionQuantum) return (size_t)-1;
+  const int part = partition_size ? partition_size : auto_partition(max_context_len);
+  const long long parts = num_parts_for(max_context_len, part);
+  if (parts <= 1) return 0;
+  return (size_t)num_seqs * num_q_heads * parts * (head_dim + 2) * sizeof(float);
+}
+
+pkv_status_t pkv_paged_attn_decode(void* out, const void* q, const void* k_cache,
+                                   const void* v_cache, const int32_t* block_tables,
+                                   int max_blocks_per_seq, const int32_t* context_lens,
+                                   int max_context_len, int num_seqs, int num_q_heads,
+                                   int num_kv_heads, int head_dim, int block_size,
+                                   int num_blocks, float scale, pkv_dtype_t dtype,
+                                   int partition_size, void* workspace, size_t workspace_bytes,
+                                   pkv_stream_t stream) {
+  if (!decode_shape_ok(num_seqs, num_q_heads, num_kv_heads, max_context_len))
+    return PKV_ERR_INVALID_ARG;
+  if (dtype != PKV_F16 && dtype != PKV_BF16) return PKV_ERR_INVALID_ARG;
+  if (partition_size < 0 || partition_size % kPartitionQuantum) return PKV_ERR_INVALID_ARG;
+  if (!isfinite(scale)) return PKV_ERR_INVALID_ARG;
+  if (head_dim != 64 && head_dim != 128) return PKV_ERR_UNSUPPORTED;
+  if (!supported_block_size(block_size)) return PKV_ERR_UNSUPPORTED;
+  if (num_seqs == 0) return PKV_OK;
+  if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens)
+    return PKV_ERR_INVALID_ARG;
+  if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
+    return PKV_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(block_tables) | reinterpret_cast<uintptr_t>(context_lens)) & 3u)
+    return PKV_ERR_INVALID_ARG;
+  if (max_blocks_per_seq <= 0 || num_blocks <= 0) return PKV_ERR_INVALID_ARG;
+  if ((long long)max_blocks_per_seq * block_size < max_context_len) return PKV_ERR_INVALID_ARG;
+
+  const int group = num_q_heads / num_kv_heads;
+  const int gt = pkv::decode_heads_per_cta(group);
+  const int head_chunks = (group + gt - 1) / gt;
+  const int part = partition_size ? partition_size : auto_partition(max_context_len);
+  const long long parts = num_parts_for(max_context_len, part);
+  if (num_seqs > 65535 || (long long)num_kv_heads * head_chunks > 65535 || parts > 0x7fffffffLL)
+    return PKV_ERR_UNSUPPORTED;
+  if ((long long)num_seqs * num_q_heads > 0x7fffffffLL) return PKV_ERR_UNSUPPORTED;
+
+  pkv::DecodeParams p{};
+  p.out = out;
+  p.q = q;
+  p.k_cache = k_cache;
+  p.v_cache = v_cache;
+  p.block_tables = block_tables;
+  p.context_lens = context_lens;
+  p.max_blocks_per_seq = max_blocks_per_seq;
+  p.max_context_len = max_context_len;
+  p.num_seqs = num_seqs;
+  p.num_q_heads = num_q_heads;
+  p.num_kv_heads = num_kv_heads;
+  p.group = group;
+  p.head_chunks = head_chunks;
+  p.block_size = block_size;
+  p.log2_block = log2_int(block_size);
+  p.num_blocks = num_blocks;
+  p.partition_size = part;
+  p.num_parts = (int)parts;
+  p.qscale = scale * 1.4426950408889634f;  // log2(e): softmax is evaluated with exp2
+  if (parts > 1) {
+    const size_t need = (size_t)num_seqs * num_q_heads * parts * (head_dim + 2) * sizeof(float);
+    if (!workspace || workspace_bytes < need) return PKV_ERR_WORKSPACE_TOO_SMALL;
+    if (!aligned16(workspace)) return PKV_ERR_INVALID_ARG;
+    float* ws = static_cast<float*>(workspace);
+    const size_t rows = (size_t)num_seqs * num_q_heads * parts;
+    p.ws_o = ws;
+    p.ws_m = ws + rows * head_dim;
+    p.ws_l = p.ws_m + rows;
+  }
+  cudaError_t err = status_word(&p.status);
+  if (err != cudaSuccess) return cuda_fail(err);
+  err = pkv::launch_paged_decode(p, dtype, head_dim, gt, reinterpret_cast<cudaStream_t>(stream));
+  if (err != cudaSuccess) return cuda_fail(err);
+  return PKV_OK;
+}
+
+pkv_status_t pkv_kv_append(const void* k, const void* v, void* k_cache, void* v_cache,
+                           const int64_t* slot_mapping, int num_tokens, int num_kv_heads,
+                           int head_dim, int block_size, int num_blocks, pkv_dtype_t dtype,
+                           pkv_stream_t stream) {
+  if (num_tokens < 0 || num_kv_heads <= 0 || num_blocks <= 0) return PKV_ERR_INVALID_ARG;
+  if (dtype != PKV_F16 && dtype != PKV_BF16) return PKV_ERR_INVALID_ARG;
+  if (head_dim != 64 && head_dim != 128) return PKV_ERR_UNSUPPORTED;
+  if (!supported_block_size(block_size)) return PKV_ERR_UNSUPPORTED;
+  if (num_tokens == 0) return PKV_OK;
+  if (!k || !v || !k_cache || !v_cache || !slot_mapping) return PKV_ERR_INVALID_ARG;
+  if (!aligned16(k) || !aligned16(v) || !aligned16(k_cache) || !aligned16(v_cache))
+    return PKV_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(slot_mapping) & 7u) return PKV_ERR_INVALID_ARG;
+  if ((long long)num_kv_heads * head_dim * 2 / 16 > 0x7fffffffLL) return PKV_ERR_UNSUPPORTED;
+  unsigned int* status = nullptr;
+  cudaError_t err = status_word(&status);
+  if (err != cudaSuccess) return cuda_fail(err);
+  err = pkv::launch_kv_append(k, v, k_cache, v_cache, slot_mapping, num_tokens, num_kv_heads,
+                              head_dim, block_size, num_blocks, status,
+                              reinterpret_cast<cudaStream_t>(stream));
+  if (err != cudaSuccess) return cuda_fail(err);
+  return PKV_OK;
+}
+
+pkv_status_t pkv_block_copy(void* k_cache, void* v_cache, const int64_t* src_dst_pairs,
+                            int num_pairs, int num_blocks, size_t block_bytes,
+                            pkv_stream_t stream) {
+  if (num_pairs < 0 || num_blocks <= 0 || block_bytes == 0 || block_bytes % 16)
+    return PKV_ERR_INVALID_ARG;
+  if (num_pairs == 0) return PKV_OK;
+  if (!k_cache || !v_cache || !src_dst_pairs) return PKV_ERR_INVALID_ARG;
+  if (!aligned16(k_cache) || !aligned16(v_cache)) return PKV_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(src_dst_pairs) & 7u) return PKV_ERR_INVALID_ARG;
+  unsigned int* status = nullptr;
+  cudaError_t err = status_word(&status);
+  if (err != cudaSuccess) return cuda_fail(err);
+  err = pkv::launch_block_copy(k_cache, v_cache, src_dst_pairs, num_pairs, num_blocks,
+                               block_bytes, status, reinterpret_cast<cudaStream_t>(stream));
+  if (err != cudaSuccess) return cuda_fail(err);
+  return PKV_OK;
+}
+
+pkv_status_t pkv_device_status(uint32_t* flags, int clear, pkv_stream_t stream) {
+  unsigned int* status = nullptr;
+  cudaError_t err = status_word(&status);
+  if (err != cudaSuccess) return cuda_fail(err);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  err = cudaStreamSynchronize(st);
+  if (err != cudaSuccess) return cuda_fail(err);
+  if (flags) {
+    unsigned int host = 0;
+    err = cudaMemcpyAsync(&host, status, sizeof(host), cudaMemcpyDeviceToHost, st);
+    if (err == cudaSuccess) err = cudaStreamSynchronize(st);
+    if (err != cudaSuccess) return cuda_fail(err);
+    *flags = host;
+  }
+  if (clear) {
+    err = cudaMemsetAsync(status, 0, sizeof(unsigned int), st);
+    if (err == cudaSuccess) err = cudaStreamSynchronize(st);
+    if (err != cudaSuccess) return cuda_fail(err);
+  }
+  return PKV_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,494 @@
+// Paged single-query decode attention for sm_103a.
+//
+// What it computes ("Only 20.4% of your KV cache held actual tokens", section
+// "The page table, relocated into attention"): for each sequence and query
+// head, softmax(scale * q . K) V over the sequence's context, with K and V
+// gathered block by block through the sequence's block table.
+//
+// One CTA owns (sequence s, KV head, partition of the context) and computes
+// every query head of the KV head's group, so each K/V block is read from HBM
+// once per group.  Five warps:
+//
+//   warp 4      producer: keeps the partition's physical block ids in shared
+//               memory (the table walker) and streams K and V into a ring of
+//               NSTAGE stages of 32 tokens with bulk asynchronous copies
+//               (cp.async.bulk, the 1-D TMA path), one copy per contiguous
+//               (block, head) run, completing on an mbarrier per stage.
+//   warps 0-3   consumers: each takes 8 of a stage's 32 rows.  Eight lanes
+//               share one row (16 bytes each per 64 columns), so a group of
+//               8 lanes reads 128 contiguous bytes per load; logits of the
+//               warp's rows are summed with a transposed butterfly over the
+//               8 lanes, then an online softmax (running max and sum in base
+//               2, fp32) updates the warp's accumulator of p * V.
+//
+// At the end the four warps' (max, sum, accumulator) triples are merged in
+// shared memory.  A partition that is the whole context writes the output
+// directly; otherwise it writes a normalised partial output with its max and
+// sum, and a second kernel merges the partitions (split context,
+// flash-decoding style).
+//
+// HBM traffic is the K and V bytes of the context plus q, the table and the
+// output: the kernel is bandwidth-bound; the copy engine keeps up to NSTAGE x
+// 16 KiB in flight per CTA.
+
+#include <math_constants.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace pkv {
+namespace {
+
+constexpr int kTokStage = 32;       // tokens per pipeline stage
+constexpr int kConsumerWarps = 4;   // warps doing arithmetic
+constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kTbl = 128;           // block ids held in shared memory at once
+constexpr unsigned kFull = 0xffffffffu;
+
+template <int D>
+constexpr int stages_for() { return D >= 128 ? 4 : 8; }
+
+template <typename T, int D, int GT>
+struct SmemLayout {
+  static constexpr int kStages = stages_for<D>();
+  static constexpr size_t kStageElems = (size_t)kTokStage * D;
+  static constexpr size_t kRing = kStages * kStageElems * sizeof(T);        // one of K, V
+  static constexpr size_t kMergeAcc = (size_t)kConsumerWarps * GT * D * 4;   // floats
+  static constexpr size_t kMergeMl = (size_t)kConsumerWarps * GT * 4;
+  static constexpr size_t kTable = kTbl * 4;
+  static constexpr size_t kBars = 2 * kStages * 8;
+  static constexpr size_t kBytes = 2 * kRing + kMergeAcc + 2 * kMergeMl + kTable + kBars;
+};
+
+template <typename T, int D, int GT>
+__global__ void __launch_bounds__(kThreads, GT >= 4 ? 2 : 3)
+    paged_decode_kernel(const DecodeParams p) {
+  using L = SmemLayout<T, D, GT>;
+  constexpr int NSTAGE = L::kStages;
+  constexpr int NCH = D / 64;           // 16-byte chunks per lane per row
+  constexpr int NF2 = D / 16;           // float2 per lane per row (= 4 * NCH)
+  constexpr int NV = 2 * GT;            // logits per lane before the reduction
+  constexpr int LB = NV == 2 ? 1 : (NV == 4 ? 2 : 3);
+  constexpr int SH = 3 - LB;            // lane-bit shift of a reduced logit index
+  constexpr int kTokMask = 1 << SH;     // lane bit separating the two row passes
+
+  extern __shared__ __align__(128) unsigned char smem[];
+  T* Ks = reinterpret_cast<T*>(smem);
+  T* Vs = Ks + NSTAGE * L::kStageElems;
+  float* mg_acc = reinterpret_cast<float*>(Vs + NSTAGE * L::kStageElems);
+  float* mg_max = mg_acc + kConsumerWarps * GT * D;
+  float* mg_sum = mg_max + kConsumerWarps * GT;
+  int* tbl = reinterpret_cast<int*>(mg_sum + kConsumerWarps * GT);
+  uint64_t* full = reinterpret_cast<uint64_t*>(tbl + kTbl);
+  uint64_t* empty = full + NSTAGE;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int part = blockIdx.x;
+  const int kvh = blockIdx.y / p.head_chunks;
+  const int hc = blockIdx.y - kvh * p.head_chunks;
+  const int s = blockIdx.z;
+  const int h0 = kvh * p.group + hc * GT;
+  const int nh = min(GT, p.group - hc * GT);
+
+  int ctx = p.context_lens[s];
+  const long long cap_ll = min((long long)p.max_context_len,
+                               (long long)p.max_blocks_per_seq * p.block_size);
+  const int ctx_cap = (int)cap_ll;
+  if (ctx < 0 || ctx > ctx_cap) {
+    if (threadIdx.x == 0 && part == 0) atomicOr(p.status, PKV_DEV_BAD_CONTEXT_LEN);
+    ctx = ctx < 0 ? 0 : ctx_cap;
+  }
+  const int t_begin = part * p.partition_size;
+  const int t_end = min(ctx, t_begin + p.partition_size);
+  const int nparts_seq = (ctx + p.partition_size - 1) / p.partition_size;
+  if (t_begin >= t_end) {
+    if (ctx == 0 && part == 0) {  // empty context: the output is zero
+      uint16_t* o = reinterpret_cast<uint16_t*>(p.out) + ((size_t)s * p.num_q_heads + h0) * D;
+      for (int i = threadIdx.x; i < nh * D; i += kThreads) o[i] = 0;
+    }
+    return;
+  }
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < NSTAGE; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], kConsumerWarps);
+    }
+    fence_barrier_init();
+  }
+  __syncthreads();
+  const int nstages = (t_end - t_begin + kTokStage - 1) / kTokStage;
+
+  // ------------------------------------------------------------ producer --
+  if (warp == kConsumerWarps) {
+    const uint64_t policy = policy_evict_first();
+    const int log2B = p.log2_block;
+    const int lb_last = (t_end - 1) >> log2B;
+    const int32_t* trow = p.block_tables + (size_t)s * p.max_blocks_per_seq;
+    const T* kbase = static_cast<const T*>(p.k_cache);
+    const T* vbase = static_cast<const T*>(p.v_cache);
+    const size_t tile = (size_t)p.block_size * D;  // elements of one (block, head) tile
+    int chunk_base = -1;
+    for (int it = 0; it < nstages; ++it) {
+      const int stg = it % NSTAGE;
+      if (it >= NSTAGE && !mbar_wait_warp(&empty[stg], ((it / NSTAGE) - 1) & 1, p.status)) break;
+      const int tok0 = t_begin + it * kTokStage;
+      const int ntok = min(kTokStage, t_end - tok0);
+      const int lb0 = tok0 >> log2B;
+      const int lb1 = (tok0 + ntok - 1) >> log2B;
+      if (chunk_base < 0 || lb1 >= chunk_base + kTbl) {
+        // Walk the next window of the block table into shared memory.
+        __syncwarp();
+        chunk_base = lb0;
+        for (int i = lane; i < kTbl; i += 32) {
+          const int lb = chunk_base + i;
+          int id = 0;
+          if (lb <= lb_last) {
+            id = __ldg(trow + lb);
+            if ((unsigned)id >= (unsigned)p.num_blocks) {
+              atomicOr(p.status, PKV_DEV_BAD_BLOCK_ID);
+              id = 0;
+            }
+          }
+          tbl[i] = id;
+        }
+        __syncwarp();
+      }
+      if (lane == 0) mbar_arrive_expect_tx(&full[stg], (uint32_t)ntok * D * sizeof(T) * 2);
+      __syncwarp();
+      // One copy per block the stage touches; rows past the context are not
+      // copied, so positions beyond context_lens are never read.
+      if (lane <= lb1 - lb0) {
+        const int lb = lb0 + lane;
+        const int seg0 = max(tok0, lb << log2B);
+        const int seg1 = min(tok0 + ntok, (lb + 1) << log2B);
+        const size_t off = ((size_t)tbl[lb - chunk_base] * p.num_kv_heads + kvh) * tile +
+                           (size_t)(seg0 - (lb << log2B)) * D;
+        const uint32_t bytes = (uint32_t)(seg1 - seg0) * D * sizeof(T);
+        const int row = seg0 - tok0;
+        bulk_load(Ks + stg * L::kStageElems + row * D, kbase + off, bytes, &full[stg], policy);
+        bulk_load(Vs + stg * L::kStageElems + row * D, vbase + off, bytes, &full[stg], policy);
+      }
+    }
+    return;
+  }
+
+  // ----------------------------------------------------------- consumers --
+  const int grp = lane >> 3;  // which of the 4 rows of a pass this lane reads
+  const int gi = lane & 7;    // position inside the 8-lane row group
+
+  // q for this lane's columns {8*(gi + 8c) .. +7}, pre-scaled to base-2 logits.
+  float2 qf[GT][NF2];
+  {
+    const T* qrow = static_cast<const T*>(p.q) + ((size_t)s * p.num_q_heads + h0) * D;
+    const float2 sc = make_float2(p.qscale, p.qscale);
+#pragma unroll
+    for (int g = 0; g < GT; ++g) {
+#pragma unroll
+      for (int c = 0; c < NCH; ++c) {
+        uint4 w = make_uint4(0, 0, 0, 0);
+        if (g < nh) w = *reinterpret_cast<const uint4*>(qrow + g * D + (gi + 8 * c) * 8);
+        qf[g][4 * c + 0] = __fmul2_rn(Cvt<T>::to_float2(w.x), sc);
+        qf[g][4 * c + 1] = __fmul2_rn(Cvt<T>::to_float2(w.y), sc);
+        qf[g][4 * c + 2] = __fmul2_rn(Cvt<T>::to_float2(w.z), sc);
+        qf[g][4 * c + 3] = __fmul2_rn(Cvt<T>::to_float2(w.w), sc);
+      }
+    }
+  }
+
+  float2 acc[GT][NF2];
+#pragma unroll
+  for (int g = 0; g < GT; ++g)
+#pragma unroll
+    for (int e = 0; e < NF2; ++e) acc[g][e] = make_float2(0.f, 0.f);
+  float m_run = -CUDART_INF_F;  // running max of this lane's head (base 2)
+  float l_run = 0.f;            // running sum of exp2(logit - m_run)
+
+  const int idx_l = gi >> SH;  // (g * 2 + j) of the logit this lane ends up with
+  const int g_l = idx_l >> 1;
+  const int j_l = idx_l & 1;
+
+  for (int it = 0; it < nstages; ++it) {
+    const int stg = it % NSTAGE;
+    if (!mbar_wait_warp(&full[stg], (it / NSTAGE) & 1, p.status)) break;
+    const int ntok = min(kTokStage, t_end - (t_begin + it * kTokStage));
+    const T* Kst = Ks + stg * L::kStageElems;
+    const T* Vst = Vs + stg * L::kStageElems;
+
+    // Partial dot products: this lane's 16 (D=128) or 8 (D=64) columns of
+    // rows warp*8 + j*4 + grp, for every head of the group.
+    float v[NV];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int row = warp * 8 + j * 4 + grp;
+      float2 kf[NF2];
+#pragma unroll
+      for (int c = 0; c < NCH; ++c) {
+        const uint4 w = *reinterpret_cast<const uint4*>(Kst + row * D + (gi + 8 * c) * 8);
+        kf[4 * c + 0] = Cvt<T>::to_float2(w.x);
+        kf[4 * c + 1] = Cvt<T>::to_float2(w.y);
+        kf[4 * c + 2] = Cvt<T>::to_float2(w.z);
+        kf[4 * c + 3] = Cvt<T>::to_float2(w.w);
+      }
+#pragma unroll
+      for (int g = 0; g < GT; ++g) {
+        float2 a = __fmul2_rn(qf[g][0], kf[0]);
+#pragma unroll
+        for (int e = 1; e < NF2; ++e) a = __ffma2_rn(qf[g][e], kf[e], a);
+        v[g * 2 + j] = a.x + a.y;
+      }
+    }
+    // Transposed butterfly over the group's 8 lanes: each exchange halves the
+    // values a lane holds, so NV sums cost NV - 1 shuffles instead of 3 * NV.
+#pragma unroll
+    for (int step = 0; step < LB; ++step) {
+      const int mk = 4 >> step;
+      const bool upper = (gi & mk) != 0;
+      const int half = NV >> (step + 1);
+#pragma unroll
+      for (int i = 0; i < half; ++i) {
+        const float send = upper ? v[i] : v[i + half];
+        const float keep = upper ? v[i + half] : v[i];
+        v[i] = keep + __shfl_xor_sync(kFull, send, mk);
+      }
+    }
+    float x = v[0];
+#pragma unroll
+    for (int mk = (4 >> LB); mk >= 1; mk >>= 1) x += __shfl_xor_sync(kFull, x, mk);
+
+    // Online softmax over the warp's 8 rows of this stage.
+    if (warp * 8 + j_l * 4 + grp >= ntok) x = -CUDART_INF_F;
+    float mt = fmaxf(x, __shfl_xor_sync(kFull, x, kTokMask));
+    mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 8));
+    mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 16));
+    const float m_new = fmaxf(m_run, mt);
+    const float alpha = (m_new == -CUDART_INF_F) ? 1.f : exp2f(m_run - m_new);
+    const float pe = (x == -CUDART_INF_F) ? 0.f : exp2f(x - m_new);
+    float ps = pe + __shfl_xor_sync(kFull, pe, kTokMask);
+    ps += __shfl_xor_sync(kFull, ps, 8);
+    ps += __shfl_xor_sync(kFull, ps, 16);
+    l_run = l_run * alpha + ps;
+    m_run = m_new;
+    if (__any_sync(kFull, alpha != 1.f)) {
+#pragma unroll
+      for (int g = 0; g < GT; ++g) {
+        const float a = __shfl_sync(kFull, alpha, (g * 2) << SH);
+        const float2 a2 = make_float2(a, a);
+#pragma unroll
+        for (int e = 0; e < NF2; ++e) acc[g][e] = __fmul2_rn(acc[g][e], a2);
+      }
+    }
+
+    // acc += p * V for this lane's row of each pass.
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int row = warp * 8 + j * 4 + grp;
+      float pg[GT];
+#pragma unroll
+      for (int g = 0; g < GT; ++g) pg[g] = __shfl_sync(kFull, pe, (grp << 3) | ((g * 2 + j) << SH));
+      if (row < ntok) {
+        float2 vf[NF2];
+#pragma unroll
+        for (int c = 0; c < NCH; ++c) {
+          const uint4 w = *reinterpret_cast<const uint4*>(Vst + row * D + (gi + 8 * c) * 8);
+          vf[4 * c + 0] = Cvt<T>::to_float2(w.x);
+          vf[4 * c + 1] = Cvt<T>::to_float2(w.y);
+          vf[4 * c + 2] = Cvt<T>::to_float2(w.z);
+          vf[4 * c + 3] = Cvt<T>::to_float2(w.w);
+        }
+#pragma unroll
+        for (int g = 0; g < GT; ++g) {
+          const float2 pp = make_float2(pg[g], pg[g]);
+#pragma unroll
+          for (int e = 0; e < NF2; ++e) acc[g][e] = __ffma2_rn(pp, vf[e], acc[g][e]);
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[stg]);
+  }
+
+  // The four row groups of a warp share its running max: add their sums.
+#pragma unroll
+  for (int g = 0; g < GT; ++g)
+#pragma unroll
+    for (int e = 0; e < NF2; ++e) {
+      float2 a = acc[g][e];
+      a.x += __shfl_xor_sync(kFull, a.x, 8);
+      a.y += __shfl_xor_sync(kFull, a.y, 8);
+      a.x += __shfl_xor_sync(kFull, a.x, 16);
+      a.y += __shfl_xor_sync(kFull, a.y, 16);
+      acc[g][e] = a;
+    }
+  if (grp == 0) {
+#pragma unroll
+    for (int g = 0; g < GT; ++g)
+#pragma unroll
+      for (int c = 0; c < NCH; ++c) {
+        float4* dst = reinterpret_cast<float4*>(mg_acc + (warp * GT + g) * D + (gi + 8 * c) * 8);
+        dst[0] = make_float4(acc[g][4 * c].x, acc[g][4 * c].y, acc[g][4 * c + 1].x, acc[g][4 * c + 1].y);
+        dst[1] = make_float4(acc[g][4 * c + 2].x, acc[g][4 * c + 2].y, acc[g][4 * c + 3].x,
+                             acc[g][4 * c + 3].y);
+      }
+    if (j_l == 0 && (gi & (kTokMask - 1)) == 0) {
+      mg_max[warp * GT + g_l] = m_run;
+      mg_sum[warp * GT + g_l] = l_run;
+    }
+  }
+  named_barrier_sync(1, kConsumerWarps * 32);
+
+  // Merge the warps and write out (or the partition's partial result).
+  for (int e0 = threadIdx.x * 4; e0 < nh * D; e0 += kConsumerWarps * 32 * 4) {
+    const int g = e0 / D;
+    const int e = e0 - g * D;
+    float M = -CUDART_INF_F;
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, mg_max[w * GT + g]);
+    float Lsum = 0.f;
+    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; ++w) {
+      const float mw = mg_max[w * GT + g];
+      const float sc = (mw == -CUDART_INF_F) ? 0.f : exp2f(mw - M);
+      Lsum += mg_sum[w * GT + g] * sc;
+      const float4 a = *reinterpret_cast<const float4*>(mg_acc + (w * GT + g) * D + e);
+      o.x += a.x * sc;
+      o.y += a.y * sc;
+      o.z += a.z * sc;
+      o.w += a.w * sc;
+    }
+    const float inv = 1.f / Lsum;
+    if (nparts_seq == 1) {
+      T* orow = static_cast<T*>(p.out) + ((size_t)s * p.num_q_heads + h0 + g) * D + e;
+      uint2 pk;
+      pk.x = Cvt<T>::from_float2(o.x * inv, o.y * inv);
+      pk.y = Cvt<T>::from_float2(o.z * inv, o.w * inv);
+      *reinterpret_cast<uint2*>(orow) = pk;
+    } else {
+      const size_t r = ((size_t)s * p.num_q_heads + h0 + g) * p.num_parts + part;
+      *reinterpret_cast<float4*>(p.ws_o + r * D + e) =
+          make_float4(o.x * inv, o.y * inv, o.z * inv, o.w * inv);
+      if (e == 0) {
+        p.ws_m[r] = M;
+        p.ws_l[r] = Lsum;
+      }
+    }
+  }
+}
+
+// Merge the partitions of sequences whose context spans more than one:
+// out = sum_p w_p o_p / sum_p w_p with w_p = l_p * 2^(m_p - max m).
+// One warp per (sequence, query head).
+template <typename T, int D>
+__global__ void __launch_bounds__(128) paged_decode_reduce_kernel(const DecodeParams p) {
+  constexpr int EPL = D / 32;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int pair = blockIdx.x * 4 + warp;
+  if (pair >= p.num_seqs * p.num_q_heads) return;
+  const int s = pair / p.num_q_heads;
+  int ctx = p.context_lens[s];
+  const long long cap_ll = min((long long)p.max_context_len,
+                               (long long)p.max_blocks_per_seq * p.block_size);
+  ctx = ctx < 0 ? 0 : (ctx > cap_ll ? (int)cap_ll : ctx);
+  const int np = (ctx + p.partition_size - 1) / p.partition_size;
+  if (np <= 1) return;  // written directly by the decode kernel
+  const float* mrow = p.ws_m + (size_t)pair * p.num_parts;
+  const float* lrow = p.ws_l + (size_t)pair * p.num_parts;
+  float M = -CUDART_INF_F;
+  for (int i = lane; i < np; i += 32) M = fmaxf(M, mrow[i]);
+#pragma unroll
+  for (int mk = 16; mk >= 1; mk >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, mk));
+  float Lsum = 0.f;
+  for (int i = lane; i < np; i += 32) Lsum += lrow[i] * exp2f(mrow[i] - M);
+#pragma unroll
+  for (int mk = 16; mk >= 1; mk >>= 1) Lsum += __shfl_xor_sync(kFull, Lsum, mk);
+  const float inv = 1.f / Lsum;
+  const float* orow = p.ws_o + (size_t)pair * p.num_parts * D + lane * EPL;
+  float acc[EPL];
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
+#pragma unroll 4
+  for (int i = 0; i < np; ++i) {
+    const float w = lrow[i] * exp2f(mrow[i] - M) * inv;
+    if constexpr (EPL == 4) {
+      const float4 a = *reinterpret_cast<const float4*>(orow + (size_t)i * D);
+      acc[0] += w * a.x;
+      acc[1] += w * a.y;
+      acc[2] += w * a.z;
+      acc[3] += w * a.w;
+    } else {
+      const float2 a = *reinterpret_cast<const float2*>(orow + (size_t)i * D);
+      acc[0] += w * a.x;
+      acc[1] += w * a.y;
+    }
+  }
+  T* out = static_cast<T*>(p.out) + (size_t)pair * D + lane * EPL;
+  if constexpr (EPL == 4) {
+    uint2 pk;
+    pk.x = Cvt<T>::from_float2(acc[0], acc[1]);
+    pk.y = Cvt<T>::from_float2(acc[2], acc[3]);
+    *reinterpret_cast<uint2*>(out) = pk;
+  } else {
+    *reinterpret_cast<uint32_t*>(out) = Cvt<T>::from_float2(acc[0], acc[1]);
+  }
+}
+
+template <typename T, int D, int GT>
+cudaError_t launch_typed(const DecodeParams& p, cudaStream_t stream) {
+  using L = SmemLayout<T, D, GT>;
+  // Opt in to more than 48 KiB of dynamic shared memory, once per device.
+  static unsigned long long configured = 0;  // bit per device ordinal (< 64)
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (dev >= 64 || !(__atomic_load_n(&configured, __ATOMIC_ACQUIRE) & (1ull << dev))) {
+    err = cudaFuncSetAttribute(paged_decode_kernel<T, D, GT>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::kBytes);
+    if (err != cudaSuccess) return err;
+    if (dev < 64) __atomic_fetch_or(&configured, 1ull << dev, __ATOMIC_RELEASE);
+  }
+  const dim3 grid(p.num_parts, p.num_kv_heads * p.head_chunks, p.num_seqs);
+  paged_decode_kernel<T, D, GT><<<grid, kThreads, L::kBytes, stream>>>(p);
+  err = cudaGetLastError();
+  if (err != cudaSuccess || p.num_parts <= 1) return err;
+  const int pairs = p.num_seqs * p.num_q_heads;
+  paged_decode_reduce_kernel<T, D><<<(pairs + 3) / 4, 128, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+template <typename T, int D>
+cudaError_t launch_for_group(const DecodeParams& p, int gt, cudaStream_t stream) {
+  switch (gt) {
+    case 1: return launch_typed<T, D, 1>(p, stream);
+    case 2: return launch_typed<T, D, 2>(p, stream);
+    default: return launch_typed<T, D, 4>(p, stream);
+  }
+}
+
+}  // namespace
+
+int decode_heads_per_cta(int group) { return group == 1 ? 1 : (group == 2 ? 2 : 4); }
+
+size_t decode_smem_bytes(int head_dim, int gt) {
+  // The layout does not depend on the element type beyond its size (2 bytes).
+  if (head_dim == 64) {
+    return gt == 1 ? SmemLayout<__half, 64, 1>::kBytes
+                   : (gt == 2 ? SmemLayout<__half, 64, 2>::kBytes : SmemLayout<__half, 64, 4>::kBytes);
+  }
+  return gt == 1 ? SmemLayout<__half, 128, 1>::kBytes
+                 : (gt == 2 ? SmemLayout<__half, 128, 2>::kBytes : SmemLayout<__half, 128, 4>::kBytes);
+}
+
+cudaError_t launch_paged_decode(const DecodeParams& p, int dtype, int head_dim, int gt,
+                                cudaStream_t stream) {
+  if (dtype == PKV_F16) {
+    return head_dim == 64 ? launch_for_group<__half, 64>(p, gt, stream)
+                          : launch_for_group<__half, 128>(p, gt, stream);
+  }
+  return head_dim == 64 ? launch_for_group<__nv_bfloat16, 64>(p, gt, stream)
+                        : launch_for_group<__nv_bfloat16, 128>(p, gt, stream);
+}
+
+}  // namespace pkv

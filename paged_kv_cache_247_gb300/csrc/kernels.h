@@ -1,0 +1,57 @@
+// Host-side launch interface between the C ABI (api.cu) and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace pkv {
+
+// Everything one paged decode launch needs.  Filled and checked by the API
+// layer; the kernels trust it.
+struct DecodeParams {
+  void* out;                  // [S, Hq, D] element type
+  const void* q;              // [S, Hq, D]
+  const void* k_cache;        // [NB, Hkv, B, D]
+  const void* v_cache;        // [NB, Hkv, B, D]
+  const int32_t* block_tables;  // [S, max_blocks_per_seq]
+  const int32_t* context_lens;  // [S]
+  float* ws_o;                // split only: [S, Hq, num_parts, D]
+  float* ws_m;                // split only: [S, Hq, num_parts] (log2 domain)
+  float* ws_l;                // split only: [S, Hq, num_parts]
+  unsigned int* status;       // device status word
+  int max_blocks_per_seq;
+  int max_context_len;
+  int num_seqs;
+  int num_q_heads;
+  int num_kv_heads;
+  int group;        // Hq / Hkv
+  int head_chunks;  // CTAs per KV head (ceil(group / heads per CTA))
+  int block_size;
+  int log2_block;
+  int num_blocks;
+  int partition_size;  // tokens per CTA (multiple of 32)
+  int num_parts;       // ceil(max_context_len / partition_size), >= 1
+  float qscale;        // scale * log2(e): logits are kept in base-2 units
+};
+
+// Query heads one CTA processes for a group size (1, 2 or 4).
+int decode_heads_per_cta(int group);
+
+// Shared memory one decode CTA uses.
+size_t decode_smem_bytes(int head_dim, int heads_per_cta);
+
+// Launch the decode kernel and, when num_parts > 1, the reduction kernel.
+cudaError_t launch_paged_decode(const DecodeParams& p, int dtype, int head_dim,
+                                int heads_per_cta, cudaStream_t stream);
+
+cudaError_t launch_kv_append(const void* k, const void* v, void* k_cache, void* v_cache,
+                             const int64_t* slot_mapping, int num_tokens, int num_kv_heads,
+                             int head_dim, int block_size, int num_blocks,
+                             unsigned int* status, cudaStream_t stream);
+
+cudaError_t launch_block_copy(void* k_cache, void* v_cache, const int64_t* pairs,
+                              int num_pairs, int num_blocks, size_t block_bytes,
+                              unsigned int* status, cudaStream_t stream);
+
+}  // namespace pkv

@@ -1,0 +1,94 @@
+"""The C ABI on a machine without a GPU: the library loads, exports every
+symbol include/pagedkv.h declares, and rejects bad arguments on the host
+before anything is enqueued (none of these calls reaches CUDA)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from paged_kv_cache_247_gb300 import _lib as L
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                      "include", "pagedkv.h")
+
+
+def declared_functions():
+    with open(HEADER) as f:
+        text = re.sub(r"/\*.*?\*/", "", f.read(), flags=re.S)
+    return sorted(set(re.findall(r"\b(pkv_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("pkv_paged_attn_decode", "pkv_kv_append", "pkv_block_copy",
+                     "pkv_decode_workspace_size", "pkv_alloc_create", "pkv_alloc_append_slot"):
+        assert required in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing
+    # and the binding attaches a signature to each of them
+    assert set(declared_functions()) == set(L.SIGNATURES)
+
+
+def test_status_strings(lib):
+    assert lib.pkv_status_string(0) == b"ok"
+    assert lib.pkv_status_string(3) == b"workspace too small"
+    assert lib.pkv_version() == 1
+
+
+def _decode(lib, **over):
+    a = dict(out=16, q=16, k=16, v=16, tables=16, mbps=4, lens=16, maxctx=64, S=2, Hq=8,
+             Hkv=2, D=128, B=16, NB=10, scale=0.1, dtype=0, part=0, ws=None, wsb=0)
+    a.update(over)
+    return lib.pkv_paged_attn_decode(a["out"], a["q"], a["k"], a["v"], a["tables"], a["mbps"],
+                                     a["lens"], a["maxctx"], a["S"], a["Hq"], a["Hkv"], a["D"],
+                                     a["B"], a["NB"], a["scale"], a["dtype"], a["part"], a["ws"],
+                                     a["wsb"], None)
+
+
+@pytest.mark.parametrize("over,expect", [
+    (dict(Hq=6, Hkv=4), 1),             # Hq not a multiple of Hkv
+    (dict(D=96), 2),                    # head_dim not built
+    (dict(B=24), 2),                    # block size not built
+    (dict(dtype=7), 1),
+    (dict(part=48), 1),                 # partition not a multiple of 32
+    (dict(q=None), 1),
+    (dict(q=8), 1),                     # misaligned
+    (dict(tables=2), 1),                # misaligned int32
+    (dict(mbps=3), 1),                  # 3 * 16 < 64 = max context
+    (dict(maxctx=-1), 1),
+    (dict(scale=float("inf")), 1),
+    (dict(S=70000), 2),                 # grid limit
+    (dict(maxctx=4096, part=512), 3),   # split needs workspace
+    (dict(S=0, q=None), 0),             # empty batch is a no-op
+])
+def test_decode_host_validation(lib, over, expect):
+    if over.get("maxctx") == 4096:
+        over["mbps"] = 256
+    assert _decode(lib, **over) == expect
+
+
+def test_workspace_size_arithmetic(lib):
+    # 8 sequences, 32 heads, 32k context, 512-token partitions -> 64 parts
+    n = lib.pkv_decode_workspace_size(8, 32, 8, 128, 32768, 0)
+    assert n == 8 * 32 * 64 * (128 + 2) * 4
+    assert lib.pkv_decode_workspace_size(8, 32, 8, 128, 512, 0) == 0
+    assert lib.pkv_decode_workspace_size(8, 32, 8, 128, 4096, 4096) == 0
+    assert lib.pkv_decode_workspace_size(8, 32, 8, 128, 4097, 4096) == 8 * 32 * 2 * 130 * 4
+    assert lib.pkv_decode_workspace_size(8, 32, 8, 96, 100, 0) == ctypes.c_size_t(-1).value
+    assert lib.pkv_decode_partition_size(8, 32, 8, 128, 100) == 128
+    assert lib.pkv_decode_partition_size(8, 32, 8, 128, 32768) == 512
+
+
+def test_append_and_copy_host_validation(lib):
+    assert lib.pkv_kv_append(None, None, None, None, None, 0, 8, 128, 16, 4, 0, None) == 0
+    assert lib.pkv_kv_append(16, 16, 16, 16, 16, 3, 8, 80, 16, 4, 0, None) == 2
+    assert lib.pkv_kv_append(16, 16, 16, 16, 12, 3, 8, 128, 16, 4, 0, None) == 1
+    assert lib.pkv_kv_append(16, 16, 16, 16, 16, -1, 8, 128, 16, 4, 0, None) == 1
+    assert lib.pkv_block_copy(None, None, None, 0, 4, 4096, None) == 0
+    assert lib.pkv_block_copy(16, 16, 16, 2, 4, 4090, None) == 1
+    assert lib.pkv_block_copy(16, 16, None, 2, 4, 4096, None) == 1
