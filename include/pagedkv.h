@@ -237,9 +237,10 @@ pkv_status_t pkv_alloc_append_slot(pkv_allocator* a, int64_t seq_id, int64_t* sl
                                    int64_t* cow_src, int64_t* cow_dst);
 /* append_slot for n sequences in order.  slots[i] receives the slot of
  * seq_ids[i]; every copy needed is written to cow_pairs (int64 [n, 2]) and
- * *num_pairs receives their count.  On failure the earlier sequences of the
- * batch keep their new slots and *num_pairs counts their copies; the
- * failing sequence and the ones after it are unchanged. */
+ * *num_pairs receives their count.  All or nothing: if any sequence fails
+ * (unknown id, pool exhausted) the appends already made in the batch are
+ * undone, the allocator is left as before the call and *num_pairs is 0.
+ * A sequence id may appear at most once per batch. */
 pkv_status_t pkv_alloc_append_slots(pkv_allocator* a, const int64_t* seq_ids, int n,
                                     int64_t* slots, int64_t* cow_pairs, int* num_pairs);
 /* Drop a sequence (finish or cancel); blocks reaching count 0 are freed. */

@@ -24,7 +24,8 @@ can be compared with this model id for id:
 * copy-on-write happens iff the write position is inside the last block
   (position % B != 0) and that block's count is above one; a write at a block
   boundary takes a fresh block and copies nothing;
-* running out of blocks raises and leaves the state unchanged.
+* running out of blocks raises and leaves the state unchanged; a batch of
+  appends is all or nothing.
 """
 
 
@@ -98,6 +99,27 @@ class OracleAllocator:
                 self.cow_copies += 1
         self.lengths[seq_id] = pos + 1
         return table[-1] * self.block_size + offset, cow_src, cow_dst
+
+    def append_slots(self, seq_ids):
+        """append_slot for each sequence in order, all or nothing.
+
+        Returns ``(slots, pairs)``; if any append fails the allocator is
+        restored to its state before the call and the error is raised.
+        """
+        saved = (list(self.free), list(self.refcount),
+                 {k: list(v) for k, v in self.tables.items()}, dict(self.lengths),
+                 self.cow_copies)
+        slots, pairs = [], []
+        try:
+            for s in seq_ids:
+                slot, src, dst = self.append_slot(s)
+                slots.append(slot)
+                if src >= 0:
+                    pairs.append([src, dst])
+        except Exception:
+            (self.free, self.refcount, self.tables, self.lengths, self.cow_copies) = saved
+            raise
+        return slots, pairs
 
     def free_seq(self, seq_id: int):
         """Drop the sequence; blocks whose count reaches zero are reusable."""

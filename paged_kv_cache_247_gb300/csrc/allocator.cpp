@@ -48,23 +48,51 @@ struct pkv_allocator {
     return (tokens + block_size - 1) / block_size;
   }
 
-  // One sequence's next slot; fills *pair with the copy-on-write pair
-  // (or -1, -1).  Leaves everything unchanged on failure.
-  pkv_status_t append(int64_t seq_id, int64_t* slot, int64_t* cow_src, int64_t* cow_dst) {
+  // Undo record of one append, so that a failed batch can be rolled back.
+  struct Undo {
+    Seq* seq;
+    int32_t taken;    // block taken from the free list (-1: none)
+    int32_t cow_src;  // block the sequence held before copy-on-write (-1: none)
+  };
+
+  // Reverse one append.  Undoing in reverse order restores the LIFO free
+  // list exactly.
+  void undo(const Undo& u) {
+    u.seq->length -= 1;
+    if (u.cow_src >= 0) {
+      ++refcount[u.cow_src];
+      u.seq->table.back() = u.cow_src;
+      --cow_copies;
+    } else if (u.taken >= 0) {
+      u.seq->table.pop_back();
+    }
+    if (u.taken >= 0) {
+      refcount[u.taken] = 0;
+      free_list.push_back(u.taken);
+    }
+  }
+
+  // One sequence's next slot; fills the copy-on-write pair (or -1, -1).
+  // Leaves everything unchanged on failure.
+  pkv_status_t append(int64_t seq_id, int64_t* slot, int64_t* cow_src, int64_t* cow_dst,
+                      Undo* record = nullptr) {
     auto it = seqs.find(seq_id);
     if (it == seqs.end()) return PKV_ERR_UNKNOWN_SEQ;
     Seq& s = it->second;
     const int64_t pos = s.length;
     const int offset = static_cast<int>(pos % block_size);
     int64_t src = -1, dst = -1;
+    int32_t taken = -1;
     if (offset == 0) {
       if (free_list.empty()) return PKV_ERR_OUT_OF_BLOCKS;
-      s.table.push_back(take());
+      taken = take();
+      s.table.push_back(taken);
     } else {
       const int32_t last = s.table.back();
       if (refcount[last] > 1) {
         if (free_list.empty()) return PKV_ERR_OUT_OF_BLOCKS;
         const int32_t fresh = take();
+        taken = fresh;
         --refcount[last];  // still > 0: other sequences keep it
         s.table.back() = fresh;
         src = last;
@@ -76,6 +104,7 @@ struct pkv_allocator {
     *slot = static_cast<int64_t>(s.table.back()) * block_size + offset;
     *cow_src = src;
     *cow_dst = dst;
+    if (record) *record = Undo{&s, taken, static_cast<int32_t>(src)};
     return PKV_OK;
   }
 };
@@ -131,12 +160,15 @@ pkv_status_t pkv_alloc_append_slots(pkv_allocator* a, const int64_t* seq_ids, in
                                     int64_t* slots, int64_t* cow_pairs, int* num_pairs) {
   if (!a || n < 0 || !num_pairs || (n > 0 && (!seq_ids || !slots || !cow_pairs)))
     return PKV_ERR_INVALID_ARG;
+  // All or nothing: on failure every append of the batch is undone.
+  std::vector<pkv_allocator::Undo> log(static_cast<size_t>(n));
   int pairs = 0;
   for (int i = 0; i < n; ++i) {
     int64_t src, dst;
-    const pkv_status_t st = a->append(seq_ids[i], &slots[i], &src, &dst);
+    const pkv_status_t st = a->append(seq_ids[i], &slots[i], &src, &dst, &log[i]);
     if (st != PKV_OK) {
-      *num_pairs = pairs;
+      for (int j = i - 1; j >= 0; --j) a->undo(log[j]);
+      *num_pairs = 0;
       return st;
     }
     if (src >= 0) {

@@ -77,16 +77,11 @@ def test_matches_oracle_model(native, seed):
                 assert nat.append_slot(s) == want
         elif op == "batch":
             seqs = [int(x) for x in rng.choice(live, size=min(len(live), 4), replace=False)]
-            want_slots, want_pairs, failed = [], [], False
-            for s in seqs:
-                try:
-                    slot, cs, cd = ora.append_slot(s)
-                except OracleOutOfBlocks:
-                    failed = True
-                    break
-                want_slots.append(slot)
-                if cs >= 0:
-                    want_pairs.append([cs, cd])
+            try:
+                want_slots, want_pairs = ora.append_slots(seqs)
+                failed = False
+            except OracleOutOfBlocks:
+                failed = True
             if failed:
                 with pytest.raises(OutOfBlocks):
                     nat.append_slots(seqs)
