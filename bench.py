@@ -44,7 +44,7 @@ FALLBACK_HBM_GBS = 6800.0
 def parse_args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--steps", type=int, default=5000)
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="opt13b", choices=["opt13b", "gqa4k"])
@@ -87,7 +87,7 @@ def ncu_traffic(kernel_key, workload):
 
 
 class ClockSampler:
-    """nvidia-smi sampling every 200 ms in the background."""
+    """nvidia-smi sampling every 100 ms in the background."""
 
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -103,7 +103,7 @@ class ClockSampler:
             self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=self.file, stderr=subprocess.DEVNULL)
         except (OSError, ValueError):
             self.proc = None
@@ -224,7 +224,9 @@ def run_reference(args, rank, world):
         return
     from paged_kv_cache_247_gb300 import workloads as W
     case, k_new, v_new, slots, desc, label = make_workload(args.workload, "cpu")
-    per_step = max(0.5, min(6.0, 150.0 / max(1, args.steps + args.warmup)))
+    # bounded so that the whole run stays within a few minutes (at least one
+    # whole sequence per step)
+    per_step = min(6.0, 150.0 / max(1, args.steps + args.warmup))
     for _ in range(args.warmup):
         oracle_sample_rate(case, k_new, v_new, slots, per_step / 4, max_seqs=1)
     total_bytes_t, seqs, elapsed = 0.0, 0, 0.0
