@@ -128,6 +128,42 @@ pkv_status_t pkv_paged_attn_decode(
     int partition_size, void* workspace, size_t workspace_bytes,
     pkv_stream_t stream);
 
+/* ------------------------------------------------------------------------
+ * Allocation-free decode.  (The source pages have no counterpart: this is an
+ * interface for callers, not part of the method.)
+ *
+ * For callers that cannot provide a workspace: engines that reserve all
+ * device memory for their own pool and forbid allocation while serving, and
+ * latency-critical loops where cudaMalloc, which may synchronise the device,
+ * is not allowed.  Same arguments and result as pkv_paged_attn_decode minus
+ * the workspace: the split-context partials go to a fixed array of
+ * PKV_NOALLOC_SCRATCH_BYTES inside the library, which every GPU that loads
+ * the library holds until the process exits.
+ *
+ *   - Allocates nothing (no cudaMalloc/cudaFree, no allocating library call).
+ *   - Sizes whose pkv_decode_workspace_size(...) exceeds
+ *     PKV_NOALLOC_SCRATCH_BYTES are rejected with PKV_ERR_WORKSPACE_TOO_SMALL
+ *     before anything is enqueued; use a larger partition_size or the
+ *     workspace entry point for them.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current) and caches it; make
+ *     that first call before any stream capture.
+ *   - All calls on a device share the one array, which keeps whatever the
+ *     last call left in it.  Nothing in it needs to start at zero (each
+ *     partial is written before it is read), but calls that overlap on the
+ *     GPU (different streams without ordering between them) race on it:
+ *     order them on one stream or with events.
+ * ---------------------------------------------------------------------- */
+#define PKV_NOALLOC_SCRATCH_BYTES (16u << 20) /* 16 MiB */
+
+pkv_status_t pkv_paged_attn_decode_noalloc(
+    void* out, const void* q, const void* k_cache, const void* v_cache,
+    const int32_t* block_tables, int max_blocks_per_seq,
+    const int32_t* context_lens, int max_context_len,
+    int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+    int block_size, int num_blocks, float scale, pkv_dtype_t dtype,
+    int partition_size, pkv_stream_t stream);
+
 /* Partition size the library picks for partition_size == 0 on the current
  * device (depends on its SM count).  Returns a positive multiple of 32, or
  * -1 for invalid arguments. */

@@ -269,3 +269,71 @@ pkv_status_t pkv_device_status(uint32_t* flags, int clear, pkv_stream_t stream) 
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free decode.
+//
+// Some callers cannot hand this library a workspace: serving engines that
+// reserve all device memory for their own pool up front and do not let a
+// library allocate while it runs, and latency-critical loops where a
+// cudaMalloc (which may synchronise the device) is not allowed.  For them,
+// pkv_paged_attn_decode_noalloc runs the same decode with its split-context
+// partials kept in a fixed array that lives in this library's device image.
+// Every GPU that loads the library holds this array until the process exits.
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[PKV_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+void* g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of the array on the current device.  Host code only sees a
+// host-side stand-in under the array's name, so the address is looked up once
+// per device (with that device current) and cached.
+cudaError_t noalloc_scratch(void** out) {
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    err = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (err != cudaSuccess) return err;
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return cudaSuccess;
+}
+
+}  // namespace
+
+extern "C" pkv_status_t pkv_paged_attn_decode_noalloc(
+    void* out, const void* q, const void* k_cache, const void* v_cache,
+    const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+    int max_context_len, int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+    int block_size, int num_blocks, float scale, pkv_dtype_t dtype, int partition_size,
+    pkv_stream_t stream) {
+  const size_t need = pkv_decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                                max_context_len, partition_size);
+  if (need == (size_t)-1) {
+    // Invalid sizes: the regular entry point reports the precise error
+    // before it touches any memory.
+    return pkv_paged_attn_decode(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                                 context_lens, max_context_len, num_seqs, num_q_heads,
+                                 num_kv_heads, head_dim, block_size, num_blocks, scale, dtype,
+                                 partition_size, nullptr, 0, stream);
+  }
+  if (need > PKV_NOALLOC_SCRATCH_BYTES) return PKV_ERR_WORKSPACE_TOO_SMALL;
+  void* scratch = nullptr;
+  if (need > 0) {
+    const cudaError_t err = noalloc_scratch(&scratch);
+    if (err != cudaSuccess) return cuda_fail(err);
+  }
+  // The partials need no clearing: every partition writes its slot before
+  // the reduction reads it, so what an earlier call left behind is ignored.
+  return pkv_paged_attn_decode(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                               context_lens, max_context_len, num_seqs, num_q_heads, num_kv_heads,
+                               head_dim, block_size, num_blocks, scale, dtype, partition_size,
+                               scratch, need > 0 ? (size_t)PKV_NOALLOC_SCRATCH_BYTES : 0, stream);
+}
