@@ -172,6 +172,47 @@ def step_bytes(case):
     return decode, append
 
 
+def contiguous_baseline(pkv, case, out, part, dev, stream, iters):
+    S, Hq, D = case.q.shape
+    Hkv, B = case.k_cache.shape[1], case.block_size
+    cap = case.max_context_len
+    kc = torch.zeros((S, Hkv, cap, D), dtype=case.q.dtype, device=dev)
+    vc = torch.zeros_like(kc)
+    tables = case.block_tables.long()
+    for s, n in enumerate(case.context_lens.tolist()):
+        nb = -(-n // B)
+        ids = tables[s, :nb]
+        kc[s, :, :n] = case.k_cache[ids].permute(1, 0, 2, 3).reshape(Hkv, nb * B, D)[:, :n]
+        vc[s, :, :n] = case.v_cache[ids].permute(1, 0, 2, 3).reshape(Hkv, nb * B, D)[:, :n]
+    ws = torch.empty(max(16, pkv.decode_workspace_size(S, Hq, Hkv, D, cap, part)),
+                     dtype=torch.uint8, device=dev)
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(iters):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / iters
+
+    t_paged = timed(lambda: pkv.paged_attn_decode(
+        out, case.q, case.k_cache, case.v_cache, case.block_tables, case.context_lens,
+        case.scale, cap, partition_size=part, workspace=ws))
+    t_contig = timed(lambda: pkv.contiguous_attn_decode(
+        out, case.q, kc, vc, case.context_lens, case.scale, partition_size=part, workspace=ws))
+    reserved = kc.numel() * kc.element_size() * 2
+    held = int(case.context_lens.sum().item()) * Hkv * D * case.q.element_size() * 2
+    del kc, vc
+    torch.cuda.empty_cache()
+    return {"paged_decode_ms": round(t_paged, 5), "contiguous_decode_ms": round(t_contig, 5),
+            "indirection_overhead_pct": round(100.0 * (t_paged / t_contig - 1.0), 2),
+            "contiguous_reserved_bytes": reserved, "paged_held_bytes": held,
+            "partition_size": part, "iters": iters}
+
+
 # ------------------------------------------------------------- CPU legs --
 
 def oracle_sample_rate(case, k_new, v_new, slots, seconds, max_seqs=None):
@@ -353,6 +394,11 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / K_e2e
 
+    # Contiguous baseline: the same tokens with each sequence reserved at
+    # max_context_len and no block table; the ratio of the two decode times
+    # is the cost of the indirection.
+    contig = contiguous_baseline(pkv, case, out, part, dev, stream, max(20, K // 10))
+
     decode_b, append_b = step_bytes(case)
     ms_step = elapsed_ms / K
     value = (decode_b + append_b) * world / (ms_step * 1e-3) / 1e9
@@ -385,6 +431,7 @@ def run_ours(args, rank, world, local_rank):
         "e2e": {"value": round((decode_b + append_b) * world / (e2e_ms * 1e-3) / 1e9, 2),
                 "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e_ms, 5)},
+        "contiguous_baseline": contig,
         "gpu_launches": K * launches_per_step,
         "clocks": clock_rec,
     }

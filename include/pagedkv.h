@@ -180,6 +180,31 @@ size_t pkv_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads
                                  int head_dim, int max_context_len, int partition_size);
 
 /* ------------------------------------------------------------------------
+ * Contiguous-cache decode: the baseline without a block table.
+ *
+ * [P3] "When the extra machinery is not worth it": keep a simple contiguous
+ * cache as a baseline and compare both under identical token distributions;
+ * [P2] "What the indirection costs": the paged kernel's price is the table
+ * reads, extra branches and variable lengths.  This call runs the same
+ * kernels over the pre-paging layout ([P2] opening section: one contiguous
+ * tensor per request, reserved at its maximum length), so the difference to
+ * pkv_paged_attn_decode on the same tokens is the cost of the indirection.
+ *
+ *   k_cache/v_cache [num_seqs, num_kv_heads, capacity, head_dim] dtype:
+ *                 sequence s holds its positions t < context_lens[s] at
+ *                 [s][h][t][:]; capacity is the reservation per sequence
+ *   context_lens  int32 [num_seqs], each in [0, capacity]
+ * Other arguments, results, workspace and errors as pkv_paged_attn_decode
+ * (with max_context_len = capacity).
+ * ---------------------------------------------------------------------- */
+pkv_status_t pkv_contiguous_attn_decode(
+    void* out, const void* q, const void* k_cache, const void* v_cache,
+    const int32_t* context_lens, int capacity,
+    int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+    float scale, pkv_dtype_t dtype, int partition_size,
+    void* workspace, size_t workspace_bytes, pkv_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * Append new tokens' K and V into their cache slots.
  *
  * The cache grows token by token ([P2] "Why the KV cache is the thing that

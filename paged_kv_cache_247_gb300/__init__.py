@@ -15,6 +15,7 @@ is no fallback: a missing library raises.
 from ._lib import PagedKVError, load as load_library  # noqa: F401
 from .ops import (  # noqa: F401
     paged_attn_decode,
+    contiguous_attn_decode,
     kv_append,
     block_copy,
     device_status,

@@ -12,8 +12,10 @@
 namespace {
 
 constexpr int kMaxDevices = 64;
-constexpr int kDefaultPartition = 512;  // tokens per split-context partition
-constexpr int kPartitionQuantum = 32;   // partitions are whole pipeline stages
+constexpr int kPartitionQuantum = 32;    // partitions are whole pipeline stages
+constexpr int kMaxAutoPartition = 2048;  // longest partition the library picks
+constexpr int kAssumedSms = 152;         // used only when no device can be queried
+constexpr int kAssumedCtasPerSm = 3;
 
 // Sticky per-device record of problems the kernels saw (PKV_DEV_* bits).
 __device__ unsigned int g_device_status;
@@ -47,7 +49,7 @@ cudaError_t status_word(unsigned int** out) {
   return cudaSuccess;
 }
 
-[[maybe_unused]] int sm_count() {
+int sm_count() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
   std::lock_guard<std::mutex> lock(g_mutex);
@@ -79,12 +81,35 @@ int round_partition(int tokens) {
   return ((t + kPartitionQuantum - 1) / kPartitionQuantum) * kPartitionQuantum;
 }
 
-int auto_partition(int max_context_len) {
-  // Contexts up to one partition run unsplit; longer ones are cut into
-  // fixed partitions so that every CTA streams a bounded, similar amount of
-  // K/V (even for a batch of one) and a reduction merges them.
-  if (max_context_len <= kDefaultPartition) return round_partition(max_context_len);
-  return kDefaultPartition;
+// Tokens per partition when the caller leaves the choice to the library.
+//
+// Every partition costs a CTA start-up (barrier set-up, table window,
+// pipeline fill), a drain and a round trip of its partial result through the
+// workspace, so partitions are kept long (up to 2048 tokens; measured best on
+// GB300 for 1k-32k contexts) and contexts are split only as far as needed to
+// give about two waves of CTAs.  Batches with very few (sequence, KV head)
+// units split finer (down to 256 tokens) because idle SMs cost more than
+// partition overhead there.
+int auto_partition(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                   int max_context_len) {
+  if (max_context_len <= kPartitionQuantum) return kPartitionQuantum;
+  const int group = num_q_heads / num_kv_heads;
+  const int gt = pkv::decode_heads_per_cta(group);
+  const long long units = (long long)num_seqs * num_kv_heads * ((group + gt - 1) / gt);
+  int sms = sm_count();
+  int per_sm = sms ? pkv::decode_ctas_per_sm(head_dim, gt) : 0;
+  if (sms <= 0) sms = kAssumedSms;  // no device: assume a GB300
+  if (per_sm <= 0) per_sm = kAssumedCtasPerSm;
+  const long long slots = (long long)sms * per_sm;
+  const long long target = 2 * slots;
+  const long long parts = units >= target ? 1 : (target + units - 1) / units;
+  const int floor_tokens = units * 4 >= slots ? 1024 : 256;
+  long long part = (max_context_len + parts - 1) / parts;
+  part = ((part + 255) / 256) * 256;
+  if (part < floor_tokens) part = floor_tokens;
+  if (part > kMaxAutoPartition) part = kMaxAutoPartition;
+  if (part >= max_context_len) return round_partition(max_context_len);
+  return (int)part;
 }
 
 long long num_parts_for(int max_context_len, int partition) {
@@ -119,7 +144,7 @@ int pkv_decode_partition_size(int num_seqs, int num_q_heads, int num_kv_heads, i
                               int max_context_len) {
   if (!decode_shape_ok(num_seqs, num_q_heads, num_kv_heads, max_context_len)) return -1;
   if (head_dim != 64 && head_dim != 128) return -1;
-  return auto_partition(max_context_len);
+  return auto_partition(num_seqs, num_q_heads, num_kv_heads, head_dim, max_context_len);
 }
 
 size_t pkv_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
@@ -127,7 +152,9 @@ size_t pkv_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads
   if (!decode_shape_ok(num_seqs, num_q_heads, num_kv_heads, max_context_len)) return (size_t)-1;
   if (head_dim != 64 && head_dim != 128) return (size_t)-1;
   if (partition_size < 0 || partition_size % kPartitionQuantum) return (size_t)-1;
-  const int part = partition_size ? partition_size : auto_partition(max_context_len);
+  const int part = partition_size ? partition_size
+                                  : auto_partition(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                                   max_context_len);
   const long long parts = num_parts_for(max_context_len, part);
   if (parts <= 1) return 0;
   return (size_t)num_seqs * num_q_heads * parts * (head_dim + 2) * sizeof(float);
@@ -161,7 +188,9 @@ pkv_status_t pkv_paged_attn_decode(void* out, const void* q, const void* k_cache
   const int group = num_q_heads / num_kv_heads;
   const int gt = pkv::decode_heads_per_cta(group);
   const int head_chunks = (group + gt - 1) / gt;
-  const int part = partition_size ? partition_size : auto_partition(max_context_len);
+  const int part = partition_size ? partition_size
+                                  : auto_partition(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                                   max_context_len);
   const long long parts = num_parts_for(max_context_len, part);
   if (num_seqs > 65535 || (long long)num_kv_heads * head_chunks > 65535 || parts > 0x7fffffffLL)
     return PKV_ERR_UNSUPPORTED;
@@ -200,6 +229,73 @@ pkv_status_t pkv_paged_attn_decode(void* out, const void* q, const void* k_cache
   cudaError_t err = status_word(&p.status);
   if (err != cudaSuccess) return cuda_fail(err);
   err = pkv::launch_paged_decode(p, dtype, head_dim, gt, reinterpret_cast<cudaStream_t>(stream));
+  if (err != cudaSuccess) return cuda_fail(err);
+  return PKV_OK;
+}
+
+pkv_status_t pkv_contiguous_attn_decode(void* out, const void* q, const void* k_cache,
+                                        const void* v_cache, const int32_t* context_lens,
+                                        int capacity, int num_seqs, int num_q_heads,
+                                        int num_kv_heads, int head_dim, float scale,
+                                        pkv_dtype_t dtype, int partition_size, void* workspace,
+                                        size_t workspace_bytes, pkv_stream_t stream) {
+  if (!decode_shape_ok(num_seqs, num_q_heads, num_kv_heads, capacity)) return PKV_ERR_INVALID_ARG;
+  if (dtype != PKV_F16 && dtype != PKV_BF16) return PKV_ERR_INVALID_ARG;
+  if (partition_size < 0 || partition_size % kPartitionQuantum) return PKV_ERR_INVALID_ARG;
+  if (!isfinite(scale)) return PKV_ERR_INVALID_ARG;
+  if (head_dim != 64 && head_dim != 128) return PKV_ERR_UNSUPPORTED;
+  if (num_seqs == 0) return PKV_OK;
+  if (!out || !q || !k_cache || !v_cache || !context_lens) return PKV_ERR_INVALID_ARG;
+  if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
+    return PKV_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(context_lens) & 3u) return PKV_ERR_INVALID_ARG;
+  if (capacity <= 0) return PKV_ERR_INVALID_ARG;
+
+  const int group = num_q_heads / num_kv_heads;
+  const int gt = pkv::decode_heads_per_cta(group);
+  const int head_chunks = (group + gt - 1) / gt;
+  const int part = partition_size ? partition_size
+                                  : auto_partition(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                                   capacity);
+  const long long parts = num_parts_for(capacity, part);
+  if (num_seqs > 65535 || (long long)num_kv_heads * head_chunks > 65535 || parts > 0x7fffffffLL)
+    return PKV_ERR_UNSUPPORTED;
+  if ((long long)num_seqs * num_q_heads > 0x7fffffffLL) return PKV_ERR_UNSUPPORTED;
+
+  pkv::DecodeParams p{};
+  p.out = out;
+  p.q = q;
+  p.k_cache = k_cache;
+  p.v_cache = v_cache;
+  p.block_tables = nullptr;
+  p.context_lens = context_lens;
+  p.max_blocks_per_seq = 1;   // one "block" per sequence: its whole reservation
+  p.max_context_len = capacity;
+  p.num_seqs = num_seqs;
+  p.num_q_heads = num_q_heads;
+  p.num_kv_heads = num_kv_heads;
+  p.group = group;
+  p.head_chunks = head_chunks;
+  p.block_size = capacity;
+  p.log2_block = 0;
+  p.num_blocks = num_seqs;
+  p.partition_size = part;
+  p.num_parts = (int)parts;
+  p.qscale = scale * 1.4426950408889634f;
+  if (parts > 1) {
+    const size_t need = (size_t)num_seqs * num_q_heads * parts * (head_dim + 2) * sizeof(float);
+    if (!workspace || workspace_bytes < need) return PKV_ERR_WORKSPACE_TOO_SMALL;
+    if (!aligned16(workspace)) return PKV_ERR_INVALID_ARG;
+    float* ws = static_cast<float*>(workspace);
+    const size_t rows = (size_t)num_seqs * num_q_heads * parts;
+    p.ws_o = ws;
+    p.ws_m = ws + rows * head_dim;
+    p.ws_l = p.ws_m + rows;
+  }
+  cudaError_t err = status_word(&p.status);
+  if (err != cudaSuccess) return cuda_fail(err);
+  err = pkv::launch_contiguous_decode(p, dtype, head_dim, gt,
+                                      reinterpret_cast<cudaStream_t>(stream));
   if (err != cudaSuccess) return cuda_fail(err);
   return PKV_OK;
 }

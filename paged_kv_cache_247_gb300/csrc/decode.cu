@@ -40,45 +40,97 @@ namespace pkv {
 namespace {
 
 constexpr int kTokStage = 32;       // tokens per pipeline stage
-constexpr int kConsumerWarps = 4;   // warps doing arithmetic
-constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kTbl = 128;           // block ids held in shared memory at once
 constexpr unsigned kFull = 0xffffffffu;
+
+constexpr int ilog2(int x) { return x <= 1 ? 0 : 1 + ilog2(x >> 1); }
 
 template <int D>
 constexpr int stages_for() { return D >= 128 ? 4 : 8; }
 
+// Thread layout of one decode CTA, chosen per head size and group size.
+//   LPR   lanes that share one K/V row (each reads D / LPR columns)
+//   NCW   consumer warps (the producer is one more warp)
+//   MINB  CTAs per SM the register budget is sized for
+// More lanes per row means fewer q/accumulator registers per thread, which
+// buys more resident warps to hide the latency of the reductions.
+#ifndef PKV_G1_LPR
+#define PKV_G1_LPR 8
+#define PKV_G1_NCW 4
+#define PKV_G1_MINB 3
+#endif
+#ifndef PKV_G2_LPR
+#define PKV_G2_LPR 16
+#define PKV_G2_NCW 4
+#define PKV_G2_MINB 3
+#endif
+#ifndef PKV_G4_LPR
+#define PKV_G4_LPR 16
+#define PKV_G4_NCW 4
+#define PKV_G4_MINB 3
+#endif
+
+template <int LPR_, int NCW_, int MINB_>
+struct Layout {
+  static constexpr int LPR = LPR_;
+  static constexpr int NCW = NCW_;
+  static constexpr int MINB = MINB_;
+};
+
+template <int D, int GT>
+struct LayoutFor;
+template <int GT>
+struct LayoutFor<64, GT> : Layout<8, 4, 3> {};  // a 128-byte row: one 16-byte chunk per lane
+template <>
+struct LayoutFor<128, 1> : Layout<PKV_G1_LPR, PKV_G1_NCW, PKV_G1_MINB> {};
+template <>
+struct LayoutFor<128, 2> : Layout<PKV_G2_LPR, PKV_G2_NCW, PKV_G2_MINB> {};
+template <>
+struct LayoutFor<128, 4> : Layout<PKV_G4_LPR, PKV_G4_NCW, PKV_G4_MINB> {};
+
 template <typename T, int D, int GT>
 struct SmemLayout {
+  static constexpr int NCW = LayoutFor<D, GT>::NCW;
   static constexpr int kStages = stages_for<D>();
   static constexpr size_t kStageElems = (size_t)kTokStage * D;
-  static constexpr size_t kRing = kStages * kStageElems * sizeof(T);        // one of K, V
-  static constexpr size_t kMergeAcc = (size_t)kConsumerWarps * GT * D * 4;   // floats
-  static constexpr size_t kMergeMl = (size_t)kConsumerWarps * GT * 4;
+  static constexpr size_t kRing = kStages * kStageElems * sizeof(T);   // one of K, V
+  static constexpr size_t kMergeAcc = (size_t)NCW * GT * D * 4;        // floats
+  static constexpr size_t kMergeMl = (size_t)NCW * GT * 4;
   static constexpr size_t kTable = kTbl * 4;
   static constexpr size_t kBars = 2 * kStages * 8;
   static constexpr size_t kBytes = 2 * kRing + kMergeAcc + 2 * kMergeMl + kTable + kBars;
+  static constexpr int kThreads = (NCW + 1) * 32;
 };
 
-template <typename T, int D, int GT>
-__global__ void __launch_bounds__(kThreads, GT >= 4 ? 2 : 3)
+// kPaged = false is the contiguous-cache baseline: sequence s owns the rows
+// [s][h][0, capacity) of the caches (block_size = capacity, no table).
+template <typename T, int D, int GT, bool kPaged>
+__global__ void __launch_bounds__(SmemLayout<T, D, GT>::kThreads, LayoutFor<D, GT>::MINB)
     paged_decode_kernel(const DecodeParams p) {
   using L = SmemLayout<T, D, GT>;
+  using LY = LayoutFor<D, GT>;
+  constexpr int LPR = LY::LPR;
+  constexpr int NCW = LY::NCW;
   constexpr int NSTAGE = L::kStages;
-  constexpr int NCH = D / 64;           // 16-byte chunks per lane per row
-  constexpr int NF2 = D / 16;           // float2 per lane per row (= 4 * NCH)
-  constexpr int NV = 2 * GT;            // logits per lane before the reduction
-  constexpr int LB = NV == 2 ? 1 : (NV == 4 ? 2 : 3);
-  constexpr int SH = 3 - LB;            // lane-bit shift of a reduced logit index
-  constexpr int kTokMask = 1 << SH;     // lane bit separating the two row passes
+  constexpr int RPP = 32 / LPR;              // rows a warp covers per pass
+  constexpr int RPW = kTokStage / NCW;       // rows a warp owns per stage
+  constexpr int NP = RPW / RPP;              // passes per stage
+  constexpr int CPL = D / (8 * LPR);         // 16-byte chunks per lane per row
+  constexpr int NF2 = 4 * CPL;               // float2 per lane per row
+  constexpr int NV = GT * NP;                // partial sums per lane before the reduction
+  constexpr int LBL = ilog2(LPR);
+  constexpr int H = ilog2(NV);               // halving steps of the butterfly
+  constexpr int SH = LBL - H;                // lane-bit shift of a reduced value's index
+  constexpr int LOG2NP = ilog2(NP);
+  static_assert(CPL >= 1 && NP >= 1 && NV <= LPR, "unsupported decode layout");
 
   extern __shared__ __align__(128) unsigned char smem[];
   T* Ks = reinterpret_cast<T*>(smem);
   T* Vs = Ks + NSTAGE * L::kStageElems;
   float* mg_acc = reinterpret_cast<float*>(Vs + NSTAGE * L::kStageElems);
-  float* mg_max = mg_acc + kConsumerWarps * GT * D;
-  float* mg_sum = mg_max + kConsumerWarps * GT;
-  int* tbl = reinterpret_cast<int*>(mg_sum + kConsumerWarps * GT);
+  float* mg_max = mg_acc + NCW * GT * D;
+  float* mg_sum = mg_max + NCW * GT;
+  int* tbl = reinterpret_cast<int*>(mg_sum + NCW * GT);
   uint64_t* full = reinterpret_cast<uint64_t*>(tbl + kTbl);
   uint64_t* empty = full + NSTAGE;
 
@@ -105,7 +157,7 @@ __global__ void __launch_bounds__(kThreads, GT >= 4 ? 2 : 3)
   if (t_begin >= t_end) {
     if (ctx == 0 && part == 0) {  // empty context: the output is zero
       uint16_t* o = reinterpret_cast<uint16_t*>(p.out) + ((size_t)s * p.num_q_heads + h0) * D;
-      for (int i = threadIdx.x; i < nh * D; i += kThreads) o[i] = 0;
+      for (int i = threadIdx.x; i < nh * D; i += L::kThreads) o[i] = 0;
     }
     return;
   }
@@ -113,7 +165,7 @@ __global__ void __launch_bounds__(kThreads, GT >= 4 ? 2 : 3)
   if (threadIdx.x == 0) {
     for (int i = 0; i < NSTAGE; ++i) {
       mbar_init(&full[i], 1);
-      mbar_init(&empty[i], kConsumerWarps);
+      mbar_init(&empty[i], NCW);
     }
     fence_barrier_init();
   }
@@ -121,13 +173,33 @@ __global__ void __launch_bounds__(kThreads, GT >= 4 ? 2 : 3)
   const int nstages = (t_end - t_begin + kTokStage - 1) / kTokStage;
 
   // ------------------------------------------------------------ producer --
-  if (warp == kConsumerWarps) {
+  if (warp == NCW) {
     const uint64_t policy = policy_evict_first();
+    const T* kbase = static_cast<const T*>(p.k_cache);
+    const T* vbase = static_cast<const T*>(p.v_cache);
+    if constexpr (!kPaged) {
+      // Contiguous baseline: one run per stage, no table.
+      const size_t seq_base = ((size_t)s * p.num_kv_heads + kvh) * (size_t)p.block_size * D;
+      for (int it = 0; it < nstages; ++it) {
+        const int stg = it % NSTAGE;
+        if (it >= NSTAGE && !mbar_wait_warp(&empty[stg], ((it / NSTAGE) - 1) & 1, p.status)) break;
+        const int tok0 = t_begin + it * kTokStage;
+        const int ntok = min(kTokStage, t_end - tok0);
+        if (lane == 0) {
+          const uint32_t bytes = (uint32_t)ntok * D * sizeof(T);
+          mbar_arrive_expect_tx(&full[stg], 2 * bytes);
+          bulk_load(Ks + stg * L::kStageElems, kbase + seq_base + (size_t)tok0 * D, bytes,
+                    &full[stg], policy);
+          bulk_load(Vs + stg * L::kStageElems, vbase + seq_base + (size_t)tok0 * D, bytes,
+                    &full[stg], policy);
+        }
+        __syncwarp();
+      }
+      return;
+    }
     const int log2B = p.log2_block;
     const int lb_last = (t_end - 1) >> log2B;
     const int32_t* trow = p.block_tables + (size_t)s * p.max_blocks_per_seq;
-    const T* kbase = static_cast<const T*>(p.k_cache);
-    const T* vbase = static_cast<const T*>(p.v_cache);
     const size_t tile = (size_t)p.block_size * D;  // elements of one (block, head) tile
     int chunk_base = -1;
     for (int it = 0; it < nstages; ++it) {
@@ -175,10 +247,10 @@ __global__ void __launch_bounds__(kThreads, GT >= 4 ? 2 : 3)
   }
 
   // ----------------------------------------------------------- consumers --
-  const int grp = lane >> 3;  // which of the 4 rows of a pass this lane reads
-  const int gi = lane & 7;    // position inside the 8-lane row group
+  const int rg = lane >> LBL;        // row group: which row of a pass this lane reads
+  const int li = lane & (LPR - 1);   // position inside the row group
 
-  // q for this lane's columns {8*(gi + 8c) .. +7}, pre-scaled to base-2 logits.
+  // q for this lane's columns {8*(li + LPR*c) .. +7}, pre-scaled to base-2 logits.
   float2 qf[GT][NF2];
   {
     const T* qrow = static_cast<const T*>(p.q) + ((size_t)s * p.num_q_heads + h0) * D;
@@ -186,9 +258,9 @@ __global__ void __launch_bounds__(kThreads, GT >= 4 ? 2 : 3)
 #pragma unroll
     for (int g = 0; g < GT; ++g) {
 #pragma unroll
-      for (int c = 0; c < NCH; ++c) {
+      for (int c = 0; c < CPL; ++c) {
         uint4 w = make_uint4(0, 0, 0, 0);
-        if (g < nh) w = *reinterpret_cast<const uint4*>(qrow + g * D + (gi + 8 * c) * 8);
+        if (g < nh) w = *reinterpret_cast<const uint4*>(qrow + g * D + (li + LPR * c) * 8);
         qf[g][4 * c + 0] = __fmul2_rn(Cvt<T>::to_float2(w.x), sc);
         qf[g][4 * c + 1] = __fmul2_rn(Cvt<T>::to_float2(w.y), sc);
         qf[g][4 * c + 2] = __fmul2_rn(Cvt<T>::to_float2(w.z), sc);
@@ -205,9 +277,9 @@ __global__ void __launch_bounds__(kThreads, GT >= 4 ? 2 : 3)
   float m_run = -CUDART_INF_F;  // running max of this lane's head (base 2)
   float l_run = 0.f;            // running sum of exp2(logit - m_run)
 
-  const int idx_l = gi >> SH;  // (g * 2 + j) of the logit this lane ends up with
-  const int g_l = idx_l >> 1;
-  const int j_l = idx_l & 1;
+  const int idx_l = li >> SH;   // (g * NP + j) of the sum this lane ends up with
+  const int g_l = idx_l / NP;
+  const int j_l = idx_l % NP;
 
   for (int it = 0; it < nstages; ++it) {
     const int stg = it % NSTAGE;
@@ -216,16 +288,16 @@ __global__ void __launch_bounds__(kThreads, GT >= 4 ? 2 : 3)
     const T* Kst = Ks + stg * L::kStageElems;
     const T* Vst = Vs + stg * L::kStageElems;
 
-    // Partial dot products: this lane's 16 (D=128) or 8 (D=64) columns of
-    // rows warp*8 + j*4 + grp, for every head of the group.
+    // Partial dot products over this lane's columns of rows
+    // warp*RPW + j*RPP + rg, for every head of the group.
     float v[NV];
 #pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      const int row = warp * 8 + j * 4 + grp;
+    for (int j = 0; j < NP; ++j) {
+      const int row = warp * RPW + j * RPP + rg;
       float2 kf[NF2];
 #pragma unroll
-      for (int c = 0; c < NCH; ++c) {
-        const uint4 w = *reinterpret_cast<const uint4*>(Kst + row * D + (gi + 8 * c) * 8);
+      for (int c = 0; c < CPL; ++c) {
+        const uint4 w = *reinterpret_cast<const uint4*>(Kst + row * D + (li + LPR * c) * 8);
         kf[4 * c + 0] = Cvt<T>::to_float2(w.x);
         kf[4 * c + 1] = Cvt<T>::to_float2(w.y);
         kf[4 * c + 2] = Cvt<T>::to_float2(w.z);
@@ -236,15 +308,15 @@ __global__ void __launch_bounds__(kThreads, GT >= 4 ? 2 : 3)
         float2 a = __fmul2_rn(qf[g][0], kf[0]);
 #pragma unroll
         for (int e = 1; e < NF2; ++e) a = __ffma2_rn(qf[g][e], kf[e], a);
-        v[g * 2 + j] = a.x + a.y;
+        v[g * NP + j] = a.x + a.y;
       }
     }
-    // Transposed butterfly over the group's 8 lanes: each exchange halves the
-    // values a lane holds, so NV sums cost NV - 1 shuffles instead of 3 * NV.
+    // Transposed butterfly over the row group's lanes: each exchange halves
+    // the values a lane holds, so NV sums cost NV - 1 shuffles, not NV * LBL.
 #pragma unroll
-    for (int step = 0; step < LB; ++step) {
-      const int mk = 4 >> step;
-      const bool upper = (gi & mk) != 0;
+    for (int step = 0; step < H; ++step) {
+      const int mk = (LPR >> 1) >> step;
+      const bool upper = (li & mk) != 0;
       const int half = NV >> (step + 1);
 #pragma unroll
       for (int i = 0; i < half; ++i) {
@@ -255,25 +327,30 @@ __global__ void __launch_bounds__(kThreads, GT >= 4 ? 2 : 3)
     }
     float x = v[0];
 #pragma unroll
-    for (int mk = (4 >> LB); mk >= 1; mk >>= 1) x += __shfl_xor_sync(kFull, x, mk);
+    for (int mk = (1 << SH) >> 1; mk >= 1; mk >>= 1) x += __shfl_xor_sync(kFull, x, mk);
 
-    // Online softmax over the warp's 8 rows of this stage.
-    if (warp * 8 + j_l * 4 + grp >= ntok) x = -CUDART_INF_F;
-    float mt = fmaxf(x, __shfl_xor_sync(kFull, x, kTokMask));
-    mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 8));
-    mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, 16));
+    // Online softmax over the warp's rows of this stage: reduce over the
+    // lanes that hold the same head (pass bits, then row-group bits).
+    if (warp * RPW + j_l * RPP + rg >= ntok) x = -CUDART_INF_F;
+    float mt = x;
+#pragma unroll
+    for (int b = 0; b < LOG2NP; ++b) mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, (1 << SH) << b));
+#pragma unroll
+    for (int mk = LPR; mk < 32; mk <<= 1) mt = fmaxf(mt, __shfl_xor_sync(kFull, mt, mk));
     const float m_new = fmaxf(m_run, mt);
     const float alpha = (m_new == -CUDART_INF_F) ? 1.f : exp2f(m_run - m_new);
     const float pe = (x == -CUDART_INF_F) ? 0.f : exp2f(x - m_new);
-    float ps = pe + __shfl_xor_sync(kFull, pe, kTokMask);
-    ps += __shfl_xor_sync(kFull, ps, 8);
-    ps += __shfl_xor_sync(kFull, ps, 16);
+    float ps = pe;
+#pragma unroll
+    for (int b = 0; b < LOG2NP; ++b) ps += __shfl_xor_sync(kFull, ps, (1 << SH) << b);
+#pragma unroll
+    for (int mk = LPR; mk < 32; mk <<= 1) ps += __shfl_xor_sync(kFull, ps, mk);
     l_run = l_run * alpha + ps;
     m_run = m_new;
     if (__any_sync(kFull, alpha != 1.f)) {
 #pragma unroll
       for (int g = 0; g < GT; ++g) {
-        const float a = __shfl_sync(kFull, alpha, (g * 2) << SH);
+        const float a = __shfl_sync(kFull, alpha, (g * NP) << SH);
         const float2 a2 = make_float2(a, a);
 #pragma unroll
         for (int e = 0; e < NF2; ++e) acc[g][e] = __fmul2_rn(acc[g][e], a2);
@@ -282,16 +359,17 @@ __global__ void __launch_bounds__(kThreads, GT >= 4 ? 2 : 3)
 
     // acc += p * V for this lane's row of each pass.
 #pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      const int row = warp * 8 + j * 4 + grp;
+    for (int j = 0; j < NP; ++j) {
+      const int row = warp * RPW + j * RPP + rg;
       float pg[GT];
 #pragma unroll
-      for (int g = 0; g < GT; ++g) pg[g] = __shfl_sync(kFull, pe, (grp << 3) | ((g * 2 + j) << SH));
+      for (int g = 0; g < GT; ++g)
+        pg[g] = __shfl_sync(kFull, pe, (rg << LBL) | ((g * NP + j) << SH));
       if (row < ntok) {
         float2 vf[NF2];
 #pragma unroll
-        for (int c = 0; c < NCH; ++c) {
-          const uint4 w = *reinterpret_cast<const uint4*>(Vst + row * D + (gi + 8 * c) * 8);
+        for (int c = 0; c < CPL; ++c) {
+          const uint4 w = *reinterpret_cast<const uint4*>(Vst + row * D + (li + LPR * c) * 8);
           vf[4 * c + 0] = Cvt<T>::to_float2(w.x);
           vf[4 * c + 1] = Cvt<T>::to_float2(w.y);
           vf[4 * c + 2] = Cvt<T>::to_float2(w.z);
@@ -309,46 +387,47 @@ __global__ void __launch_bounds__(kThreads, GT >= 4 ? 2 : 3)
     if (lane == 0) mbar_arrive(&empty[stg]);
   }
 
-  // The four row groups of a warp share its running max: add their sums.
+  // The row groups of a warp share its running max: add their sums.
 #pragma unroll
   for (int g = 0; g < GT; ++g)
 #pragma unroll
     for (int e = 0; e < NF2; ++e) {
       float2 a = acc[g][e];
-      a.x += __shfl_xor_sync(kFull, a.x, 8);
-      a.y += __shfl_xor_sync(kFull, a.y, 8);
-      a.x += __shfl_xor_sync(kFull, a.x, 16);
-      a.y += __shfl_xor_sync(kFull, a.y, 16);
+#pragma unroll
+      for (int mk = LPR; mk < 32; mk <<= 1) {
+        a.x += __shfl_xor_sync(kFull, a.x, mk);
+        a.y += __shfl_xor_sync(kFull, a.y, mk);
+      }
       acc[g][e] = a;
     }
-  if (grp == 0) {
+  if (rg == 0) {
 #pragma unroll
     for (int g = 0; g < GT; ++g)
 #pragma unroll
-      for (int c = 0; c < NCH; ++c) {
-        float4* dst = reinterpret_cast<float4*>(mg_acc + (warp * GT + g) * D + (gi + 8 * c) * 8);
+      for (int c = 0; c < CPL; ++c) {
+        float4* dst = reinterpret_cast<float4*>(mg_acc + (warp * GT + g) * D + (li + LPR * c) * 8);
         dst[0] = make_float4(acc[g][4 * c].x, acc[g][4 * c].y, acc[g][4 * c + 1].x, acc[g][4 * c + 1].y);
         dst[1] = make_float4(acc[g][4 * c + 2].x, acc[g][4 * c + 2].y, acc[g][4 * c + 3].x,
                              acc[g][4 * c + 3].y);
       }
-    if (j_l == 0 && (gi & (kTokMask - 1)) == 0) {
+    if (j_l == 0 && (li & ((1 << SH) - 1)) == 0) {
       mg_max[warp * GT + g_l] = m_run;
       mg_sum[warp * GT + g_l] = l_run;
     }
   }
-  named_barrier_sync(1, kConsumerWarps * 32);
+  named_barrier_sync(1, NCW * 32);
 
   // Merge the warps and write out (or the partition's partial result).
-  for (int e0 = threadIdx.x * 4; e0 < nh * D; e0 += kConsumerWarps * 32 * 4) {
+  for (int e0 = threadIdx.x * 4; e0 < nh * D; e0 += NCW * 32 * 4) {
     const int g = e0 / D;
     const int e = e0 - g * D;
     float M = -CUDART_INF_F;
 #pragma unroll
-    for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, mg_max[w * GT + g]);
+    for (int w = 0; w < NCW; ++w) M = fmaxf(M, mg_max[w * GT + g]);
     float Lsum = 0.f;
     float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-    for (int w = 0; w < kConsumerWarps; ++w) {
+    for (int w = 0; w < NCW; ++w) {
       const float mw = mg_max[w * GT + g];
       const float sc = (mw == -CUDART_INF_F) ? 0.f : exp2f(mw - M);
       Lsum += mg_sum[w * GT + g] * sc;
@@ -435,22 +514,42 @@ __global__ void __launch_bounds__(128) paged_decode_reduce_kernel(const DecodePa
   }
 }
 
-template <typename T, int D, int GT>
-cudaError_t launch_typed(const DecodeParams& p, cudaStream_t stream) {
+// Opt the kernel in to more than 48 KiB of dynamic shared memory, once per
+// device.
+template <typename T, int D, int GT, bool kPaged>
+cudaError_t configure() {
   using L = SmemLayout<T, D, GT>;
-  // Opt in to more than 48 KiB of dynamic shared memory, once per device.
   static unsigned long long configured = 0;  // bit per device ordinal (< 64)
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
   if (dev >= 64 || !(__atomic_load_n(&configured, __ATOMIC_ACQUIRE) & (1ull << dev))) {
-    err = cudaFuncSetAttribute(paged_decode_kernel<T, D, GT>,
+    err = cudaFuncSetAttribute(paged_decode_kernel<T, D, GT, kPaged>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::kBytes);
     if (err != cudaSuccess) return err;
     if (dev < 64) __atomic_fetch_or(&configured, 1ull << dev, __ATOMIC_RELEASE);
   }
+  return cudaSuccess;
+}
+
+template <typename T, int D, int GT>
+int ctas_per_sm_typed() {
+  using L = SmemLayout<T, D, GT>;
+  int n = 0;
+  if (configure<T, D, GT, true>() != cudaSuccess) return 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, paged_decode_kernel<T, D, GT, true>,
+                                                    L::kThreads, L::kBytes) != cudaSuccess)
+    return 0;
+  return n;
+}
+
+template <typename T, int D, int GT, bool kPaged>
+cudaError_t launch_typed(const DecodeParams& p, cudaStream_t stream) {
+  using L = SmemLayout<T, D, GT>;
+  cudaError_t err = configure<T, D, GT, kPaged>();
+  if (err != cudaSuccess) return err;
   const dim3 grid(p.num_parts, p.num_kv_heads * p.head_chunks, p.num_seqs);
-  paged_decode_kernel<T, D, GT><<<grid, kThreads, L::kBytes, stream>>>(p);
+  paged_decode_kernel<T, D, GT, kPaged><<<grid, L::kThreads, L::kBytes, stream>>>(p);
   err = cudaGetLastError();
   if (err != cudaSuccess || p.num_parts <= 1) return err;
   const int pairs = p.num_seqs * p.num_q_heads;
@@ -458,16 +557,37 @@ cudaError_t launch_typed(const DecodeParams& p, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
-template <typename T, int D>
+template <typename T, int D, bool kPaged>
 cudaError_t launch_for_group(const DecodeParams& p, int gt, cudaStream_t stream) {
   switch (gt) {
-    case 1: return launch_typed<T, D, 1>(p, stream);
-    case 2: return launch_typed<T, D, 2>(p, stream);
-    default: return launch_typed<T, D, 4>(p, stream);
+    case 1: return launch_typed<T, D, 1, kPaged>(p, stream);
+    case 2: return launch_typed<T, D, 2, kPaged>(p, stream);
+    default: return launch_typed<T, D, 4, kPaged>(p, stream);
   }
 }
 
+template <bool kPaged>
+cudaError_t launch_any(const DecodeParams& p, int dtype, int head_dim, int gt,
+                       cudaStream_t stream) {
+  if (dtype == PKV_F16) {
+    return head_dim == 64 ? launch_for_group<__half, 64, kPaged>(p, gt, stream)
+                          : launch_for_group<__half, 128, kPaged>(p, gt, stream);
+  }
+  return head_dim == 64 ? launch_for_group<__nv_bfloat16, 64, kPaged>(p, gt, stream)
+                        : launch_for_group<__nv_bfloat16, 128, kPaged>(p, gt, stream);
+}
+
 }  // namespace
+
+int decode_ctas_per_sm(int head_dim, int gt) {
+  // Occupancy depends on sizes only; both element types have the same.
+  if (head_dim == 64) {
+    return gt == 1 ? ctas_per_sm_typed<__half, 64, 1>()
+                   : (gt == 2 ? ctas_per_sm_typed<__half, 64, 2>() : ctas_per_sm_typed<__half, 64, 4>());
+  }
+  return gt == 1 ? ctas_per_sm_typed<__half, 128, 1>()
+                 : (gt == 2 ? ctas_per_sm_typed<__half, 128, 2>() : ctas_per_sm_typed<__half, 128, 4>());
+}
 
 int decode_heads_per_cta(int group) { return group == 1 ? 1 : (group == 2 ? 2 : 4); }
 
@@ -483,12 +603,12 @@ size_t decode_smem_bytes(int head_dim, int gt) {
 
 cudaError_t launch_paged_decode(const DecodeParams& p, int dtype, int head_dim, int gt,
                                 cudaStream_t stream) {
-  if (dtype == PKV_F16) {
-    return head_dim == 64 ? launch_for_group<__half, 64>(p, gt, stream)
-                          : launch_for_group<__half, 128>(p, gt, stream);
-  }
-  return head_dim == 64 ? launch_for_group<__nv_bfloat16, 64>(p, gt, stream)
-                        : launch_for_group<__nv_bfloat16, 128>(p, gt, stream);
+  return launch_any<true>(p, dtype, head_dim, gt, stream);
+}
+
+cudaError_t launch_contiguous_decode(const DecodeParams& p, int dtype, int head_dim, int gt,
+                                     cudaStream_t stream) {
+  return launch_any<false>(p, dtype, head_dim, gt, stream);
 }
 
 }  // namespace pkv

@@ -38,12 +38,20 @@ struct DecodeParams {
 // Query heads one CTA processes for a group size (1, 2 or 4).
 int decode_heads_per_cta(int group);
 
+// Decode CTAs resident per SM on the current device (0 if unknown).
+int decode_ctas_per_sm(int head_dim, int heads_per_cta);
+
 // Shared memory one decode CTA uses.
 size_t decode_smem_bytes(int head_dim, int heads_per_cta);
 
 // Launch the decode kernel and, when num_parts > 1, the reduction kernel.
 cudaError_t launch_paged_decode(const DecodeParams& p, int dtype, int head_dim,
                                 int heads_per_cta, cudaStream_t stream);
+
+// Same kernels over a contiguous cache [S, Hkv, capacity, D]: block_size is
+// the capacity, block_tables is unused and sequence s reads rows of s.
+cudaError_t launch_contiguous_decode(const DecodeParams& p, int dtype, int head_dim,
+                                     int heads_per_cta, cudaStream_t stream);
 
 cudaError_t launch_kv_append(const void* k, const void* v, void* k_cache, void* v_cache,
                              const int64_t* slot_mapping, int num_tokens, int num_kv_heads,

@@ -86,6 +86,38 @@ def paged_attn_decode(out, q, k_cache, v_cache, block_tables, context_lens, scal
     return out
 
 
+def contiguous_attn_decode(out, q, k_cache, v_cache, context_lens, scale, partition_size=0,
+                           workspace=None):
+    """Decode over a contiguous cache ``[S, Hkv, capacity, D]`` (no block
+    table): the baseline the paged layout is compared with."""
+    _cuda(q, "q", ndim=3)
+    dtype = q.dtype
+    if dtype not in _DTYPE_CODE:
+        raise ValueError("q must be float16 or bfloat16")
+    _cuda(out, "out", dtype, 3)
+    _cuda(k_cache, "k_cache", dtype, 4)
+    _cuda(v_cache, "v_cache", dtype, 4)
+    _cuda(context_lens, "context_lens", torch.int32, 1)
+    S, Hq, D = q.shape
+    S2, Hkv, cap, D2 = k_cache.shape
+    if v_cache.shape != k_cache.shape or D2 != D or S2 != S or out.shape != q.shape:
+        raise ValueError("shape mismatch between q, out and the caches")
+    lib = _lib.load()
+    ws_bytes = decode_workspace_size(S, Hq, Hkv, D, cap, partition_size)
+    ws_ptr, ws_len = None, 0
+    if ws_bytes:
+        if workspace is None:
+            workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
+        _cuda(workspace, "workspace")
+        ws_ptr, ws_len = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    st = lib.pkv_contiguous_attn_decode(
+        out.data_ptr(), q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+        context_lens.data_ptr(), cap, S, Hq, Hkv, D, float(scale), _DTYPE_CODE[dtype],
+        int(partition_size), ws_ptr, ws_len, _stream_handle(q.device))
+    _lib.check(st, "pkv_contiguous_attn_decode")
+    return out
+
+
 def kv_append(k, v, k_cache, v_cache, slot_mapping):
     """Scatter token t's K/V ([T, Hkv, D]) into slot ``slot_mapping[t]`` (int64;
     negative = skip) of both caches."""

@@ -73,15 +73,29 @@ def test_decode_host_validation(lib, over, expect):
 
 
 def test_workspace_size_arithmetic(lib):
-    # 8 sequences, 32 heads, 32k context, 512-token partitions -> 64 parts
-    n = lib.pkv_decode_workspace_size(8, 32, 8, 128, 32768, 0)
-    assert n == 8 * 32 * 64 * (128 + 2) * 4
-    assert lib.pkv_decode_workspace_size(8, 32, 8, 128, 512, 0) == 0
+    # explicit partitions: 8 sequences, 32 heads, 32k context, 512 tokens -> 64 parts
+    assert lib.pkv_decode_workspace_size(8, 32, 8, 128, 32768, 512) == 8 * 32 * 64 * (128 + 2) * 4
     assert lib.pkv_decode_workspace_size(8, 32, 8, 128, 4096, 4096) == 0
     assert lib.pkv_decode_workspace_size(8, 32, 8, 128, 4097, 4096) == 8 * 32 * 2 * 130 * 4
     assert lib.pkv_decode_workspace_size(8, 32, 8, 96, 100, 0) == ctypes.c_size_t(-1).value
-    assert lib.pkv_decode_partition_size(8, 32, 8, 128, 100) == 128
-    assert lib.pkv_decode_partition_size(8, 32, 8, 128, 32768) == 512
+    assert lib.pkv_decode_workspace_size(8, 32, 8, 128, 100, 48) == ctypes.c_size_t(-1).value
+
+
+def test_auto_partition_policy(lib):
+    """Library choice (assumes a GB300: 152 SMs, 3 CTAs each, without a device)."""
+    part = lib.pkv_decode_partition_size
+    assert part(8, 32, 8, 128, 100) == 128          # short context: one partition
+    assert part(64, 40, 40, 128, 2048) == 2048      # 2560 units: enough CTAs unsplit
+    assert part(256, 32, 8, 128, 4096) == 2048      # long contexts: 2048-token partitions
+    assert part(8, 32, 8, 128, 32768) == 2048
+    assert part(8, 32, 8, 128, 1024) == 256         # 64 units: split finer to fill the GPU
+    assert part(64, 32, 8, 128, 1024) == 1024       # 512 units: not worth splitting 1k
+    for args in [(1, 1, 1, 64, 5), (3, 12, 4, 64, 100000), (200, 64, 8, 128, 777)]:
+        p = part(*args)
+        assert p > 0 and p % 32 == 0
+        ws = lib.pkv_decode_workspace_size(*args, 0)
+        parts = -(-args[4] // p)
+        assert ws == (0 if parts <= 1 else args[0] * args[1] * parts * (args[3] + 2) * 4)
 
 
 def test_append_and_copy_host_validation(lib):

@@ -49,14 +49,14 @@ def test_noalloc_matches_workspace_entry_point(lib, cuda_device):
                                [8192, 100, 5000, 7777, 1, 4096, 3000, 8000], pool_factor=1.1,
                                device=cuda_device)
     second = W.opt13b_layer_decode(device=cuda_device)
-    for case in (first, second):
+    for case, part in ((first, 0), (second, 512)):
         S, Hq, D = case.q.shape
         Hkv = case.k_cache.shape[1]
-        need = pkv.decode_workspace_size(S, Hq, Hkv, D, case.max_context_len)
+        need = pkv.decode_workspace_size(S, Hq, Hkv, D, case.max_context_len, part)
         assert 0 < need <= SCRATCH_BYTES
-        ref = _with_workspace(case)
+        ref = _with_workspace(case, part)
         out = torch.full_like(case.q, float("nan"))
-        assert _call_noalloc(lib, out, case) == 0
+        assert _call_noalloc(lib, out, case, part) == 0
         torch.cuda.synchronize()
         assert_within_tol(out, to_f64(ref), case.q.dtype, "noalloc vs workspace entry point")
     assert pkv.device_status(clear=True) == 0
