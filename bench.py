@@ -50,6 +50,8 @@ def parse_args():
     ap.add_argument("--workload", default="opt13b", choices=["opt13b", "gqa4k"])
     ap.add_argument("--partition", type=int, default=0, help="tokens per partition (0 = library)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--num-seqs", type=int, default=None,
+                    help="fewer sequences than the workload's (for profiler captures)")
     return ap.parse_args()
 
 
@@ -141,14 +143,14 @@ class ClockSampler:
 
 # -------------------------------------------------------------- workload --
 
-def make_workload(name, device):
+def make_workload(name, device, num_seqs=None):
     from paged_kv_cache_247_gb300 import workloads as W
     if name == "opt13b":
-        case = W.opt13b_layer_decode(device=device)
+        case = W.opt13b_layer_decode(device=device, num_seqs=num_seqs)
         desc = dict(W.OPT13B_LAYER)
         label = "OPT-13B-shaped layer decode + kv_append"
     else:
-        case = W.gqa_4k_decode(device=device)
+        case = W.gqa_4k_decode(device=device, num_seqs=num_seqs)
         desc = dict(W.GQA_4K)
         label = "GQA 32q/8kv decode, ctx 4096 + kv_append"
     S, Hq, D = case.q.shape
@@ -264,7 +266,7 @@ def run_reference(args, rank, world):
     if rank != 0:
         return
     from paged_kv_cache_247_gb300 import workloads as W
-    case, k_new, v_new, slots, desc, label = make_workload(args.workload, "cpu")
+    case, k_new, v_new, slots, desc, label = make_workload(args.workload, "cpu", args.num_seqs)
     # bounded so that the whole run stays within a few minutes (at least one
     # whole sequence per step)
     per_step = min(6.0, 150.0 / max(1, args.steps + args.warmup))
@@ -306,7 +308,7 @@ def run_ours(args, rank, world, local_rank):
         torch.distributed.barrier()
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
-    case, k_new, v_new, slots, desc, label = make_workload(args.workload, dev)
+    case, k_new, v_new, slots, desc, label = make_workload(args.workload, dev, args.num_seqs)
     S, Hq, D = case.q.shape
     Hkv = case.k_cache.shape[1]
     out = torch.empty_like(case.q)
