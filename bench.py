@@ -49,6 +49,8 @@ def parse_args():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="opt13b", choices=["opt13b", "gqa4k"])
     ap.add_argument("--partition", type=int, default=0, help="tokens per partition (0 = library)")
+    ap.add_argument("--path", default="fused", choices=["fused", "separate"],
+                    help="one fused append+decode launch, or kv_append then decode")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--num-seqs", type=int, default=None,
                     help="fewer sequences than the workload's (for profiler captures)")
@@ -316,18 +318,31 @@ def run_ours(args, rank, world, local_rank):
     workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
     part = args.partition or pkv.decode_partition_size(S, Hq, Hkv, D, case.max_context_len)
     split = -(-case.max_context_len // part) > 1
-    launches_per_step = 2 + (1 if split else 0)
     stream = torch.cuda.current_stream(dev)
 
-    def step():
-        pkv.kv_append(k_new, v_new, case.k_cache, case.v_cache, slots)
-        pkv.paged_attn_decode(out, case.q, case.k_cache, case.v_cache, case.block_tables,
-                              case.context_lens, case.scale, case.max_context_len,
-                              partition_size=args.partition, workspace=workspace)
+    def enqueue(path, qd, kd, vd, sd, td, ld, ev=None):
+        """One step on the stream: append the new token and attend."""
+        if path == "separate":
+            pkv.kv_append(kd, vd, case.k_cache, case.v_cache, sd)
+        if ev is not None:
+            ev[0].record(stream)
+        if path == "separate":
+            pkv.paged_attn_decode(out, qd, case.k_cache, case.v_cache, td, ld, case.scale,
+                                  case.max_context_len, partition_size=args.partition,
+                                  workspace=workspace)
+        else:
+            pkv.paged_attn_decode_append(out, qd, kd, vd, case.k_cache, case.v_cache, td, ld,
+                                         case.scale, case.max_context_len,
+                                         partition_size=args.partition, workspace=workspace)
+        if ev is not None:
+            ev[1].record(stream)
+
+    dev_args = (case.q, k_new, v_new, slots, case.block_tables, case.context_lens)
+    launches_per_step = (2 if args.path == "separate" else 1) + (1 if split else 0)
 
     pkv.device_status(clear=True)
     for _ in range(max(3, args.warmup)):
-        step()
+        enqueue(args.path, *dev_args)
     torch.cuda.synchronize()
 
     clocks = ClockSampler(dev.index if dev.index is not None else 0)
@@ -342,12 +357,7 @@ def run_ours(args, rank, world, local_rank):
     time.sleep(0.3)  # let the sampler start before the timed region
     start.record(stream)
     for i in range(K):
-        pkv.kv_append(k_new, v_new, case.k_cache, case.v_cache, slots)
-        ev[i][0].record(stream)
-        pkv.paged_attn_decode(out, case.q, case.k_cache, case.v_cache, case.block_tables,
-                              case.context_lens, case.scale, case.max_context_len,
-                              partition_size=args.partition, workspace=workspace)
-        ev[i][1].record(stream)
+        enqueue(args.path, *dev_args, ev=ev[i])
     end.record(stream)
     torch.cuda.synchronize()
     clock_rec = clocks.stop()
@@ -364,6 +374,19 @@ def run_ours(args, rank, world, local_rank):
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
     elapsed_ms = float(t.item())
 
+    # The other path, briefly, for comparison (not the headline).
+    other = "separate" if args.path == "fused" else "fused"
+    n_alt = max(20, K // 10)
+    for _ in range(3):
+        enqueue(other, *dev_args)
+    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a0.record(stream)
+    for _ in range(n_alt):
+        enqueue(other, *dev_args)
+    a1.record(stream)
+    torch.cuda.synchronize()
+    alt = {"path": other, "ms_per_step": round(a0.elapsed_time(a1) / n_alt, 5), "steps": n_alt}
+
     # End to end through the C ABI with host buffers: every step copies its
     # inputs (q, new K/V, slots, tables, lengths) from pinned host memory and
     # reads the output back.
@@ -379,10 +402,8 @@ def run_ours(args, rank, world, local_rank):
     def e2e_step():
         for n, x in host.items():
             dev_in[n].copy_(x, non_blocking=True)
-        pkv.kv_append(dev_in["k"], dev_in["v"], case.k_cache, case.v_cache, dev_in["slots"])
-        pkv.paged_attn_decode(out, dev_in["q"], case.k_cache, case.v_cache, dev_in["tables"],
-                              dev_in["lens"], case.scale, case.max_context_len,
-                              partition_size=args.partition, workspace=workspace)
+        enqueue(args.path, dev_in["q"], dev_in["k"], dev_in["v"], dev_in["slots"],
+                dev_in["tables"], dev_in["lens"])
         out_host.copy_(out, non_blocking=True)
 
     for _ in range(3):
@@ -406,8 +427,16 @@ def run_ours(args, rank, world, local_rank):
     value = (decode_b + append_b) * world / (ms_step * 1e-3) / 1e9
     peak, peak_kind = peak_hbm()
     dec_ms = float(np.mean(decode_ms))
-    achieved = decode_b / (dec_ms * 1e-3) / 1e9
-    traffic = ncu_traffic("paged_decode_kernel", args.workload)
+    if args.path == "fused":
+        # the fused kernel also writes the new K/V rows (it reads them from
+        # the caller instead of the cache, the same bytes)
+        kernel_b = decode_b + 2 * S * Hkv * D * case.q.element_size()
+        kernel_name = "paged_attn_decode_append call (fused append + decode kernel"
+    else:
+        kernel_b = decode_b
+        kernel_name = "paged_attn_decode call (decode kernel"
+    achieved = kernel_b / (dec_ms * 1e-3) / 1e9
+    traffic = ncu_traffic(f"paged_decode_kernel:{args.path}", args.workload)
 
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
@@ -418,21 +447,23 @@ def run_ours(args, rank, world, local_rank):
                    "head_dim": D, "block_size": case.block_size,
                    "context_tokens": int(case.context_lens.sum().item()),
                    "max_context_len": case.max_context_len, "partition_size": part,
-                   "split": split, "l2": f"inputs larger than L2: {decode_b / 1e9:.2f} GB of "
+                   "split": split, "step": "fused append+decode launch" if args.path == "fused"
+                   else "kv_append then decode", "l2": f"inputs larger than L2: {decode_b / 1e9:.2f} GB of "
                    "K/V per step vs 129 MB L2, no flush", "parallelism": f"replicas x{world}"},
         "pct_of_peak": round(100.0 * value / world / peak, 2),
         "decode_seqs_per_s": round(S * world / (ms_step * 1e-3), 1),
-        "roofline": {"kernel": "paged_attn_decode call (decode kernel"
-                     + (" + split reduction)" if split else ")"),
+        "roofline": {"kernel": kernel_name + (" + split reduction)" if split else ")"),
                      "bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
                      "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_kind == "measured" else "fallback",
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "algorithmic_bytes_per_launch": decode_b,
+                     "algorithmic_bytes_per_launch": kernel_b,
                      "avg_launch_ms": round(dec_ms, 5)},
         "e2e": {"value": round((decode_b + append_b) * world / (e2e_ms * 1e-3) / 1e9, 2),
                 "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e_ms, 5)},
+        "path": args.path,
+        "other_path": alt,
         "contiguous_baseline": contig,
         "gpu_launches": K * launches_per_step,
         "clocks": clock_rec,

@@ -129,6 +129,37 @@ pkv_status_t pkv_paged_attn_decode(
     pkv_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * Fused decode step: append the step's new token, then attend.
+ *
+ * One decode step appends one token per sequence and attends over the whole
+ * context including it ([P2] "Why the KV cache is the thing that limits your
+ * batch": the cache grows token by token; [P2] "The page table, relocated
+ * into attention").  This call does both in one launch: for every sequence
+ * with context_lens[s] > 0 the new token is position ctx - 1 =
+ * context_lens[s] - 1, its slot is
+ *   block_tables[s][(ctx - 1) / B] * B + (ctx - 1) % B,
+ * and the call writes k_new[s][h][:] / v_new[s][h][:] there (bit-exact, as
+ * pkv_kv_append would) while the attention uses those rows directly.  The
+ * result equals pkv_kv_append followed by pkv_paged_attn_decode.
+ *
+ *   k_new, v_new  [num_seqs, num_kv_heads, head_dim] dtype, 16-byte aligned
+ *   k_cache/v_cache are written (one row per sequence and KV head)
+ * The slot's block must not be shared with another sequence (do the
+ * copy-on-write pkv_block_copy first, on the same stream).  Sequences with
+ * context_lens[s] == 0 append nothing.  Other arguments, results, workspace
+ * and errors as pkv_paged_attn_decode.
+ * ---------------------------------------------------------------------- */
+pkv_status_t pkv_paged_attn_decode_append(
+    void* out, const void* q, const void* k_new, const void* v_new,
+    void* k_cache, void* v_cache,
+    const int32_t* block_tables, int max_blocks_per_seq,
+    const int32_t* context_lens, int max_context_len,
+    int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+    int block_size, int num_blocks, float scale, pkv_dtype_t dtype,
+    int partition_size, void* workspace, size_t workspace_bytes,
+    pkv_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * Allocation-free decode.  (The source pages have no counterpart: this is an
  * interface for callers, not part of the method.)
  *

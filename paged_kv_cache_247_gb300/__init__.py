@@ -5,6 +5,8 @@ Device calls (hand-written CUDA behind the C ABI of ``libpagedkv.so``):
 * :func:`paged_attn_decode` — single-query decode attention walking each
   sequence's block table, with split-context partitions and GQA grouping;
 * :func:`kv_append` — scatter of each step's new K/V into its slot;
+* :func:`paged_attn_decode_append` — both in one launch (the new token is
+  written to its slot and used directly);
 * :func:`block_copy` — block-granular copy-on-write.
 
 Host: :class:`BlockAllocator`, the refcounted block allocator that decides
@@ -15,6 +17,7 @@ is no fallback: a missing library raises.
 from ._lib import PagedKVError, load as load_library  # noqa: F401
 from .ops import (  # noqa: F401
     paged_attn_decode,
+    paged_attn_decode_append,
     contiguous_attn_decode,
     kv_append,
     block_copy,

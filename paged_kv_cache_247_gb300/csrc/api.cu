@@ -160,14 +160,18 @@ size_t pkv_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads
   return (size_t)num_seqs * num_q_heads * parts * (head_dim + 2) * sizeof(float);
 }
 
-pkv_status_t pkv_paged_attn_decode(void* out, const void* q, const void* k_cache,
-                                   const void* v_cache, const int32_t* block_tables,
-                                   int max_blocks_per_seq, const int32_t* context_lens,
-                                   int max_context_len, int num_seqs, int num_q_heads,
-                                   int num_kv_heads, int head_dim, int block_size,
-                                   int num_blocks, float scale, pkv_dtype_t dtype,
-                                   int partition_size, void* workspace, size_t workspace_bytes,
-                                   pkv_stream_t stream) {
+namespace {
+
+// Shared body of the paged decode calls.  k_new/v_new (both or neither) are
+// the step's new-token rows [num_seqs, num_kv_heads, head_dim] for the fused
+// append.
+pkv_status_t paged_decode_impl(void* out, const void* q, const void* k_new, const void* v_new,
+                               void* k_cache, void* v_cache, const int32_t* block_tables,
+                               int max_blocks_per_seq, const int32_t* context_lens,
+                               int max_context_len, int num_seqs, int num_q_heads,
+                               int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                               float scale, pkv_dtype_t dtype, int partition_size,
+                               void* workspace, size_t workspace_bytes, pkv_stream_t stream) {
   if (!decode_shape_ok(num_seqs, num_q_heads, num_kv_heads, max_context_len))
     return PKV_ERR_INVALID_ARG;
   if (dtype != PKV_F16 && dtype != PKV_BF16) return PKV_ERR_INVALID_ARG;
@@ -184,6 +188,8 @@ pkv_status_t pkv_paged_attn_decode(void* out, const void* q, const void* k_cache
     return PKV_ERR_INVALID_ARG;
   if (max_blocks_per_seq <= 0 || num_blocks <= 0) return PKV_ERR_INVALID_ARG;
   if ((long long)max_blocks_per_seq * block_size < max_context_len) return PKV_ERR_INVALID_ARG;
+  if ((k_new == nullptr) != (v_new == nullptr)) return PKV_ERR_INVALID_ARG;
+  if (k_new && (!aligned16(k_new) || !aligned16(v_new))) return PKV_ERR_INVALID_ARG;
 
   const int group = num_q_heads / num_kv_heads;
   const int gt = pkv::decode_heads_per_cta(group);
@@ -201,6 +207,8 @@ pkv_status_t pkv_paged_attn_decode(void* out, const void* q, const void* k_cache
   p.q = q;
   p.k_cache = k_cache;
   p.v_cache = v_cache;
+  p.k_new = k_new;
+  p.v_new = v_new;
   p.block_tables = block_tables;
   p.context_lens = context_lens;
   p.max_blocks_per_seq = max_blocks_per_seq;
@@ -231,6 +239,40 @@ pkv_status_t pkv_paged_attn_decode(void* out, const void* q, const void* k_cache
   err = pkv::launch_paged_decode(p, dtype, head_dim, gt, reinterpret_cast<cudaStream_t>(stream));
   if (err != cudaSuccess) return cuda_fail(err);
   return PKV_OK;
+}
+
+}  // namespace
+
+pkv_status_t pkv_paged_attn_decode(void* out, const void* q, const void* k_cache,
+                                   const void* v_cache, const int32_t* block_tables,
+                                   int max_blocks_per_seq, const int32_t* context_lens,
+                                   int max_context_len, int num_seqs, int num_q_heads,
+                                   int num_kv_heads, int head_dim, int block_size,
+                                   int num_blocks, float scale, pkv_dtype_t dtype,
+                                   int partition_size, void* workspace, size_t workspace_bytes,
+                                   pkv_stream_t stream) {
+  // The caches are only read on this path.
+  return paged_decode_impl(out, q, nullptr, nullptr, const_cast<void*>(k_cache),
+                           const_cast<void*>(v_cache), block_tables, max_blocks_per_seq,
+                           context_lens, max_context_len, num_seqs, num_q_heads, num_kv_heads,
+                           head_dim, block_size, num_blocks, scale, dtype, partition_size,
+                           workspace, workspace_bytes, stream);
+}
+
+pkv_status_t pkv_paged_attn_decode_append(void* out, const void* q, const void* k_new,
+                                          const void* v_new, void* k_cache, void* v_cache,
+                                          const int32_t* block_tables, int max_blocks_per_seq,
+                                          const int32_t* context_lens, int max_context_len,
+                                          int num_seqs, int num_q_heads, int num_kv_heads,
+                                          int head_dim, int block_size, int num_blocks,
+                                          float scale, pkv_dtype_t dtype, int partition_size,
+                                          void* workspace, size_t workspace_bytes,
+                                          pkv_stream_t stream) {
+  if (num_seqs > 0 && (!k_new || !v_new)) return PKV_ERR_INVALID_ARG;
+  return paged_decode_impl(out, q, k_new, v_new, k_cache, v_cache, block_tables,
+                           max_blocks_per_seq, context_lens, max_context_len, num_seqs,
+                           num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale,
+                           dtype, partition_size, workspace, workspace_bytes, stream);
 }
 
 pkv_status_t pkv_contiguous_attn_decode(void* out, const void* q, const void* k_cache,

@@ -202,6 +202,20 @@ __global__ void __launch_bounds__(SmemLayout<T, D, GT>::kThreads, LayoutFor<D, G
     const int32_t* trow = p.block_tables + (size_t)s * p.max_blocks_per_seq;
     const size_t tile = (size_t)p.block_size * D;  // elements of one (block, head) tile
     int chunk_base = -1;
+    // Fused append: the step's new token is position ctx - 1, the last row of
+    // this partition when t_end == ctx.  Its K (lanes 0..kRowChunks-1) and V
+    // (the next kRowChunks lanes) 16-byte chunks are fetched now so that the
+    // load overlaps the pipeline.
+    constexpr int kRowChunks = D * (int)sizeof(T) / 16;  // 16-byte chunks per row
+    const bool fused_here = p.k_new != nullptr && t_end == ctx;
+    const bool new_is_v = lane >= kRowChunks;
+    const int new_c = new_is_v ? lane - kRowChunks : lane;
+    uint4 new_chunk = make_uint4(0, 0, 0, 0);
+    if (fused_here && lane < 2 * kRowChunks) {
+      const size_t row_off = ((size_t)s * p.num_kv_heads + kvh) * D;
+      new_chunk = reinterpret_cast<const uint4*>(
+          static_cast<const T*>(new_is_v ? p.v_new : p.k_new) + row_off)[new_c];
+    }
     for (int it = 0; it < nstages; ++it) {
       const int stg = it % NSTAGE;
       if (it >= NSTAGE && !mbar_wait_warp(&empty[stg], ((it / NSTAGE) - 1) & 1, p.status)) break;
@@ -227,14 +241,38 @@ __global__ void __launch_bounds__(SmemLayout<T, D, GT>::kThreads, LayoutFor<D, G
         }
         __syncwarp();
       }
-      if (lane == 0) mbar_arrive_expect_tx(&full[stg], (uint32_t)ntok * D * sizeof(T) * 2);
+      // Fused append: the last row of the sequence's last stage comes from
+      // the prefetched new row instead of the cache (the CTA of the first
+      // head chunk also writes it to its slot); the cache copy stops one row
+      // short.
+      int copy_end = tok0 + ntok;
+      if (fused_here && copy_end == ctx) {
+        copy_end -= 1;
+        if (lane < 2 * kRowChunks) {
+          T* srow = (new_is_v ? Vs : Ks) + stg * L::kStageElems + (ntok - 1) * D;
+          reinterpret_cast<uint4*>(srow)[new_c] = new_chunk;
+          if (hc == 0) {
+            const int pos = ctx - 1;
+            const int lbn = pos >> log2B;
+            const size_t dst = ((size_t)tbl[lbn - chunk_base] * p.num_kv_heads + kvh) * tile +
+                               (size_t)(pos - (lbn << log2B)) * D;
+            T* cache = const_cast<T*>(new_is_v ? vbase : kbase);
+            reinterpret_cast<uint4*>(cache + dst)[new_c] = new_chunk;
+          }
+        }
+        __threadfence_block();
+      }
+      __syncwarp();
+      if (lane == 0)
+        mbar_arrive_expect_tx(&full[stg], (uint32_t)(copy_end - tok0) * D * sizeof(T) * 2);
       __syncwarp();
       // One copy per block the stage touches; rows past the context are not
       // copied, so positions beyond context_lens are never read.
-      if (lane <= lb1 - lb0) {
+      const int lbc = copy_end > tok0 ? ((copy_end - 1) >> log2B) : lb0 - 1;
+      if (lane <= lbc - lb0) {
         const int lb = lb0 + lane;
         const int seg0 = max(tok0, lb << log2B);
-        const int seg1 = min(tok0 + ntok, (lb + 1) << log2B);
+        const int seg1 = min(copy_end, (lb + 1) << log2B);
         const size_t off = ((size_t)tbl[lb - chunk_base] * p.num_kv_heads + kvh) * tile +
                            (size_t)(seg0 - (lb << log2B)) * D;
         const uint32_t bytes = (uint32_t)(seg1 - seg0) * D * sizeof(T);

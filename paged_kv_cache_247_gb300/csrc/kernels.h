@@ -14,6 +14,8 @@ struct DecodeParams {
   const void* q;              // [S, Hq, D]
   const void* k_cache;        // [NB, Hkv, B, D]
   const void* v_cache;        // [NB, Hkv, B, D]
+  const void* k_new;          // fused append only: [S, Hkv, D] rows of position ctx - 1
+  const void* v_new;          // (nullptr: plain decode)
   const int32_t* block_tables;  // [S, max_blocks_per_seq]
   const int32_t* context_lens;  // [S]
   float* ws_o;                // split only: [S, Hq, num_parts, D]

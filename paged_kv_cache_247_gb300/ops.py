@@ -86,6 +86,46 @@ def paged_attn_decode(out, q, k_cache, v_cache, block_tables, context_lens, scal
     return out
 
 
+def paged_attn_decode_append(out, q, k_new, v_new, k_cache, v_cache, block_tables,
+                             context_lens, scale, max_context_len, partition_size=0,
+                             workspace=None):
+    """One fused decode step: write each sequence's new token (``k_new``,
+    ``v_new`` [S, Hkv, D], position ``context_lens[s] - 1``) into its slot and
+    attend over the whole context in the same launch."""
+    _cuda(q, "q", ndim=3)
+    dtype = q.dtype
+    if dtype not in _DTYPE_CODE:
+        raise ValueError("q must be float16 or bfloat16")
+    for t, name in ((out, "out"), (k_new, "k_new"), (v_new, "v_new")):
+        _cuda(t, name, dtype, 3)
+    _cuda(k_cache, "k_cache", dtype, 4)
+    _cuda(v_cache, "v_cache", dtype, 4)
+    _cuda(block_tables, "block_tables", torch.int32, 2)
+    _cuda(context_lens, "context_lens", torch.int32, 1)
+    S, Hq, D = q.shape
+    NB, Hkv, B, D2 = k_cache.shape
+    if (v_cache.shape != k_cache.shape or D2 != D or out.shape != q.shape
+            or k_new.shape != (S, Hkv, D) or v_new.shape != (S, Hkv, D)):
+        raise ValueError("shape mismatch between q, out, new rows and the caches")
+    if block_tables.shape[0] != S or context_lens.shape[0] != S:
+        raise ValueError("block_tables / context_lens must have one row per sequence")
+    lib = _lib.load()
+    ws_bytes = decode_workspace_size(S, Hq, Hkv, D, max_context_len, partition_size)
+    ws_ptr, ws_len = None, 0
+    if ws_bytes:
+        if workspace is None:
+            workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
+        _cuda(workspace, "workspace")
+        ws_ptr, ws_len = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    st = lib.pkv_paged_attn_decode_append(
+        out.data_ptr(), q.data_ptr(), k_new.data_ptr(), v_new.data_ptr(), k_cache.data_ptr(),
+        v_cache.data_ptr(), block_tables.data_ptr(), block_tables.shape[1],
+        context_lens.data_ptr(), int(max_context_len), S, Hq, Hkv, D, B, NB, float(scale),
+        _DTYPE_CODE[dtype], int(partition_size), ws_ptr, ws_len, _stream_handle(q.device))
+    _lib.check(st, "pkv_paged_attn_decode_append")
+    return out
+
+
 def contiguous_attn_decode(out, q, k_cache, v_cache, context_lens, scale, partition_size=0,
                            workspace=None):
     """Decode over a contiguous cache ``[S, Hkv, capacity, D]`` (no block
