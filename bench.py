@@ -49,7 +49,7 @@ def parse_args():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="opt13b", choices=["opt13b", "gqa4k"])
     ap.add_argument("--partition", type=int, default=0, help="tokens per partition (0 = library)")
-    ap.add_argument("--path", default="fused", choices=["fused", "separate"],
+    ap.add_argument("--path", default="separate", choices=["fused", "separate"],
                     help="one fused append+decode launch, or kv_append then decode")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--num-seqs", type=int, default=None,

@@ -21,7 +21,8 @@ Sources (cited by page title and section throughout):
 Modules:
 
 * :mod:`oracle.facts` — closed-form byte and block counts.
-* :mod:`oracle.attention` — paged single-query decode attention in fp64.
+* :mod:`oracle.attention` — paged single-query decode attention and paged
+  multi-query (chunked prompt) attention in fp64.
 * :mod:`oracle.cache_ops` — the slot scatter (append) and block copy.
 * :mod:`oracle.allocator` — a pure-Python refcounted block allocator model.
 
@@ -35,6 +36,7 @@ from .facts import (  # noqa: F401
     blocks_for_tokens,
     unused_tail_slots,
 )
-from .attention import paged_decode_attention, gather_sequence_kv  # noqa: F401
+from .attention import (  # noqa: F401
+    paged_decode_attention, paged_prefill_attention, gather_sequence_kv)
 from .cache_ops import kv_append, block_copy  # noqa: F401
 from .allocator import OracleAllocator, OracleOutOfBlocks  # noqa: F401

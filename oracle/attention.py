@@ -95,3 +95,44 @@ def paged_decode_attention(q, k_cache, v_cache, block_tables, context_lens, scal
             weights /= weights.sum()
             out[s, h] = weights @ v_seq[:, kvh, :]
     return out
+
+
+def paged_prefill_attention(q, k_cache, v_cache, block_tables, context_lens, query_start, scale):
+    """Multi-query (chunked prompt) attention over a paged cache, in fp64.
+
+    Sequence s contributes ``L_s = query_start[s+1] - query_start[s]`` query
+    rows ``q[query_start[s] : query_start[s+1]]``: the last L_s positions of
+    its context, whose K/V are already in the cache.  Query j sits at position
+    ``p = context_lens[s] - L_s + j`` and attends to positions ``0 .. p``
+    (causal), through the block table as in decode.  This is prompt processing
+    in chunks ("The KV cache is a systems problem", section "Memory savings
+    change the scheduling question": prompt chunks share the step budget with
+    decoding); with L_s = 1 it is one decode step.
+
+    Args:
+      q: ``[total_queries, num_q_heads, head_dim]``.
+      query_start: ``[num_seqs + 1]`` non-decreasing offsets, ``query_start[0] = 0``.
+      context_lens: ``[num_seqs]`` with ``context_lens[s] >= L_s``.
+    Returns ``[total_queries, num_q_heads, head_dim]`` float64.
+    """
+    q = np.asarray(q)
+    total, num_q_heads, head_dim = q.shape
+    group = num_q_heads // k_cache.shape[1]
+    out = np.zeros((total, num_q_heads, head_dim))
+    for s in range(len(context_lens)):
+        q0, q1 = int(query_start[s]), int(query_start[s + 1])
+        n_q, ctx = q1 - q0, int(context_lens[s])
+        if n_q == 0:
+            continue
+        if n_q > ctx:
+            raise ValueError("a chunk cannot be longer than its context")
+        k_seq, v_seq = gather_sequence_kv(k_cache, v_cache, block_tables[s], ctx)
+        for j in range(n_q):
+            pos = ctx - n_q + j
+            for h in range(num_q_heads):
+                kvh = h // group
+                logits = scale * (k_seq[:pos + 1, kvh, :] @ q[q0 + j, h].astype(np.float64))
+                weights = np.exp(logits - logits.max())
+                weights /= weights.sum()
+                out[q0 + j, h] = weights @ v_seq[:pos + 1, kvh, :]
+    return out

@@ -246,26 +246,30 @@ __global__ void __launch_bounds__(SmemLayout<T, D, GT>::kThreads, LayoutFor<D, G
       // head chunk also writes it to its slot); the cache copy stops one row
       // short.
       int copy_end = tok0 + ntok;
-      if (fused_here && copy_end == ctx) {
+      const bool new_row_stage = fused_here && copy_end == ctx;
+      if (new_row_stage) {
         copy_end -= 1;
         if (lane < 2 * kRowChunks) {
           T* srow = (new_is_v ? Vs : Ks) + stg * L::kStageElems + (ntok - 1) * D;
           reinterpret_cast<uint4*>(srow)[new_c] = new_chunk;
-          if (hc == 0) {
-            const int pos = ctx - 1;
-            const int lbn = pos >> log2B;
-            const size_t dst = ((size_t)tbl[lbn - chunk_base] * p.num_kv_heads + kvh) * tile +
-                               (size_t)(pos - (lbn << log2B)) * D;
-            T* cache = const_cast<T*>(new_is_v ? vbase : kbase);
-            reinterpret_cast<uint4*>(cache + dst)[new_c] = new_chunk;
-          }
         }
+        // Only shared-memory stores are outstanding here, so this fence is
+        // cheap; the global store of the row into its slot comes after the
+        // arrive, off the consumers' path.
         __threadfence_block();
       }
       __syncwarp();
       if (lane == 0)
         mbar_arrive_expect_tx(&full[stg], (uint32_t)(copy_end - tok0) * D * sizeof(T) * 2);
       __syncwarp();
+      if (new_row_stage && hc == 0 && lane < 2 * kRowChunks) {
+        const int pos = ctx - 1;
+        const int lbn = pos >> log2B;
+        const size_t dst = ((size_t)tbl[lbn - chunk_base] * p.num_kv_heads + kvh) * tile +
+                           (size_t)(pos - (lbn << log2B)) * D;
+        T* cache = const_cast<T*>(new_is_v ? vbase : kbase);
+        reinterpret_cast<uint4*>(cache + dst)[new_c] = new_chunk;
+      }
       // One copy per block the stage touches; rows past the context are not
       // copied, so positions beyond context_lens are never read.
       const int lbc = copy_end > tok0 ? ((copy_end - 1) >> log2B) : lb0 - 1;

@@ -356,3 +356,85 @@ def test_block_copy_copies_exact_bytes():
         assert np.array_equal(v2[dst].view(np.uint16), vc[src].view(np.uint16))
     for b in (1, 2, 3, 4, 6, 7):
         assert np.array_equal(k2[b].view(np.uint16), kc[b].view(np.uint16))
+
+
+# ------------------------------------------------------ chunked prompt ----
+
+def _prefill_batch(seed, lens, chunks, hq, hkv, d, block_size):
+    rng = np.random.default_rng(seed)
+    ks = [rng.standard_normal((n, hkv, d)) for n in lens]
+    vs = [rng.standard_normal((n, hkv, d)) for n in lens]
+    kc, vc, tables = _pool_from_contiguous(rng, ks, vs, block_size)
+    qs = np.concatenate([[0], np.cumsum(chunks)]).astype(np.int64)
+    q = rng.standard_normal((int(qs[-1]), hq, d))
+    return q, ks, vs, kc, vc, tables, qs
+
+
+def _sdpa_prefill(q, ks, vs, lens, qs, scale):
+    """torch SDPA with an explicit causal-with-offset mask, per sequence."""
+    out = np.zeros_like(q)
+    for s in range(len(lens)):
+        q0, q1 = qs[s], qs[s + 1]
+        n_q, n = q1 - q0, lens[s]
+        if n_q == 0:
+            continue
+        qt = torch.from_numpy(q[q0:q1]).permute(1, 0, 2).unsqueeze(0)      # [1, Hq, L, d]
+        k = torch.from_numpy(ks[s]).permute(1, 0, 2).unsqueeze(0)           # [1, Hkv, n, d]
+        v = torch.from_numpy(vs[s]).permute(1, 0, 2).unsqueeze(0)
+        pos = torch.arange(n - n_q, n).unsqueeze(1)
+        mask = torch.arange(n).unsqueeze(0) <= pos                           # [L, n]
+        o = F.scaled_dot_product_attention(qt, k, v, attn_mask=mask, scale=scale, enable_gqa=True)
+        out[q0:q1] = o[0].permute(1, 0, 2).numpy()
+    return out
+
+
+@pytest.mark.parametrize("hq,hkv,d,B", [(4, 4, 16, 4), (8, 2, 32, 16), (6, 3, 8, 8)])
+def test_prefill_equals_masked_sdpa(hq, hkv, d, B):
+    lens = [1, 9, 33, 64, 100]
+    chunks = [1, 9, 5, 64, 17]  # whole prompt, partial chunks, one token
+    q, ks, vs, kc, vc, tables, qs = _prefill_batch(hq * 10 + B, lens, chunks, hq, hkv, d, B)
+    got = oracle.paged_prefill_attention(q, kc, vc, tables, lens, qs, 0.3)
+    np.testing.assert_allclose(got, _sdpa_prefill(q, ks, vs, lens, qs, 0.3), rtol=1e-10, atol=1e-12)
+
+
+def test_prefill_whole_prompt_is_causal_attention():
+    lens = [40]
+    q, ks, vs, kc, vc, tables, qs = _prefill_batch(3, lens, [40], 4, 2, 16, 16)
+    got = oracle.paged_prefill_attention(q, kc, vc, tables, lens, qs, 0.25)
+    qt = torch.from_numpy(q).permute(1, 0, 2).unsqueeze(0)
+    k = torch.from_numpy(ks[0]).permute(1, 0, 2).unsqueeze(0)
+    v = torch.from_numpy(vs[0]).permute(1, 0, 2).unsqueeze(0)
+    ref = F.scaled_dot_product_attention(qt, k, v, is_causal=True, scale=0.25, enable_gqa=True)
+    np.testing.assert_allclose(got, ref[0].permute(1, 0, 2).numpy(), rtol=1e-10, atol=1e-12)
+
+
+def test_prefill_brute_force_tiny():
+    lens = [7, 12]
+    q, ks, vs, kc, vc, tables, qs = _prefill_batch(4, lens, [3, 5], 2, 1, 4, 4)
+    got = oracle.paged_prefill_attention(q, kc, vc, tables, lens, qs, 0.7)
+    for s in range(2):
+        for j in range(qs[s + 1] - qs[s]):
+            pos = lens[s] - (qs[s + 1] - qs[s]) + j
+            for h in range(2):
+                lg = [0.7 * sum(q[qs[s] + j, h, i] * ks[s][t, 0, i] for i in range(4)) for t in range(pos + 1)]
+                mx = max(lg)
+                w = [math.exp(x - mx) for x in lg]
+                for i in range(4):
+                    ref = sum(w[t] * vs[s][t, 0, i] for t in range(pos + 1)) / sum(w)
+                    assert abs(got[qs[s] + j, h, i] - ref) < 1e-12
+
+
+@pytest.mark.parametrize("old,new", [
+    ("logits = scale * (k_seq[:pos + 1, kvh, :]", "logits = scale * (k_seq[:pos, kvh, :]"),
+    ("out[q0 + j, h] = weights @ v_seq[:pos + 1, kvh, :]", "out[q0 + j, h] = weights @ v_seq[1:pos + 2, kvh, :]"),
+    ("pos = ctx - n_q + j", "pos = j"),
+])
+def test_prefill_planted_mistake_is_caught(old, new):
+    mod = _mutated_attention(old, new)
+    lens = [9, 33, 64]
+    q, ks, vs, kc, vc, tables, qs = _prefill_batch(12, lens, [9, 5, 17], 8, 2, 16, 16)
+    try:
+        got = mod.paged_prefill_attention(q, kc, vc, tables, lens, qs, 0.3)
+    except Exception:
+        return
+    assert not np.allclose(got, _sdpa_prefill(q, ks, vs, lens, qs, 0.3), rtol=1e-8, atol=1e-10)
