@@ -236,6 +236,42 @@ pkv_status_t pkv_contiguous_attn_decode(
     void* workspace, size_t workspace_bytes, pkv_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * Multi-query (chunked prompt) attention over the paged cache.
+ *
+ * Prompts are processed in chunks that share the step budget with decoding
+ * ([P3] "Memory savings change the scheduling question"); each chunk attends
+ * causally to the sequence's cached prefix and to itself, through the block
+ * table ([P2] "The page table, relocated into attention").
+ *
+ * Sequence s brings L_s = query_start[s+1] - query_start[s] query rows
+ * q[query_start[s] .. query_start[s+1]), the last L_s positions of its
+ * context: query j is position p = context_lens[s] - L_s + j, and its K/V
+ * (like every position < context_lens[s]) must already be in the cache
+ * (pkv_kv_append).  For every query head h:
+ *   out[query_start[s] + j][h] = softmax_{t <= p}(scale * q . K_s[t][h/G]) @ V_s[t][h/G]
+ * Q.K and P.V run on the tensor cores (fp32 accumulation); the softmax
+ * weights P are rounded to dtype before P.V, as the operand type requires.
+ *
+ *   q, out        [total_queries, num_q_heads, head_dim] dtype, total =
+ *                 query_start[num_seqs]
+ *   query_start   int32 [num_seqs + 1], non-decreasing, starting at 0
+ *   max_query_len host-side bound on L_s (sizes the grid)
+ *   context_lens  int32 [num_seqs] with L_s <= context_lens[s] <= max_context_len
+ *   num_q_heads / num_kv_heads <= 128
+ * Other arguments as pkv_paged_attn_decode.  Errors: PKV_ERR_INVALID_ARG,
+ * PKV_ERR_UNSUPPORTED (also when the caches cannot be described to the
+ * tensor-memory-access unit), PKV_ERR_CUDA.
+ * ---------------------------------------------------------------------- */
+pkv_status_t pkv_paged_attn_prefill(
+    void* out, const void* q, const int32_t* query_start, int max_query_len,
+    const void* k_cache, const void* v_cache,
+    const int32_t* block_tables, int max_blocks_per_seq,
+    const int32_t* context_lens, int max_context_len,
+    int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+    int block_size, int num_blocks, float scale, pkv_dtype_t dtype,
+    pkv_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * Append new tokens' K and V into their cache slots.
  *
  * The cache grows token by token ([P2] "Why the KV cache is the thing that

@@ -7,7 +7,9 @@ Device calls (hand-written CUDA behind the C ABI of ``libpagedkv.so``):
 * :func:`kv_append` — scatter of each step's new K/V into its slot;
 * :func:`paged_attn_decode_append` — both in one launch (the new token is
   written to its slot and used directly);
-* :func:`block_copy` — block-granular copy-on-write.
+* :func:`block_copy` — block-granular copy-on-write;
+* :func:`paged_attn_prefill` — causal multi-query (chunked prompt) attention
+  over the paged cache on the tcgen05 tensor cores.
 
 Host: :class:`BlockAllocator`, the refcounted block allocator that decides
 slots and copy-on-write pairs.  The library is loaded on first use and there
@@ -18,6 +20,7 @@ from ._lib import PagedKVError, load as load_library  # noqa: F401
 from .ops import (  # noqa: F401
     paged_attn_decode,
     paged_attn_decode_append,
+    paged_attn_prefill,
     contiguous_attn_decode,
     kv_append,
     block_copy,

@@ -51,6 +51,9 @@ SIGNATURES = {
     "pkv_contiguous_attn_decode": (c_int, [
         c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int,
         c_float, c_int, c_int, c_void_p, c_size_t, c_void_p]),
+    "pkv_paged_attn_prefill": (c_int, [
+        c_void_p, c_void_p, c_void_p, c_int, c_void_p, c_void_p, c_void_p, c_int, c_void_p,
+        c_int, c_int, c_int, c_int, c_int, c_int, c_int, c_float, c_int, c_void_p]),
     "pkv_decode_partition_size": (c_int, [c_int, c_int, c_int, c_int, c_int]),
     "pkv_decode_workspace_size": (c_size_t, [c_int, c_int, c_int, c_int, c_int, c_int]),
     "pkv_kv_append": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int,

@@ -342,6 +342,61 @@ pkv_status_t pkv_contiguous_attn_decode(void* out, const void* q, const void* k_
   return PKV_OK;
 }
 
+pkv_status_t pkv_paged_attn_prefill(void* out, const void* q, const int32_t* query_start,
+                                    int max_query_len, const void* k_cache, const void* v_cache,
+                                    const int32_t* block_tables, int max_blocks_per_seq,
+                                    const int32_t* context_lens, int max_context_len,
+                                    int num_seqs, int num_q_heads, int num_kv_heads,
+                                    int head_dim, int block_size, int num_blocks, float scale,
+                                    pkv_dtype_t dtype, pkv_stream_t stream) {
+  if (!decode_shape_ok(num_seqs, num_q_heads, num_kv_heads, max_context_len))
+    return PKV_ERR_INVALID_ARG;
+  if (dtype != PKV_F16 && dtype != PKV_BF16) return PKV_ERR_INVALID_ARG;
+  if (!isfinite(scale) || max_query_len < 0) return PKV_ERR_INVALID_ARG;
+  if (head_dim != 64 && head_dim != 128) return PKV_ERR_UNSUPPORTED;
+  if (!supported_block_size(block_size)) return PKV_ERR_UNSUPPORTED;
+  if (num_q_heads / num_kv_heads > 128) return PKV_ERR_UNSUPPORTED;
+  if (num_seqs == 0 || max_query_len == 0) return PKV_OK;
+  if (!out || !q || !query_start || !k_cache || !v_cache || !block_tables || !context_lens)
+    return PKV_ERR_INVALID_ARG;
+  if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
+    return PKV_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(block_tables) | reinterpret_cast<uintptr_t>(context_lens) |
+       reinterpret_cast<uintptr_t>(query_start)) & 3u)
+    return PKV_ERR_INVALID_ARG;
+  if (max_blocks_per_seq <= 0 || num_blocks <= 0) return PKV_ERR_INVALID_ARG;
+  if ((long long)max_blocks_per_seq * block_size < max_context_len) return PKV_ERR_INVALID_ARG;
+  if (num_seqs > 65535 || num_kv_heads > 65535) return PKV_ERR_UNSUPPORTED;
+  if ((long long)num_blocks * num_kv_heads * block_size > 0x7fffffffLL) return PKV_ERR_UNSUPPORTED;
+
+  pkv::PrefillArgs a{};
+  a.out = out;
+  a.q = q;
+  a.query_start = query_start;
+  a.max_query_len = max_query_len;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.block_tables = block_tables;
+  a.max_blocks_per_seq = max_blocks_per_seq;
+  a.context_lens = context_lens;
+  a.max_context_len = max_context_len;
+  a.num_seqs = num_seqs;
+  a.num_q_heads = num_q_heads;
+  a.num_kv_heads = num_kv_heads;
+  a.head_dim = head_dim;
+  a.block_size = block_size;
+  a.num_blocks = num_blocks;
+  a.scale = scale;
+  a.dtype = dtype;
+  cudaError_t err = status_word(&a.status);
+  if (err != cudaSuccess) return cuda_fail(err);
+  bool map_failed = false;
+  err = pkv::launch_paged_prefill(a, reinterpret_cast<cudaStream_t>(stream), &map_failed);
+  if (map_failed) return PKV_ERR_UNSUPPORTED;
+  if (err != cudaSuccess) return cuda_fail(err);
+  return PKV_OK;
+}
+
 pkv_status_t pkv_kv_append(const void* k, const void* v, void* k_cache, void* v_cache,
                            const int64_t* slot_mapping, int num_tokens, int num_kv_heads,
                            int head_dim, int block_size, int num_blocks, pkv_dtype_t dtype,

@@ -55,6 +55,32 @@ cudaError_t launch_paged_decode(const DecodeParams& p, int dtype, int head_dim,
 cudaError_t launch_contiguous_decode(const DecodeParams& p, int dtype, int head_dim,
                                      int heads_per_cta, cudaStream_t stream);
 
+// Multi-query (chunked prompt) attention over the paged cache.
+struct PrefillArgs {
+  void* out;
+  const void* q;
+  const int32_t* query_start;
+  int max_query_len;
+  const void* k_cache;
+  const void* v_cache;
+  const int32_t* block_tables;
+  int max_blocks_per_seq;
+  const int32_t* context_lens;
+  int max_context_len;
+  int num_seqs;
+  int num_q_heads;
+  int num_kv_heads;
+  int head_dim;
+  int block_size;
+  int num_blocks;
+  float scale;
+  int dtype;
+  unsigned int* status;
+};
+
+// map_failed is set when the tensor maps of the caches cannot be encoded.
+cudaError_t launch_paged_prefill(const PrefillArgs& a, cudaStream_t stream, bool* map_failed);
+
 cudaError_t launch_kv_append(const void* k, const void* v, void* k_cache, void* v_cache,
                              const int64_t* slot_mapping, int num_tokens, int num_kv_heads,
                              int head_dim, int block_size, int num_blocks,

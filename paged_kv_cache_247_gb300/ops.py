@@ -126,6 +126,37 @@ def paged_attn_decode_append(out, q, k_new, v_new, k_cache, v_cache, block_table
     return out
 
 
+def paged_attn_prefill(out, q, query_start, k_cache, v_cache, block_tables, context_lens, scale,
+                       max_context_len, max_query_len):
+    """Causal multi-query attention of each sequence's last L_s positions
+    (``q[query_start[s]:query_start[s+1]]``) over its paged context, on the
+    tensor cores.  Writes ``out`` ([total_queries, Hq, D]) and returns it."""
+    _cuda(q, "q", ndim=3)
+    dtype = q.dtype
+    if dtype not in _DTYPE_CODE:
+        raise ValueError("q must be float16 or bfloat16")
+    _cuda(out, "out", dtype, 3)
+    _cuda(k_cache, "k_cache", dtype, 4)
+    _cuda(v_cache, "v_cache", dtype, 4)
+    _cuda(block_tables, "block_tables", torch.int32, 2)
+    _cuda(context_lens, "context_lens", torch.int32, 1)
+    _cuda(query_start, "query_start", torch.int32, 1)
+    T, Hq, D = q.shape
+    NB, Hkv, B, D2 = k_cache.shape
+    S = context_lens.shape[0]
+    if v_cache.shape != k_cache.shape or D2 != D or out.shape != q.shape:
+        raise ValueError("shape mismatch between q, out and the caches")
+    if block_tables.shape[0] != S or query_start.shape[0] != S + 1:
+        raise ValueError("block_tables / query_start must match context_lens")
+    st = _lib.load().pkv_paged_attn_prefill(
+        out.data_ptr(), q.data_ptr(), query_start.data_ptr(), int(max_query_len),
+        k_cache.data_ptr(), v_cache.data_ptr(), block_tables.data_ptr(), block_tables.shape[1],
+        context_lens.data_ptr(), int(max_context_len), S, Hq, Hkv, D, B, NB, float(scale),
+        _DTYPE_CODE[dtype], _stream_handle(q.device))
+    _lib.check(st, "pkv_paged_attn_prefill")
+    return out
+
+
 def contiguous_attn_decode(out, q, k_cache, v_cache, context_lens, scale, partition_size=0,
                            workspace=None):
     """Decode over a contiguous cache ``[S, Hkv, capacity, D]`` (no block

@@ -1,0 +1,81 @@
+"""GPU parity of the tensor-core chunked-prompt (multi-query) attention.
+
+Each sequence's last L_s positions attend causally over its paged context;
+the kernel runs on tcgen05 with the softmax weights rounded to the operand
+type before P.V, so results are compared with the fp64 oracle under the
+same tolerances as decode.  Cases cover whole prompts, partial chunks, one
+query (which must agree with decode), several 128-row query tiles and
+128-key tiles, ragged and NaN-poisoned block tails, every block size and
+grouped heads."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_247_gb300 as pkv
+from paged_kv_cache_247_gb300 import workloads as W
+from _gpu_util import TOL, assert_within_tol, to_f64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _clean_status(lib, cuda_device):
+    pkv.device_status(clear=True)
+    yield
+    assert pkv.device_status(clear=True) == 0
+
+
+def _run(case, chunks, seed):
+    dev = case.q.device
+    S, Hq, D = case.q.shape
+    qs = np.concatenate([[0], np.cumsum(chunks)]).astype(np.int32)
+    gen = torch.Generator(device=dev).manual_seed(seed)
+    q = torch.randn((int(qs[-1]), Hq, D), generator=gen, device=dev).to(case.q.dtype)
+    out = torch.full_like(q, float("nan"))
+    pkv.paged_attn_prefill(out, q, torch.from_numpy(qs).to(dev), case.k_cache, case.v_cache,
+                           case.block_tables, case.context_lens, case.scale,
+                           case.max_context_len, int(max(chunks)))
+    torch.cuda.synchronize()
+    ref = oracle.paged_prefill_attention(to_f64(q), to_f64(case.k_cache), to_f64(case.v_cache),
+                                         case.block_tables.cpu().numpy(),
+                                         case.context_lens.cpu().numpy(), qs, case.scale)
+    return q, out, ref, qs
+
+
+@pytest.mark.parametrize("dtype,hq,hkv,D,B", [
+    ("bf16", 8, 8, 128, 16), ("fp16", 8, 8, 128, 16), ("bf16", 32, 8, 128, 16),
+    ("fp16", 16, 2, 64, 8), ("bf16", 12, 4, 128, 128), ("bf16", 6, 2, 64, 32),
+    ("fp16", 4, 4, 64, 64)])
+def test_prefill_matches_oracle(cuda_device, dtype, hq, hkv, D, B):
+    lens = [1, 17, 130, 300, 64, 257]
+    chunks = [1, 17, 130, 45, 1, 200]   # whole prompt, partial chunks, single queries
+    case = W.make_decode_case(hq * 3 + B, len(lens), hq, hkv, D, B, dtype, lens, pool_factor=1.3,
+                              poison=True, device=cuda_device)
+    q, out, ref, qs = _run(case, chunks, seed=B + hq)
+    assert_within_tol(out, ref, W.DTYPES[dtype], f"prefill {dtype} {hq}/{hkv} D={D} B={B}")
+
+
+def test_single_query_agrees_with_decode(cuda_device):
+    lens = [5, 700, 1500, 33]
+    case = W.make_decode_case(77, len(lens), 32, 8, 128, 16, "bf16", lens, pool_factor=1.2,
+                              device=cuda_device)
+    q, out, ref, qs = _run(case, [1] * len(lens), seed=3)
+    dec = torch.empty_like(q)
+    pkv.paged_attn_decode(dec, q, case.k_cache, case.v_cache, case.block_tables,
+                          case.context_lens, case.scale, case.max_context_len)
+    torch.cuda.synchronize()
+    assert_within_tol(out, ref, torch.bfloat16, "prefill L=1")
+    assert_within_tol(dec, ref, torch.bfloat16, "decode")
+
+
+def test_long_prompt_chunks(cuda_device):
+    """A 2,000-token prompt processed as chunks of 512 against a growing context."""
+    case = W.make_decode_case(5, 1, 32, 8, 128, 16, "bf16", [2000], pool_factor=1.0,
+                              device=cuda_device)
+    for done in (512, 1024, 1536, 2000):
+        chunk = min(512, done) if done < 2000 else 2000 - 1536
+        case.context_lens.fill_(done)
+        q, out, ref, qs = _run(case, [chunk], seed=done)
+        assert_within_tol(out, ref, torch.bfloat16, f"chunk ending at {done}")
