@@ -47,7 +47,7 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=5000)
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="opt13b", choices=["opt13b", "gqa4k"])
+    ap.add_argument("--workload", default="opt13b", choices=["opt13b", "gqa4k", "prefill"])
     ap.add_argument("--partition", type=int, default=0, help="tokens per partition (0 = library)")
     ap.add_argument("--path", default="separate", choices=["fused", "separate"],
                     help="one fused append+decode launch, or kv_append then decode")
@@ -478,6 +478,133 @@ def run_ours(args, rank, world, local_rank):
         print(json.dumps(line), flush=True)
 
 
+def prefill_flops(lens, chunks, num_q_heads, head_dim):
+    """Algorithmic FLOPs of causal chunked attention: every (query, key<=pos)
+    pair costs a D-long dot product and a D-long axpy (2 flops per MAC)."""
+    total = 0
+    for n, c in zip(lens, chunks):
+        first = n - c  # position of the chunk's first query
+        total += (c * (first + 1) + c * (c - 1) // 2) * num_q_heads * 4 * head_dim
+    return total
+
+
+def run_prefill(args, rank, world, local_rank):
+    import paged_kv_cache_247_gb300 as pkv
+    from paged_kv_cache_247_gb300 import build as _build
+    from paged_kv_cache_247_gb300 import workloads as W
+    if rank == 0 or not os.path.exists(_build.LIB):
+        _build.build_library()
+    if world > 1:
+        torch.distributed.barrier()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    w = W.PREFILL_CHUNKS
+    case, q, qs = W.prefill_chunks(device=dev, num_seqs=args.num_seqs)
+    S, Hq, D = q.shape[0] // w["chunk"], q.shape[1], q.shape[2]
+    out = torch.empty_like(q)
+    stream = torch.cuda.current_stream(dev)
+
+    def call(qd, od):
+        pkv.paged_attn_prefill(od, qd, qs, case.k_cache, case.v_cache, case.block_tables,
+                               case.context_lens, case.scale, case.max_context_len, w["chunk"])
+
+    pkv.device_status(clear=True)
+    for _ in range(max(3, args.warmup)):
+        call(q, out)
+    torch.cuda.synchronize()
+    K = args.steps
+    clocks = ClockSampler(dev.index if dev.index is not None else 0)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    a.record(stream)
+    for _ in range(K):
+        call(q, out)
+    b.record(stream)
+    torch.cuda.synchronize()
+    clock_rec = clocks.stop()
+    if pkv.device_status(clear=True):
+        raise RuntimeError("device status flags during the prefill bench")
+    ms = a.elapsed_time(b) / K
+    t = torch.tensor([ms], dtype=torch.float64)
+    if world > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    ms = float(t.item())
+    lens = case.context_lens.cpu().tolist()
+    flops = prefill_flops(lens, [w["chunk"]] * S, Hq, D)
+    tflops = flops / (ms * 1e-3) / 1e12
+    # MMA work actually issued: full 128x128 tiles up to each tile's last query
+    group = Hq // case.k_cache.shape[1]
+    gp = 1
+    while gp < group:
+        gp *= 2
+    qpt = 128 // gp
+    issued = 0
+    for n in lens:
+        for qt in range(-(-w["chunk"] // qpt)):
+            last = n - w["chunk"] + min(w["chunk"], (qt + 1) * qpt) - 1
+            issued += (last // 128 + 1) * 2 * 2 * 128 * 128 * D
+    issued *= case.k_cache.shape[1]
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peak, kind = float(json.load(f)["bf16_tflops"]), "measured (MEASURED_PEAKS.json bf16_tflops, burst)"
+    except (OSError, KeyError, ValueError):
+        peak, kind = 1900.0, "fallback"
+    # end to end: queries in from pinned host memory, output back, each step
+    q_host = q.cpu().pin_memory()
+    out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    q_dev = torch.empty_like(q)
+    n_e2e = max(5, K // 4)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(n_e2e):
+        q_dev.copy_(q_host, non_blocking=True)
+        call(q_dev, out)
+        out_host.copy_(out, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / n_e2e
+    line = {
+        "metric": "paged chunked-prefill attention TFLOP/s (causal, algorithmic)",
+        "value": round(tflops * world, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"chunked prefill: {S} seqs x {w['chunk']} queries over ctx "
+                   f"{w['ctx']}, 32q/8kv, D=128, B=16", "algorithmic_flops": flops,
+                   "mma_flops_issued": issued},
+        "roofline": {"kernel": "paged_prefill_kernel (tcgen05)", "bound": "tensor",
+                     "achieved": round(tflops, 2), "peak": peak, "peak_kind": kind,
+                     "unit": "TFLOP/s", "frac": round(tflops / peak, 4),
+                     "frac_issued": round(issued / (ms * 1e-3) / 1e12 / peak, 4),
+                     "traffic": None},
+        "e2e": {"value": round(flops / (e2e_ms * 1e-3) / 1e12 * world, 2), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": q_host.numel() * 2, "d2h_bytes_per_step": out_host.numel() * 2},
+        "gpu_launches": K, "clocks": clock_rec,
+    }
+    if rank == 0 and world == 1:
+        import oracle
+        n_q = 8
+        tables = case.block_tables.cpu().numpy()
+        nb = -(-lens[0] // case.block_size)
+        ids = torch.from_numpy(tables[0, :nb].astype(np.int64)).to(dev)
+        kc = case.k_cache.index_select(0, ids).float().cpu().numpy()
+        vc = case.v_cache.index_select(0, ids).float().cpu().numpy()
+        qq = q[w["chunk"] - n_q: w["chunk"]].float().cpu().numpy()
+        t0 = time.perf_counter()
+        oracle.paged_prefill_attention(qq, kc, vc, np.arange(nb)[None, :], [lens[0]],
+                                       np.array([0, n_q]), case.scale)
+        secs = time.perf_counter() - t0
+        f_sample = prefill_flops([lens[0]], [n_q], Hq, D)
+        line["cpu_baseline"] = {"value": round(f_sample / secs / 1e12, 6), "unit": "TFLOP/s",
+                                "cores": cores_used(), "kind": "oracle",
+                                "sample": f"the last {n_q} queries of one sequence, {secs:.2f} s"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -486,7 +613,14 @@ def main():
     if world > 1:
         torch.distributed.init_process_group("gloo")
     try:
-        if args.impl == "reference":
+        if args.workload == "prefill":
+            if args.impl == "reference":
+                if rank == 0:
+                    print(json.dumps({"impl": "reference", "unavailable":
+                                      "the reference arm is timed on the decode workloads"}))
+            else:
+                run_prefill(args, rank, world, local_rank)
+        elif args.impl == "reference":
             run_reference(args, rank, world)
         else:
             run_ours(args, rank, world, local_rank)

@@ -154,6 +154,39 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) 
       : "memory");
 }
 
+// Same load straight into float registers, and a wait that names them, so
+// that no use of the loaded values can be scheduled before the wait.
+__device__ __forceinline__ void tmem_ld32f(uint32_t taddr, float* v) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3]), "=f"(v[4]), "=f"(v[5]), "=f"(v[6]),
+        "=f"(v[7]), "=f"(v[8]), "=f"(v[9]), "=f"(v[10]), "=f"(v[11]), "=f"(v[12]), "=f"(v[13]),
+        "=f"(v[14]), "=f"(v[15]), "=f"(v[16]), "=f"(v[17]), "=f"(v[18]), "=f"(v[19]),
+        "=f"(v[20]), "=f"(v[21]), "=f"(v[22]), "=f"(v[23]), "=f"(v[24]), "=f"(v[25]),
+        "=f"(v[26]), "=f"(v[27]), "=f"(v[28]), "=f"(v[29]), "=f"(v[30]), "=f"(v[31])
+      : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_wait_ld_bind(float* v) {
+  asm volatile(
+      "tcgen05.wait::ld.sync.aligned;"
+      : "+f"(v[0]), "+f"(v[1]), "+f"(v[2]), "+f"(v[3]), "+f"(v[4]), "+f"(v[5]), "+f"(v[6]),
+        "+f"(v[7]), "+f"(v[8]), "+f"(v[9]), "+f"(v[10]), "+f"(v[11]), "+f"(v[12]), "+f"(v[13]),
+        "+f"(v[14]), "+f"(v[15]), "+f"(v[16]), "+f"(v[17]), "+f"(v[18]), "+f"(v[19]),
+        "+f"(v[20]), "+f"(v[21]), "+f"(v[22]), "+f"(v[23]), "+f"(v[24]), "+f"(v[25]),
+        "+f"(v[26]), "+f"(v[27]), "+f"(v[28]), "+f"(v[29]), "+f"(v[30]), "+f"(v[31])
+      :
+      : "memory");
+}
+
+// 2^x with the hardware approximation (MUFU.EX2, flush-to-zero).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
@@ -355,35 +388,54 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       tc_fence_after();
       float sv[kBN];
 #pragma unroll
-      for (int c = 0; c < kBN / 32; ++c) {
-        float t[32];
-        tmem_ld32(tmem_s + lane_base + c * 32, t);
-        tmem_wait_ld();  // the loaded registers are valid only after the wait
+      for (int c = 0; c < kBN / 32; ++c) tmem_ld32f(tmem_s + lane_base + c * 32, &sv[c * 32]);
 #pragma unroll
-        for (int k = 0; k < 32; ++k) sv[c * 32 + k] = t[k];
-      }
+      for (int c = 0; c < kBN / 32; ++c) tmem_wait_ld_bind(&sv[c * 32]);
       tc_fence_before();
       mbar_arrive(s_free);
 
-      // causal mask and online softmax (base 2)
+      // Causal mask, only on tiles where some row of the warp sees keys past
+      // its position (the diagonal); elsewhere every key is visible.
       const int key0 = i * kBN;
-      float mt = -CUDART_INF_F;
+      if (__any_sync(0xffffffffu, key0 + kBN - 1 > pos)) {
 #pragma unroll
-      for (int c = 0; c < kBN; ++c) {
-        const float x = (key0 + c <= pos) ? sv[c] * p.qscale : -CUDART_INF_F;
-        sv[c] = x;
-        mt = fmaxf(mt, x);
+        for (int c = 0; c < kBN; ++c)
+          if (key0 + c > pos) sv[c] = -CUDART_INF_F;
       }
-      const float m_new = fmaxf(m_run, mt);
-      const float alpha = (m_new == -CUDART_INF_F) ? 1.f : exp2f(m_run - m_new);
-      float rowsum = 0.f;
+      // Row max with 8 independent chains (scaling by qscale > 0 commutes).
+      float mx[8];
 #pragma unroll
-      for (int c = 0; c < kBN; ++c) {
-        const float e = (sv[c] == -CUDART_INF_F) ? 0.f : exp2f(sv[c] - m_new);
-        sv[c] = e;
-        rowsum += e;
+      for (int k = 0; k < 8; ++k) mx[k] = sv[k];
+#pragma unroll
+      for (int c = 8; c < kBN; ++c) mx[c & 7] = fmaxf(mx[c & 7], sv[c]);
+#pragma unroll
+      for (int k = 4; k >= 1; k >>= 1)
+#pragma unroll
+        for (int j = 0; j < k; ++j) mx[j] = fmaxf(mx[j], mx[j + k]);
+      const float mt = mx[0] * p.qscale;
+      // Lazy rescaling: the running max moves only when this tile exceeds it
+      // by more than 8 (base 2), so P stays <= 2^8 and O is rescaled rarely.
+      // Numerator and denominator share the same max, so the result is exact.
+      const float m_new = (mt > m_run + 8.f) ? mt : m_run;
+      const float alpha = (m_new == m_run) ? 1.f : ex2(m_run - m_new);
+      const float negm = (m_new == -CUDART_INF_F) ? 0.f : -m_new;
+      const float2 qs2 = make_float2(p.qscale, p.qscale);
+      const float2 nm2 = make_float2(negm, negm);
+      float sm[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) sm[k] = 0.f;
+#pragma unroll
+      for (int c = 0; c < kBN; c += 2) {
+        const float2 x = __ffma2_rn(make_float2(sv[c], sv[c + 1]), qs2, nm2);
+        sv[c] = ex2(x.x);
+        sv[c + 1] = ex2(x.y);
+        sm[(c >> 1) & 7] += sv[c] + sv[c + 1];
       }
-      l_run = l_run * alpha + rowsum;
+#pragma unroll
+      for (int k = 4; k >= 1; k >>= 1)
+#pragma unroll
+        for (int j = 0; j < k; ++j) sm[j] += sm[j + k];
+      l_run = l_run * alpha + sm[0];
       m_run = m_new;
 
       // P V of the previous tile must be done before P and O are touched.
@@ -391,13 +443,18 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         if (!mbar_wait_warp(o_done, (i - 1) & 1, p.status)) { ok = false; break; }
         tc_fence_after();
         if (__any_sync(0xffffffffu, alpha != 1.f)) {
+          const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll
           for (int c = 0; c < D / 32; ++c) {
             float t[32];
-            tmem_ld32(tmem_o + lane_base + c * 32, t);
-            tmem_wait_ld();
+            tmem_ld32f(tmem_o + lane_base + c * 32, t);
+            tmem_wait_ld_bind(t);
 #pragma unroll
-            for (int k = 0; k < 32; ++k) t[k] *= alpha;
+            for (int k = 0; k < 32; k += 2) {
+              const float2 y = __fmul2_rn(make_float2(t[k], t[k + 1]), a2);
+              t[k] = y.x;
+              t[k + 1] = y.y;
+            }
             tmem_st32(tmem_o + lane_base + c * 32, t);
           }
           tmem_wait_st();

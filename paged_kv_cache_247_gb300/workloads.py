@@ -209,3 +209,22 @@ def shared_prefix_prompts():
     """Prompt lengths of the parallel-sampling workload."""
     w = SHARED_PREFIX
     return context_lens_uniform(w["seed"], w["num_prompts"], w["prompt_lo"], w["prompt_hi"])
+
+
+PREFILL_CHUNKS = dict(num_seqs=8, num_q_heads=32, num_kv_heads=8, head_dim=128, block_size=16,
+                      dtype="bf16", ctx=4096, chunk=2048, seed=5)
+
+
+def prefill_chunks(device="cpu", num_seqs=None):
+    """Chunked prompt processing: each sequence's context is `ctx` tokens, the
+    last `chunk` of which are the queries (their K/V already cached)."""
+    w = PREFILL_CHUNKS
+    n = w["num_seqs"] if num_seqs is None else num_seqs
+    lens = np.full(n, w["ctx"], dtype=np.int64)
+    case = make_decode_case(w["seed"], n, w["num_q_heads"], w["num_kv_heads"], w["head_dim"],
+                            w["block_size"], w["dtype"], lens, pool_factor=1.0, device=device)
+    gen = torch.Generator(device=device)
+    gen.manual_seed(int(w["seed"]) * 31 + 7)
+    q = _randn((n * w["chunk"], w["num_q_heads"], w["head_dim"]), gen, device, DTYPES[w["dtype"]])
+    query_start = torch.arange(0, n + 1, dtype=torch.int32, device=device) * w["chunk"]
+    return case, q, query_start
