@@ -14,21 +14,28 @@
 // (query, head-of-group) pairs, so every head of a KV group shares each K/V
 // tile (grouped-query attention packs into the MMA's M dimension).
 //
-//   warp 4   producer: per key tile, reads the tile's block ids and loads
-//            every (block, head) run of K and V with 2-D TMA
-//            (cp.async.bulk.tensor, 128-byte swizzle) into a 2-stage ring.
-//   warp 5   MMA issuer (one thread): S = Q K^T into tensor memory, then,
+//   warps 8, 10  producers: per key tile, read the tile's block ids and
+//            load every (block, head) run of K (warp 8, 4-stage ring) and of
+//            V (warp 10, 3-stage ring) with 2-D TMA (cp.async.bulk.tensor,
+//            128-byte swizzle).
+//   warp 9   MMA issuer (one thread): S = Q K^T into tensor memory and,
 //            once the softmax warps have written P, O += P V (V as an
-//            MN-major operand); completion via tcgen05.commit on mbarriers.
+//            MN-major operand), each issued as soon as ready; completion via
+//            tcgen05.commit on mbarriers.
 //            The warp also allocates and frees the tensor memory.
-//   warps 0-3  softmax: thread r owns row r of S (tcgen05.ld), applies the
-//            causal mask, keeps the row's running max and sum in base 2,
-//            rescales its O row in tensor memory when the max grows, and
-//            writes its row of P (same 16-bit type as V) into shared memory
-//            in the swizzled K-major layout the next MMA reads.  At the end
-//            it divides O by the sum and stores the row.
+//   warps 0-7  softmax, two warpgroups: thread (wg, r) owns half of row r
+//            of S (tcgen05.ld), applies the causal mask, exchanges the
+//            half-row max through shared memory, keeps the running max and
+//            its half of the sum in base 2, rescales its half of the O row
+//            in tensor memory when the max grows, and writes its half of the
+//            P row (same 16-bit type as V) into shared memory in the
+//            swizzled K-major layout the next MMA reads.  At the end the two
+//            halves' sums are combined and each stores its half of O.
 //
-// Tensor memory: S in columns [0, 128), O in [128, 128 + D).
+// Tensor memory: two S buffers in columns [0, 128), O in [128, 128 + D).
+// Key tiles are 64 wide; S and P are double-buffered and K and V have rings
+// of their own, so the tensor core runs S_(i+1) and P_i V_i while the softmax
+// warps work on tiles i and i+1.
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -43,23 +50,34 @@ namespace pkv {
 namespace {
 
 constexpr int kBM = 128;  // rows of a tile: MMA M
-constexpr int kBN = 128;  // keys per tile: N of Q K^T, K of P V
-constexpr int kPrefillThreads = 192;
-constexpr int kKvStages = 2;
+constexpr int kBN = 64;   // keys per tile: N of Q K^T, K of P V
+constexpr int kSoftmaxWarps = 8;  // two warpgroups share each row (half the columns each)
+constexpr int kKProducerWarp = kSoftmaxWarps;
+constexpr int kMmaWarp = kSoftmaxWarps + 1;
+constexpr int kVProducerWarp = kSoftmaxWarps + 2;
+constexpr int kPrefillThreads = (kSoftmaxWarps + 3) * 32;
+constexpr int kSoftmaxThreads = kSoftmaxWarps * 32;
+constexpr int kKStages = 4;  // K is released as soon as its Q K^T is done,
+constexpr int kVStages = 3;  // V only after its P V: separate rings
+constexpr int kBufs = 2;   // S (tensor memory) and P (shared memory) are double-buffered
 constexpr int kTmemCols = 256;
-constexpr int kAtomBytes = kBM * 128;  // one 64-column (128-byte) swizzle region of 128 rows
+constexpr int kQAtom = kBM * 128;   // 64 columns (128 bytes) of the 128 query rows
+constexpr int kKvAtom = kBN * 128;  // 64 columns of the 64 key rows of a tile
+constexpr int kPBuf = kBM * 128;    // a [128 rows x 64 keys] P tile
 
 template <int D>
 struct PrefillSmem {
-  static constexpr int kAtoms = D / 64;                 // 64-column atoms per row
-  static constexpr int kTileBytes = kAtoms * kAtomBytes;  // a Q, K or V tile
+  static constexpr int kAtoms = D / 64;  // 64-column atoms per row
+  static constexpr int kKvTile = kAtoms * kKvAtom;
   static constexpr int kQ = 0;
-  static constexpr int kK = kQ + kTileBytes;
-  static constexpr int kV = kK + kKvStages * kTileBytes;
-  static constexpr int kP = kV + kKvStages * kTileBytes;  // [128 rows x 128 keys]
-  static constexpr int kBar = kP + 2 * kAtomBytes;
-  static constexpr int kTmemSlot = kBar + 16 * 8;
-  static constexpr int kBytes = kTmemSlot + 16 + 1024;    // + 1024-byte alignment slack
+  static constexpr int kK = kQ + kAtoms * kQAtom;
+  static constexpr int kV = kK + kKStages * kKvTile;
+  static constexpr int kP = kV + kVStages * kKvTile;
+  // row-max exchange [2 tiles][2 halves][128] and row-sum exchange [2][128] floats
+  static constexpr int kRed = kP + kBufs * kPBuf;
+  static constexpr int kBar = kRed + 3 * 2 * kBM * 4;
+  static constexpr int kTmemSlot = kBar + 32 * 8;
+  static constexpr int kBytes = kTmemSlot + 16 + 1024;  // + 1024-byte alignment slack
 };
 
 struct PrefillParams {
@@ -225,14 +243,17 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
   unsigned char* sV = smem + L::kV;
   unsigned char* sP = smem + L::kP;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBar);
-  uint64_t* kv_full = bars;         // [2]
-  uint64_t* kv_empty = bars + 2;    // [2]
-  uint64_t* q_full = bars + 4;
-  uint64_t* s_full = bars + 5;
-  uint64_t* s_free = bars + 6;
-  uint64_t* p_full = bars + 7;
-  uint64_t* o_done = bars + 8;
+  uint64_t* k_full = bars;         // [4] K stage landed (TMA transaction bytes)
+  uint64_t* k_empty = bars + 4;    // [4] K stage consumed by Q K^T (MMA commit)
+  uint64_t* v_full = bars + 8;     // [3] V stage landed
+  uint64_t* v_empty = bars + 11;   // [3] V stage consumed by P V
+  uint64_t* q_full = bars + 14;    // Q tile written (softmax threads)
+  uint64_t* s_full = bars + 15;    // [2] S buffer computed (MMA commit)
+  uint64_t* s_free = bars + 17;    // [2] S buffer read (softmax threads)
+  uint64_t* p_full = bars + 19;    // [2] P buffer written (softmax threads)
+  uint64_t* pv_done = bars + 21;   // [2] P V of that buffer finished (MMA commit)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kTmemSlot);
+  float* red = reinterpret_cast<float*>(smem + L::kRed);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -260,18 +281,24 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
   const int n_tiles = pos_max / kBN + 1;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kKvStages; ++i) {
-      mbar_init(&kv_full[i], 1);
-      mbar_init(&kv_empty[i], 1);
+    for (int i = 0; i < kKStages; ++i) {
+      mbar_init(&k_full[i], 1);
+      mbar_init(&k_empty[i], 1);
     }
-    mbar_init(q_full, kBM);
-    mbar_init(s_full, 1);
-    mbar_init(s_free, kBM);
-    mbar_init(p_full, kBM);
-    mbar_init(o_done, 1);
+    for (int i = 0; i < kVStages; ++i) {
+      mbar_init(&v_full[i], 1);
+      mbar_init(&v_empty[i], 1);
+    }
+    mbar_init(q_full, kSoftmaxThreads);
+    for (int b = 0; b < kBufs; ++b) {
+      mbar_init(&s_full[b], 1);
+      mbar_init(&s_free[b], kSoftmaxThreads);
+      mbar_init(&p_full[b], kSoftmaxThreads);
+      mbar_init(&pv_done[b], 1);
+    }
     fence_barrier_init();
   }
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_addr(tmem_slot)),
                  "r"(kTmemCols));
@@ -281,46 +308,54 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tmem_s = tmem;
-  const uint32_t tmem_o = tmem + kBN;
+  const uint32_t tmem_o = tmem + kBufs * kBN;  // S buffers at columns [0, 128)
 
-  if (warp == 4) {
-    // ------------------------------------------------------------ producer
+  if (warp == kKProducerWarp || warp == kVProducerWarp) {
+    // ----------------------------------------------------- K and V producers
+    // One warp streams K tiles, another V tiles, each into its own ring.
+    // Each tile's keys are loaded as runs of R rows; a run never crosses a
+    // block boundary (R divides both the block size and the tile).
+    const bool is_k = warp == kKProducerWarp;
+    const int nstages = is_k ? kKStages : kVStages;
+    uint64_t* full = is_k ? k_full : v_full;
+    uint64_t* empty = is_k ? k_empty : v_empty;
+    unsigned char* ring = is_k ? sK : sV;
+    const CUtensorMap* map = is_k ? &kmap : &vmap;
     const int B = p.block_size;
+    const int R = B < kBN ? B : kBN;
     const int32_t* trow = p.block_tables + (size_t)s * p.max_blocks_per_seq;
     for (int i = 0; i < n_tiles; ++i) {
-      const int st = i % kKvStages;
-      if (i >= kKvStages && !mbar_wait_warp(&kv_empty[st], ((i / kKvStages) - 1) & 1, p.status))
-        break;
+      const int st = i % nstages;
+      if (i >= nstages && !mbar_wait_warp(&empty[st], ((i / nstages) - 1) & 1, p.status)) break;
       const int key0 = i * kBN;
-      const int key_end = min(ctx, key0 + kBN);
-      const int lb0 = key0 / B;
-      const int nblk = (key_end - 1) / B - lb0 + 1;
-      int phys = 0;
-      if (lane < nblk) {
-        phys = __ldg(trow + lb0 + lane);
+      const int nvalid = min(ctx, key0 + kBN) - key0;
+      const int nseg = (nvalid + R - 1) / R;
+      int y = 0;
+      if (lane < nseg) {
+        const int key = key0 + lane * R;
+        int phys = __ldg(trow + key / B);
         if ((unsigned)phys >= (unsigned)p.num_blocks) {
           atomicOr(p.status, PKV_DEV_BAD_BLOCK_ID);
           phys = 0;
         }
+        y = (phys * p.num_kv_heads + kvh) * B + key % B;
       }
       if (lane == 0)
-        mbar_arrive_expect_tx(&kv_full[st], (uint32_t)nblk * B * D * (uint32_t)sizeof(T) * 2);
+        mbar_arrive_expect_tx(&full[st], (uint32_t)nseg * R * D * (uint32_t)sizeof(T));
       __syncwarp();
-      if (lane < nblk) {
-        const int y = (phys * p.num_kv_heads + kvh) * B;
-        const int row = lane * B;  // key row inside the tile
+      if (lane < nseg) {
 #pragma unroll
-        for (int a = 0; a < kAtoms; ++a) {
-          tma_load_2d(sK + st * L::kTileBytes + a * kAtomBytes + row * 128, &kmap, 64 * a, y,
-                      &kv_full[st]);
-          tma_load_2d(sV + st * L::kTileBytes + a * kAtomBytes + row * 128, &vmap, 64 * a, y,
-                      &kv_full[st]);
-        }
+        for (int a = 0; a < kAtoms; ++a)
+          tma_load_2d(ring + st * L::kKvTile + a * kKvAtom + lane * R * 128, map, 64 * a, y,
+                      &full[st]);
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == kMmaWarp) {
     // ------------------------------------------------------- MMA issuer
+    // Issues S_i = Q K_i^T and P_j V_j in order of i and of j, each as soon
+    // as its inputs are ready (polling, never blocking one on the other),
+    // so the tensor core computes the next scores while the softmax warps
+    // work on the previous tile and a late V never holds back Q K^T.
     if (lane == 0) {
       constexpr bool bf16 = std::is_same<T, __nv_bfloat16>::value;
       const uint32_t idesc_s = instr_desc(bf16, false, kBN, kBM);
@@ -328,91 +363,121 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       const uint32_t aQ = smem_addr(sQ), aK = smem_addr(sK), aV = smem_addr(sV),
                      aP = smem_addr(sP);
       bool ok = mbar_wait(q_full, 0, p.status);
-      for (int i = 0; ok && i < n_tiles; ++i) {
-        const int st = i % kKvStages;
-        if (!mbar_wait(&kv_full[st], (i / kKvStages) & 1, p.status)) break;
-        if (i > 0 && !mbar_wait(s_free, (i - 1) & 1, p.status)) break;
-        tc_fence_after();
-        // S = Q K^T over D in steps of 16 (4 steps per 64-column atom)
+      int next_s = 0, next_pv = 0;
+      unsigned long long idle_since = global_ns();
+      while (ok && next_pv < n_tiles) {
+        bool progressed = false;
+        if (next_s < n_tiles) {
+          const int i = next_s, st = i % kKStages, b = i % kBufs;
+          if (mbar_test_wait(&k_full[st], (i / kKStages) & 1) &&
+              (i < kBufs || mbar_test_wait(&s_free[b], ((i / kBufs) - 1) & 1))) {
+            tc_fence_after();
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t off = (ks / 4) * kAtomBytes + (ks % 4) * 32;
-          mma_f16(tmem_s, smem_desc(aQ + off, 16, 1024),
-                  smem_desc(aK + st * L::kTileBytes + off, 16, 1024), idesc_s, ks > 0);
+            for (int ks = 0; ks < D / 16; ++ks)
+              mma_f16(tmem + b * kBN,
+                      smem_desc(aQ + (ks / 4) * kQAtom + (ks % 4) * 32, 16, 1024),
+                      smem_desc(aK + st * L::kKvTile + (ks / 4) * kKvAtom + (ks % 4) * 32, 16,
+                                1024),
+                      idesc_s, ks > 0);
+            mma_commit(&s_full[b]);
+            mma_commit(&k_empty[st]);
+            ++next_s;
+            progressed = true;
+          }
         }
-        mma_commit(s_full);
-        if (!mbar_wait(p_full, i & 1, p.status)) break;
-        tc_fence_after();
-        // O += P V over the tile's 128 keys in steps of 16; V is read as an
-        // MN-major operand: 8-key groups 1024 B apart, 64-column atoms
-        // kAtomBytes apart.
+        if (next_pv < next_s) {
+          const int j = next_pv, bj = j % kBufs, stj = j % kVStages;
+          if (mbar_test_wait(&p_full[bj], (j / kBufs) & 1) &&
+              mbar_test_wait(&v_full[stj], (j / kVStages) & 1)) {
+            tc_fence_after();
+            // V as an MN-major operand: 8-key groups 1024 B apart, 64-column
+            // atoms kKvAtom apart.
 #pragma unroll
-        for (int ks = 0; ks < kBN / 16; ++ks) {
-          const uint32_t offp = (ks / 4) * kAtomBytes + (ks % 4) * 32;
-          mma_f16(tmem_o, smem_desc(aP + offp, 16, 1024),
-                  smem_desc(aV + st * L::kTileBytes + ks * 16 * 128, kAtomBytes, 1024), idesc_o,
-                  (i > 0 || ks > 0) ? 1u : 0u);
+            for (int ks = 0; ks < kBN / 16; ++ks)
+              mma_f16(tmem_o, smem_desc(aP + bj * kPBuf + ks * 32, 16, 1024),
+                      smem_desc(aV + stj * L::kKvTile + ks * 16 * 128, kKvAtom, 1024), idesc_o,
+                      (j > 0 || ks > 0) ? 1u : 0u);
+            mma_commit(&pv_done[bj]);
+            mma_commit(&v_empty[stj]);
+            ++next_pv;
+            progressed = true;
+          }
         }
-        mma_commit(o_done);
-        mma_commit(&kv_empty[st]);
+        if (progressed) {
+          idle_since = global_ns();
+        } else if (global_ns() - idle_since > kWaitLimitNs || timed_out(p.status)) {
+          atomicOr(p.status, PKV_DEV_WAIT_TIMEOUT);
+          ok = false;
+        }
       }
     }
     __syncwarp();
   } else {
     // ---------------------------------------------- softmax / epilogue (rows)
-    const int r = threadIdx.x;  // row of the tile == TMEM lane
+    // Thread (wg, r): row r of the tile, columns [wg * half, (wg + 1) * half)
+    // of S, P and O, with half = 32 keys of S/P and D / 2 columns of O.
+    constexpr int kHalfS = kBN / 2;
+    constexpr int kHalfO = D / 2;
+    const int wg = warp >> 2;
+    const int r = threadIdx.x & (kBM - 1);  // row of the tile == TMEM lane
     const int jq = j_first + r / Gp;
     const int g = r % Gp;
     const bool row_valid = (r / Gp) < qpt && jq < nq && g < G;
     const int pos = row_valid ? ctx - nq + jq : -1;
     const size_t row_elem =
         ((size_t)(q0 + (row_valid ? jq : 0)) * p.num_q_heads + kvh * G + (row_valid ? g : 0)) * D;
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
 
-    // Q row into the swizzled K-major tile (zeros for padding rows).
+    // This thread's half of the Q row into the swizzled K-major tile.
     {
       const uint4* src = reinterpret_cast<const uint4*>(static_cast<const T*>(p.q) + row_elem);
 #pragma unroll
-      for (int c = 0; c < D / 8; ++c) {
+      for (int c = wg * (D / 16); c < (wg + 1) * (D / 16); ++c) {
         const uint4 w = row_valid ? src[c] : make_uint4(0, 0, 0, 0);
-        *reinterpret_cast<uint4*>(sQ + (c / 8) * kAtomBytes + sw128_chunk(r, c % 8)) = w;
+        *reinterpret_cast<uint4*>(sQ + (c / 8) * kQAtom + sw128_chunk(r, c % 8)) = w;
       }
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       mbar_arrive(q_full);
     }
 
-    float m_run = -CUDART_INF_F, l_run = 0.f;
+    float m_run = -CUDART_INF_F, l_run = 0.f;  // l_run: this half's share of the row sum
     bool ok = true;
     for (int i = 0; i < n_tiles; ++i) {
-      if (!mbar_wait_warp(s_full, i & 1, p.status)) { ok = false; break; }
+      const int b = i % kBufs;
+      // A wait that gives up (never expected) leaves ok false and the loop
+      // running without further waits, so that both halves still meet at
+      // every named barrier below.
+      if (ok && !mbar_wait_warp(&s_full[b], (i / kBufs) & 1, p.status)) ok = false;
       tc_fence_after();
-      float sv[kBN];
-#pragma unroll
-      for (int c = 0; c < kBN / 32; ++c) tmem_ld32f(tmem_s + lane_base + c * 32, &sv[c * 32]);
-#pragma unroll
-      for (int c = 0; c < kBN / 32; ++c) tmem_wait_ld_bind(&sv[c * 32]);
+      float sv[kHalfS];
+      tmem_ld32f(tmem + b * kBN + wg * kHalfS + lane_base, sv);
+      tmem_wait_ld_bind(sv);
       tc_fence_before();
-      mbar_arrive(s_free);
+      mbar_arrive(&s_free[b]);
 
       // Causal mask, only on tiles where some row of the warp sees keys past
       // its position (the diagonal); elsewhere every key is visible.
-      const int key0 = i * kBN;
-      if (__any_sync(0xffffffffu, key0 + kBN - 1 > pos)) {
+      const int key0 = i * kBN + wg * kHalfS;
+      if (__any_sync(0xffffffffu, key0 + kHalfS - 1 > pos)) {
 #pragma unroll
-        for (int c = 0; c < kBN; ++c)
+        for (int c = 0; c < kHalfS; ++c)
           if (key0 + c > pos) sv[c] = -CUDART_INF_F;
       }
-      // Row max with 8 independent chains (scaling by qscale > 0 commutes).
+      // Half-row max with 8 independent chains, then the other half's via
+      // shared memory (scaling by qscale > 0 commutes with the max).
       float mx[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k) mx[k] = sv[k];
 #pragma unroll
-      for (int c = 8; c < kBN; ++c) mx[c & 7] = fmaxf(mx[c & 7], sv[c]);
+      for (int c = 8; c < kHalfS; ++c) mx[c & 7] = fmaxf(mx[c & 7], sv[c]);
 #pragma unroll
       for (int k = 4; k >= 1; k >>= 1)
 #pragma unroll
         for (int j = 0; j < k; ++j) mx[j] = fmaxf(mx[j], mx[j + k]);
-      const float mt = mx[0] * p.qscale;
+      float* red_i = red + (i & 1) * 2 * kBM;
+      red_i[wg * kBM + r] = mx[0];
+      named_barrier_sync(1, kSoftmaxThreads);
+      const float mt = fmaxf(mx[0], red_i[(wg ^ 1) * kBM + r]) * p.qscale;
       // Lazy rescaling: the running max moves only when this tile exceeds it
       // by more than 8 (base 2), so P stays <= 2^8 and O is rescaled rarely.
       // Numerator and denominator share the same max, so the result is exact.
@@ -425,7 +490,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
 #pragma unroll
       for (int k = 0; k < 8; ++k) sm[k] = 0.f;
 #pragma unroll
-      for (int c = 0; c < kBN; c += 2) {
+      for (int c = 0; c < kHalfS; c += 2) {
         const float2 x = __ffma2_rn(make_float2(sv[c], sv[c + 1]), qs2, nm2);
         sv[c] = ex2(x.x);
         sv[c + 1] = ex2(x.y);
@@ -438,63 +503,76 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       l_run = l_run * alpha + sm[0];
       m_run = m_new;
 
-      // P V of the previous tile must be done before P and O are touched.
-      if (i > 0) {
-        if (!mbar_wait_warp(o_done, (i - 1) & 1, p.status)) { ok = false; break; }
+      // P buffer b is free once the P V of tile i-2 is done.
+      if (ok && i >= kBufs && !mbar_wait_warp(&pv_done[b], ((i / kBufs) - 1) & 1, p.status))
+        ok = false;
+      // Rescaling O needs every earlier P V finished (the last is tile i-1).
+      if (i > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+        const int bp = (i - 1) % kBufs;
+        if (ok && !mbar_wait_warp(&pv_done[bp], ((i - 1) / kBufs) & 1, p.status)) ok = false;
         tc_fence_after();
-        if (__any_sync(0xffffffffu, alpha != 1.f)) {
-          const float2 a2 = make_float2(alpha, alpha);
+        const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
-            float t[32];
-            tmem_ld32f(tmem_o + lane_base + c * 32, t);
-            tmem_wait_ld_bind(t);
+        for (int c = 0; c < kHalfO / 32; ++c) {
+          float t[32];
+          const uint32_t ta = tmem_o + wg * kHalfO + lane_base + c * 32;
+          tmem_ld32f(ta, t);
+          tmem_wait_ld_bind(t);
 #pragma unroll
-            for (int k = 0; k < 32; k += 2) {
-              const float2 y = __fmul2_rn(make_float2(t[k], t[k + 1]), a2);
-              t[k] = y.x;
-              t[k + 1] = y.y;
-            }
-            tmem_st32(tmem_o + lane_base + c * 32, t);
+          for (int k = 0; k < 32; k += 2) {
+            const float2 y = __fmul2_rn(make_float2(t[k], t[k + 1]), a2);
+            t[k] = y.x;
+            t[k + 1] = y.y;
           }
-          tmem_wait_st();
+          tmem_st32(ta, t);
         }
+        tmem_wait_st();
       }
-      // P row, rounded to the operand type, in the swizzled K-major layout.
+      // This half of the P row, rounded to the operand type, swizzled K-major.
 #pragma unroll
-      for (int c = 0; c < kBN / 8; ++c) {
+      for (int c = 0; c < kHalfS / 8; ++c) {
         uint4 w;
         w.x = Cvt<T>::from_float2(sv[c * 8 + 0], sv[c * 8 + 1]);
         w.y = Cvt<T>::from_float2(sv[c * 8 + 2], sv[c * 8 + 3]);
         w.z = Cvt<T>::from_float2(sv[c * 8 + 4], sv[c * 8 + 5]);
         w.w = Cvt<T>::from_float2(sv[c * 8 + 6], sv[c * 8 + 7]);
-        *reinterpret_cast<uint4*>(sP + (c / 8) * kAtomBytes + sw128_chunk(r, c % 8)) = w;
+        *reinterpret_cast<uint4*>(sP + b * kPBuf + sw128_chunk(r, wg * (kHalfS / 8) + c)) = w;
       }
       // Key rows past the context (the tail of the last block, or rows no
       // block was loaded into) must not feed NaN or stale values into P V.
-      if (key0 + r >= ctx) {
-        const int st = i % kKvStages;
+      if (i * kBN + kBN > ctx) {
+        // V of this tile must have landed before its tail rows are cleared.
+        if (ok && !mbar_wait_warp(&v_full[i % kVStages], (i / kVStages) & 1, p.status)) ok = false;
+      }
+      if (wg == 0 && r < kBN && i * kBN + r >= ctx) {
+        const int st = i % kVStages;
 #pragma unroll
         for (int a = 0; a < kAtoms; ++a)
 #pragma unroll
           for (int c = 0; c < 8; ++c)
-            *reinterpret_cast<uint4*>(sV + st * L::kTileBytes + a * kAtomBytes + r * 128 + c * 16) =
+            *reinterpret_cast<uint4*>(sV + st * L::kKvTile + a * kKvAtom + r * 128 + c * 16) =
                 make_uint4(0, 0, 0, 0);
       }
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       tc_fence_before();
-      mbar_arrive(p_full);
+      mbar_arrive(&p_full[b]);
     }
 
-    if (ok && mbar_wait_warp(o_done, (n_tiles - 1) & 1, p.status)) {
+    // The row sum is split between the two halves.
+    float* red_l = red + 2 * 2 * kBM;
+    red_l[wg * kBM + r] = l_run;
+    named_barrier_sync(1, kSoftmaxThreads);
+    const float l_row = l_run + red_l[(wg ^ 1) * kBM + r];
+    const int bl = (n_tiles - 1) % kBufs;
+    if (ok && mbar_wait_warp(&pv_done[bl], ((n_tiles - 1) / kBufs) & 1, p.status)) {
       tc_fence_after();
-      const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-      T* orow = static_cast<T*>(p.out) + row_elem;
+      const float inv = l_row > 0.f ? 1.f / l_row : 0.f;
+      T* orow = static_cast<T*>(p.out) + row_elem + wg * kHalfO;
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
+      for (int c = 0; c < kHalfO / 32; ++c) {
         float t[32];
-        tmem_ld32(tmem_o + lane_base + c * 32, t);
-        tmem_wait_ld();
+        tmem_ld32f(tmem_o + wg * kHalfO + lane_base + c * 32, t);
+        tmem_wait_ld_bind(t);
         if (row_valid) {
 #pragma unroll
           for (int k = 0; k < 32; k += 8) {
@@ -512,7 +590,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                  "r"(kTmemCols));
@@ -537,14 +615,14 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // 2-D view of a cache: rows (block, head, slot), columns head_dim; boxes of
-// 64 columns x block_size rows, 128-byte swizzle.
+// 64 columns x min(block_size, 64) rows, 128-byte swizzle.
 bool make_cache_map(CUtensorMap* map, const void* base, int dtype, long long rows, int head_dim,
                     int block_size) {
   PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
   if (!fn) return false;
   const cuuint64_t dims[2] = {(cuuint64_t)head_dim, (cuuint64_t)rows};
   const cuuint64_t strides[1] = {(cuuint64_t)head_dim * 2};
-  const cuuint32_t box[2] = {64, (cuuint32_t)block_size};
+  const cuuint32_t box[2] = {64, (cuuint32_t)(block_size < kBN ? block_size : kBN)};
   const cuuint32_t estr[2] = {1, 1};
   const CUresult r = fn(map,
                         dtype == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
