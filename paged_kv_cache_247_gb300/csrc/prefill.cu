@@ -57,27 +57,32 @@ constexpr int kMmaWarp = kSoftmaxWarps + 1;
 constexpr int kVProducerWarp = kSoftmaxWarps + 2;
 constexpr int kPrefillThreads = (kSoftmaxWarps + 3) * 32;
 constexpr int kSoftmaxThreads = kSoftmaxWarps * 32;
-constexpr int kKStages = 4;  // K is released as soon as its Q K^T is done,
-constexpr int kVStages = 3;  // V only after its P V: separate rings
+constexpr int kKStages = 5;  // K is released as soon as its Q K^T is done,
+constexpr int kVStages = 4;  // V only after its P V: separate rings
 constexpr int kBufs = 2;   // S (tensor memory) and P (shared memory) are double-buffered
-constexpr int kTmemCols = 256;
-constexpr int kQAtom = kBM * 128;   // 64 columns (128 bytes) of the 128 query rows
-constexpr int kKvAtom = kBN * 128;  // 64 columns of the 64 key rows of a tile
-constexpr int kPBuf = kBM * 128;    // a [128 rows x 64 keys] P tile
+constexpr int kTmemCols = 512;
+constexpr int kBarSlots = 32;  // mbarriers reserved in shared memory
+constexpr int kKvAtom = kBN * 128;  // 64 columns (128 bytes) of the 64 key rows of a tile
 
 template <int D>
 struct PrefillSmem {
   static constexpr int kAtoms = D / 64;  // 64-column atoms per row
   static constexpr int kKvTile = kAtoms * kKvAtom;
-  static constexpr int kQ = 0;
-  static constexpr int kK = kQ + kAtoms * kQAtom;
+  static constexpr int kK = 0;
   static constexpr int kV = kK + kKStages * kKvTile;
-  static constexpr int kP = kV + kVStages * kKvTile;
   // row-max exchange [2 tiles][2 halves][128] and row-sum exchange [2][128] floats
-  static constexpr int kRed = kP + kBufs * kPBuf;
+  static constexpr int kRed = kV + kVStages * kKvTile;
   static constexpr int kBar = kRed + 3 * 2 * kBM * 4;
-  static constexpr int kTmemSlot = kBar + 32 * 8;
-  static constexpr int kBytes = kTmemSlot + 16 + 1024;  // + 1024-byte alignment slack
+  static constexpr int kTmemSlot = kBar + kBarSlots * 8;
+  // + 1024-byte alignment slack; at least 116 KiB so that one CTA (which
+  // takes all of tensor memory) is resident per SM
+  static constexpr int kBytes =
+      kTmemSlot + 16 + 1024 > 116 * 1024 ? kTmemSlot + 16 + 1024 : 116 * 1024;
+  // tensor-memory columns: S buffers, O, Q (bf16/fp16 pairs), P buffers
+  static constexpr int kColO = kBufs * kBN;
+  static constexpr int kColQ = kColO + D;
+  static constexpr int kColP = kColQ + D / 2;
+  static_assert(kColP + kBufs * kBN / 2 <= kTmemCols, "tensor memory overflow");
 };
 
 struct PrefillParams {
@@ -121,6 +126,16 @@ __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a, uint64_t b,
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
+}
+
+// Same with the A operand read from tensor memory: row r in lane r, element
+// pairs packed low-first, 8 columns per 16 elements of K.
+__device__ __forceinline__ void mma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
+                                           uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate));
 }
 
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
@@ -205,6 +220,15 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+__device__ __forceinline__ void tmem_st16u(uint32_t taddr, const uint32_t (&w)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+      "%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7]),
+      "r"(w[8]), "r"(w[9]), "r"(w[10]), "r"(w[11]), "r"(w[12]), "r"(w[13]), "r"(w[14]), "r"(w[15])
+      : "memory");
+}
+
 __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
@@ -238,20 +262,20 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem =
       reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  unsigned char* sQ = smem + L::kQ;
   unsigned char* sK = smem + L::kK;
   unsigned char* sV = smem + L::kV;
-  unsigned char* sP = smem + L::kP;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBar);
-  uint64_t* k_full = bars;         // [4] K stage landed (TMA transaction bytes)
-  uint64_t* k_empty = bars + 4;    // [4] K stage consumed by Q K^T (MMA commit)
-  uint64_t* v_full = bars + 8;     // [3] V stage landed
-  uint64_t* v_empty = bars + 11;   // [3] V stage consumed by P V
-  uint64_t* q_full = bars + 14;    // Q tile written (softmax threads)
-  uint64_t* s_full = bars + 15;    // [2] S buffer computed (MMA commit)
-  uint64_t* s_free = bars + 17;    // [2] S buffer read (softmax threads)
-  uint64_t* p_full = bars + 19;    // [2] P buffer written (softmax threads)
-  uint64_t* pv_done = bars + 21;   // [2] P V of that buffer finished (MMA commit)
+  uint64_t* k_full = bars;                   // K stage landed (TMA transaction bytes)
+  uint64_t* k_empty = k_full + kKStages;     // K stage consumed by Q K^T (MMA commit)
+  uint64_t* v_full = k_empty + kKStages;     // V stage landed
+  uint64_t* v_empty = v_full + kVStages;     // V stage consumed by P V
+  uint64_t* q_full = v_empty + kVStages;     // Q written to tensor memory (softmax threads)
+  uint64_t* s_full = q_full + 1;             // S buffer computed (MMA commit)
+  uint64_t* s_free = s_full + kBufs;         // S buffer read (softmax threads)
+  uint64_t* p_full = s_free + kBufs;         // P buffer written (softmax threads)
+  uint64_t* pv_done = p_full + kBufs;        // P V of that buffer finished (MMA commit)
+  static_assert(2 * kKStages + 2 * kVStages + 1 + 4 * kBufs <= kBarSlots,
+                "barrier area too small");
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kTmemSlot);
   float* red = reinterpret_cast<float*>(smem + L::kRed);
 
@@ -308,7 +332,9 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tmem_o = tmem + kBufs * kBN;  // S buffers at columns [0, 128)
+  const uint32_t tmem_o = tmem + L::kColO;  // S buffers at columns [0, 128)
+  const uint32_t tmem_q = tmem + L::kColQ;
+  const uint32_t tmem_p = tmem + L::kColP;
 
   if (warp == kKProducerWarp || warp == kVProducerWarp) {
     // ----------------------------------------------------- K and V producers
@@ -360,8 +386,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       constexpr bool bf16 = std::is_same<T, __nv_bfloat16>::value;
       const uint32_t idesc_s = instr_desc(bf16, false, kBN, kBM);
       const uint32_t idesc_o = instr_desc(bf16, true, D, kBM);
-      const uint32_t aQ = smem_addr(sQ), aK = smem_addr(sK), aV = smem_addr(sV),
-                     aP = smem_addr(sP);
+      const uint32_t aK = smem_addr(sK), aV = smem_addr(sV);
       bool ok = mbar_wait(q_full, 0, p.status);
       int next_s = 0, next_pv = 0;
       unsigned long long idle_since = global_ns();
@@ -374,11 +399,10 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
             tc_fence_after();
 #pragma unroll
             for (int ks = 0; ks < D / 16; ++ks)
-              mma_f16(tmem + b * kBN,
-                      smem_desc(aQ + (ks / 4) * kQAtom + (ks % 4) * 32, 16, 1024),
-                      smem_desc(aK + st * L::kKvTile + (ks / 4) * kKvAtom + (ks % 4) * 32, 16,
-                                1024),
-                      idesc_s, ks > 0);
+              mma_f16_ta(tmem + b * kBN, tmem_q + ks * 8,
+                         smem_desc(aK + st * L::kKvTile + (ks / 4) * kKvAtom + (ks % 4) * 32,
+                                   16, 1024),
+                         idesc_s, ks > 0);
             mma_commit(&s_full[b]);
             mma_commit(&k_empty[st]);
             ++next_s;
@@ -394,9 +418,9 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
             // atoms kKvAtom apart.
 #pragma unroll
             for (int ks = 0; ks < kBN / 16; ++ks)
-              mma_f16(tmem_o, smem_desc(aP + bj * kPBuf + ks * 32, 16, 1024),
-                      smem_desc(aV + stj * L::kKvTile + ks * 16 * 128, kKvAtom, 1024), idesc_o,
-                      (j > 0 || ks > 0) ? 1u : 0u);
+              mma_f16_ta(tmem_o, tmem_p + bj * (kBN / 2) + ks * 8,
+                         smem_desc(aV + stj * L::kKvTile + ks * 16 * 128, kKvAtom, 1024),
+                         idesc_o, (j > 0 || ks > 0) ? 1u : 0u);
             mma_commit(&pv_done[bj]);
             mma_commit(&v_empty[stj]);
             ++next_pv;
@@ -428,15 +452,26 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         ((size_t)(q0 + (row_valid ? jq : 0)) * p.num_q_heads + kvh * G + (row_valid ? g : 0)) * D;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
 
-    // This thread's half of the Q row into the swizzled K-major tile.
+    // This thread's half of the Q row into tensor memory (the A operand of
+    // Q K^T): D/2 elements as D/4 columns of packed pairs.
     {
-      const uint4* src = reinterpret_cast<const uint4*>(static_cast<const T*>(p.q) + row_elem);
+      const uint4* src = reinterpret_cast<const uint4*>(static_cast<const T*>(p.q) + row_elem) +
+                         wg * (D / 16);
+      uint32_t w[16];
 #pragma unroll
-      for (int c = wg * (D / 16); c < (wg + 1) * (D / 16); ++c) {
-        const uint4 w = row_valid ? src[c] : make_uint4(0, 0, 0, 0);
-        *reinterpret_cast<uint4*>(sQ + (c / 8) * kQAtom + sw128_chunk(r, c % 8)) = w;
+      for (int part = 0; part < D / 64; ++part) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const uint4 v = row_valid ? src[part * 4 + c] : make_uint4(0, 0, 0, 0);
+          w[c * 4 + 0] = v.x;
+          w[c * 4 + 1] = v.y;
+          w[c * 4 + 2] = v.z;
+          w[c * 4 + 3] = v.w;
+        }
+        tmem_st16u(tmem_q + wg * (D / 4) + part * 16 + lane_base, w);
       }
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      tmem_wait_st();
+      tc_fence_before();
       mbar_arrive(q_full);
     }
 
@@ -528,15 +563,14 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         }
         tmem_wait_st();
       }
-      // This half of the P row, rounded to the operand type, swizzled K-major.
+      // This half of the P row, rounded to the operand type, into tensor
+      // memory (the A operand of P V).
+      {
+        uint32_t w[16];
 #pragma unroll
-      for (int c = 0; c < kHalfS / 8; ++c) {
-        uint4 w;
-        w.x = Cvt<T>::from_float2(sv[c * 8 + 0], sv[c * 8 + 1]);
-        w.y = Cvt<T>::from_float2(sv[c * 8 + 2], sv[c * 8 + 3]);
-        w.z = Cvt<T>::from_float2(sv[c * 8 + 4], sv[c * 8 + 5]);
-        w.w = Cvt<T>::from_float2(sv[c * 8 + 6], sv[c * 8 + 7]);
-        *reinterpret_cast<uint4*>(sP + b * kPBuf + sw128_chunk(r, wg * (kHalfS / 8) + c)) = w;
+        for (int c = 0; c < kHalfS / 2; ++c) w[c] = Cvt<T>::from_float2(sv[2 * c], sv[2 * c + 1]);
+        tmem_st16u(tmem_p + b * (kBN / 2) + wg * (kHalfS / 2) + lane_base, w);
+        tmem_wait_st();
       }
       // Key rows past the context (the tail of the last block, or rows no
       // block was loaded into) must not feed NaN or stale values into P V.
@@ -553,7 +587,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
             *reinterpret_cast<uint4*>(sV + st * L::kKvTile + a * kKvAtom + r * 128 + c * 16) =
                 make_uint4(0, 0, 0, 0);
       }
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the cleared V rows
       tc_fence_before();
       mbar_arrive(&p_full[b]);
     }
