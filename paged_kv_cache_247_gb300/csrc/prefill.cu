@@ -391,40 +391,44 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       int next_s = 0, next_pv = 0;
       unsigned long long idle_since = global_ns();
       while (ok && next_pv < n_tiles) {
-        bool progressed = false;
-        if (next_s < n_tiles) {
-          const int i = next_s, st = i % kKStages, b = i % kBufs;
-          if (mbar_test_wait(&k_full[st], (i / kKStages) & 1) &&
-              (i < kBufs || mbar_test_wait(&s_free[b], ((i / kBufs) - 1) & 1))) {
-            tc_fence_after();
+        // S_i and P_j V_j accumulate into different tensor-memory regions, so
+        // when both are ready their k-steps are interleaved: each chain of
+        // dependent accumulations then overlaps the other.
+        const int i = next_s, st = i % kKStages, b = i % kBufs;
+        const bool s_ready =
+            i < n_tiles && mbar_test_wait(&k_full[st], (i / kKStages) & 1) &&
+            (i < kBufs || mbar_test_wait(&s_free[b], ((i / kBufs) - 1) & 1));
+        const int j = next_pv, bj = j % kBufs, stj = j % kVStages;
+        const bool pv_ready = j < next_s && mbar_test_wait(&p_full[bj], (j / kBufs) & 1) &&
+                              mbar_test_wait(&v_full[stj], (j / kVStages) & 1);
+        const bool progressed = s_ready || pv_ready;
+        if (progressed) {
+          tc_fence_after();
+          constexpr int kStepsS = D / 16, kStepsPV = kBN / 16;
+          constexpr int kSteps = kStepsS > kStepsPV ? kStepsS : kStepsPV;
 #pragma unroll
-            for (int ks = 0; ks < D / 16; ++ks)
+          for (int ks = 0; ks < kSteps; ++ks) {
+            if (s_ready && ks < kStepsS)
               mma_f16_ta(tmem + b * kBN, tmem_q + ks * 8,
                          smem_desc(aK + st * L::kKvTile + (ks / 4) * kKvAtom + (ks % 4) * 32,
                                    16, 1024),
                          idesc_s, ks > 0);
-            mma_commit(&s_full[b]);
-            mma_commit(&k_empty[st]);
-            ++next_s;
-            progressed = true;
-          }
-        }
-        if (next_pv < next_s) {
-          const int j = next_pv, bj = j % kBufs, stj = j % kVStages;
-          if (mbar_test_wait(&p_full[bj], (j / kBufs) & 1) &&
-              mbar_test_wait(&v_full[stj], (j / kVStages) & 1)) {
-            tc_fence_after();
             // V as an MN-major operand: 8-key groups 1024 B apart, 64-column
             // atoms kKvAtom apart.
-#pragma unroll
-            for (int ks = 0; ks < kBN / 16; ++ks)
+            if (pv_ready && ks < kStepsPV)
               mma_f16_ta(tmem_o, tmem_p + bj * (kBN / 2) + ks * 8,
                          smem_desc(aV + stj * L::kKvTile + ks * 16 * 128, kKvAtom, 1024),
                          idesc_o, (j > 0 || ks > 0) ? 1u : 0u);
+          }
+          if (pv_ready) {
             mma_commit(&pv_done[bj]);
             mma_commit(&v_empty[stj]);
             ++next_pv;
-            progressed = true;
+          }
+          if (s_ready) {
+            mma_commit(&s_full[b]);
+            mma_commit(&k_empty[st]);
+            ++next_s;
           }
         }
         if (progressed) {
