@@ -53,9 +53,10 @@ constexpr int kBM = 128;  // rows of a tile: MMA M
 constexpr int kBN = 64;   // keys per tile: N of Q K^T, K of P V
 constexpr int kSoftmaxWarps = 8;  // two warpgroups share each row (half the columns each)
 constexpr int kKProducerWarp = kSoftmaxWarps;
-constexpr int kMmaWarp = kSoftmaxWarps + 1;
+constexpr int kMmaWarp = kSoftmaxWarps + 1;  // issues Q K^T; owns the tensor memory
 constexpr int kVProducerWarp = kSoftmaxWarps + 2;
-constexpr int kPrefillThreads = (kSoftmaxWarps + 3) * 32;
+constexpr int kPvWarp = kSoftmaxWarps + 3;   // issues P V
+constexpr int kPrefillThreads = (kSoftmaxWarps + 4) * 32;
 constexpr int kSoftmaxThreads = kSoftmaxWarps * 32;
 constexpr int kKStages = 5;  // K is released as soon as its Q K^T is done,
 constexpr int kVStages = 4;  // V only after its P V: separate rings
@@ -64,9 +65,13 @@ constexpr int kTmemCols = 512;
 constexpr int kBarSlots = 32;  // mbarriers reserved in shared memory
 constexpr int kKvAtom = kBN * 128;  // 64 columns (128 bytes) of the 64 key rows of a tile
 
+// A K or V tile in shared memory: groups of 8 key rows, kGroup bytes apart;
+// within a group, one 1024-byte 128-byte-swizzled atom per 64 columns.  A
+// single TMA copy fills any number of whole groups with both atoms.
 template <int D>
 struct PrefillSmem {
   static constexpr int kAtoms = D / 64;  // 64-column atoms per row
+  static constexpr int kGroup = kAtoms * 1024;
   static constexpr int kKvTile = kAtoms * kKvAtom;
   static constexpr int kK = 0;
   static constexpr int kV = kK + kKStages * kKvTile;
@@ -211,12 +216,13 @@ __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
-__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y,
-                                            uint64_t* bar) {
+// Copy the box at coordinates (0, 0, 0, g) of a 4-D tensor map.
+__device__ __forceinline__ void tma_load_group(void* dst, const CUtensorMap* map, int g,
+                                               uint64_t* bar) {
   asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_addr(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %2, %2, %3}], [%4];" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(g), "r"(smem_addr(bar))
       : "memory");
 }
 
@@ -319,92 +325,82 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     const int B = p.block_size;
     const int R = B < kBN ? B : kBN;
     const int32_t* trow = p.block_tables + (size_t)s * p.max_blocks_per_seq;
+    // Lane l copies run l (all of its columns) with one TMA copy.  The
+    // block-table entry of the next tile is read before this tile's copies
+    // are issued, so its latency is spent while the warp waits for the next
+    // free slot.
+    const int seg = lane;
+    auto table_entry = [&](int t) -> int {
+      const int key = t * kBN + seg * R;
+      return (seg < kBN / R && t < n_tiles && key < ctx) ? __ldg(trow + key / B) : 0;
+    };
+    int phys_next = table_entry(0);
     for (int i = 0; i < n_tiles; ++i) {
       const int st = i % nstages;
       if (i >= nstages && !mbar_wait_warp(&empty[st], ((i / nstages) - 1) & 1, p.status)) break;
       const int key0 = i * kBN;
       const int nvalid = min(ctx, key0 + kBN) - key0;
       const int nseg = (nvalid + R - 1) / R;
-      int y = 0;
-      if (lane < nseg) {
-        const int key = key0 + lane * R;
-        int phys = __ldg(trow + key / B);
+      int phys = phys_next;
+      phys_next = table_entry(i + 1);
+      if (lane == 0)
+        mbar_arrive_expect_tx(&full[st], (uint32_t)nseg * R * D * (uint32_t)sizeof(T));
+      __syncwarp();
+      if (seg < nseg) {
         if ((unsigned)phys >= (unsigned)p.num_blocks) {
           atomicOr(p.status, PKV_DEV_BAD_BLOCK_ID);
           phys = 0;
         }
-        y = (phys * p.num_kv_heads + kvh) * B + key % B;
-      }
-      if (lane == 0)
-        mbar_arrive_expect_tx(&full[st], (uint32_t)nseg * R * D * (uint32_t)sizeof(T));
-      __syncwarp();
-      if (lane < nseg) {
-#pragma unroll
-        for (int a = 0; a < kAtoms; ++a)
-          tma_load_2d(ring + st * L::kKvTile + a * kKvAtom + lane * R * 128, map, 64 * a, y,
-                      &full[st]);
+        const int key = key0 + seg * R;
+        const int y = (phys * p.num_kv_heads + kvh) * B + key % B;  // a multiple of 8
+        tma_load_group(ring + st * L::kKvTile + seg * (R / 8) * L::kGroup, map, y / 8, &full[st]);
       }
     }
-  } else if (warp == kMmaWarp) {
-    // ------------------------------------------------------- MMA issuer
-    // Issues S_i = Q K_i^T and P_j V_j in order of i and of j, each as soon
-    // as its inputs are ready (polling, never blocking one on the other),
-    // so the tensor core computes the next scores while the softmax warps
-    // work on the previous tile and a late V never holds back Q K^T.
+  } else if (warp == kMmaWarp || warp == kPvWarp) {
+    // ------------------------------------------------------- MMA issuers
+    // One thread issues the chain S_i = Q K_i^T, another P_j V_j.  A single
+    // thread issues a tcgen05.mma (or commit) only every ~50 cycles whatever
+    // its size, while S_i with N = 64 keeps the tensor core busy for 32
+    // cycles per k-step: two issuers keep it fed, and neither chain waits
+    // behind the other.  Each commit tracks only its own thread's MMAs.
     if (lane == 0) {
       constexpr bool bf16 = std::is_same<T, __nv_bfloat16>::value;
-      const uint32_t idesc_s = instr_desc(bf16, false, kBN, kBM);
-      const uint32_t idesc_o = instr_desc(bf16, true, D, kBM);
-      const uint32_t aK = smem_addr(sK), aV = smem_addr(sV);
-      bool ok = mbar_wait(q_full, 0, p.status);
-      int next_s = 0, next_pv = 0;
-      unsigned long long idle_since = global_ns();
-      while (ok && next_pv < n_tiles) {
-        // S_i and P_j V_j accumulate into different tensor-memory regions, so
-        // when both are ready their k-steps are interleaved: each chain of
-        // dependent accumulations then overlaps the other.
-        const int i = next_s, st = i % kKStages, b = i % kBufs;
-        const bool s_ready =
-            i < n_tiles && mbar_test_wait(&k_full[st], (i / kKStages) & 1) &&
-            (i < kBufs || mbar_test_wait(&s_free[b], ((i / kBufs) - 1) & 1));
-        const int j = next_pv, bj = j % kBufs, stj = j % kVStages;
-        const bool pv_ready = j < next_s && mbar_test_wait(&p_full[bj], (j / kBufs) & 1) &&
-                              mbar_test_wait(&v_full[stj], (j / kVStages) & 1);
-        const bool progressed = s_ready || pv_ready;
-        if (progressed) {
+      if (warp == kMmaWarp) {
+        const uint32_t idesc_s = instr_desc(bf16, false, kBN, kBM);
+        const uint32_t aK = smem_addr(sK);
+        bool ok = mbar_wait(q_full, 0, p.status);
+        for (int i = 0; ok && i < n_tiles; ++i) {
+          const int st = i % kKStages, b = i % kBufs;
+          if (!mbar_wait(&k_full[st], (i / kKStages) & 1, p.status)) break;
+          if (i >= kBufs && !mbar_wait(&s_free[b], ((i / kBufs) - 1) & 1, p.status)) break;
           tc_fence_after();
-          constexpr int kStepsS = D / 16, kStepsPV = kBN / 16;
-          constexpr int kSteps = kStepsS > kStepsPV ? kStepsS : kStepsPV;
 #pragma unroll
-          for (int ks = 0; ks < kSteps; ++ks) {
-            if (s_ready && ks < kStepsS)
-              mma_f16_ta(tmem + b * kBN, tmem_q + ks * 8,
-                         smem_desc(aK + st * L::kKvTile + (ks / 4) * kKvAtom + (ks % 4) * 32,
-                                   16, 1024),
-                         idesc_s, ks > 0);
-            // V as an MN-major operand: 8-key groups 1024 B apart, 64-column
-            // atoms kKvAtom apart.
-            if (pv_ready && ks < kStepsPV)
-              mma_f16_ta(tmem_o, tmem_p + bj * (kBN / 2) + ks * 8,
-                         smem_desc(aV + stj * L::kKvTile + ks * 16 * 128, kKvAtom, 1024),
-                         idesc_o, (j > 0 || ks > 0) ? 1u : 0u);
-          }
-          if (pv_ready) {
-            mma_commit(&pv_done[bj]);
-            mma_commit(&v_empty[stj]);
-            ++next_pv;
-          }
-          if (s_ready) {
-            mma_commit(&s_full[b]);
-            mma_commit(&k_empty[st]);
-            ++next_s;
-          }
+          for (int ks = 0; ks < D / 16; ++ks)
+            mma_f16_ta(tmem + b * kBN, tmem_q + ks * 8,
+                       smem_desc(aK + st * L::kKvTile + (ks / 4) * 1024 + (ks % 4) * 32, 16,
+                                 L::kGroup),
+                       idesc_s, ks > 0);
+          mma_commit(&s_full[b]);
+          mma_commit(&k_empty[st]);
         }
-        if (progressed) {
-          idle_since = global_ns();
-        } else if (global_ns() - idle_since > kWaitLimitNs || timed_out(p.status)) {
-          atomicOr(p.status, PKV_DEV_WAIT_TIMEOUT);
-          ok = false;
+      } else {
+        const uint32_t idesc_o = instr_desc(bf16, true, D, kBM);
+        const uint32_t aV = smem_addr(sV);
+        for (int j = 0; j < n_tiles; ++j) {
+          const int bj = j % kBufs, stj = j % kVStages;
+          if (!mbar_wait(&p_full[bj], (j / kBufs) & 1, p.status)) break;
+          if (!mbar_wait(&v_full[stj], (j / kVStages) & 1, p.status)) break;
+          tc_fence_after();
+          // V as an MN-major operand: 8-key groups kGroup bytes apart,
+          // 64-column atoms 1024 bytes apart.
+#pragma unroll
+          for (int ks = 0; ks < kBN / 16; ++ks)
+            mma_f16_ta(tmem_o, tmem_p + bj * (kBN / 2) + ks * 8,
+                       smem_desc(aV + stj * L::kKvTile + ks * 2 * L::kGroup, 1024, L::kGroup),
+                       idesc_o,
+                       (j > 0 || ks > 0) ? 1u : 0u);
+          mma_commit(&pv_done[bj]);
+          mma_commit(&v_empty[stj]);
         }
       }
     }
@@ -557,10 +553,12 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         for (int a = 0; a < kAtoms; ++a)
 #pragma unroll
           for (int c = 0; c < 8; ++c)
-            *reinterpret_cast<uint4*>(sV + st * L::kKvTile + a * kKvAtom + r * 128 + c * 16) =
+            *reinterpret_cast<uint4*>(sV + st * L::kKvTile + (r / 8) * L::kGroup + a * 1024 +
+                                      (r % 8) * 128 + c * 16) =
                 make_uint4(0, 0, 0, 0);
       }
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the cleared V rows
+      if (i * kBN + kBN > ctx)  // make the cleared V rows visible to the tensor core
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       tc_fence_before();
       mbar_arrive(&p_full[b]);
     }
@@ -627,14 +625,19 @@ bool make_cache_map(CUtensorMap* map, const void* base, int dtype, long long row
                     int block_size) {
   PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
   if (!fn) return false;
-  const cuuint64_t dims[2] = {(cuuint64_t)head_dim, (cuuint64_t)rows};
-  const cuuint64_t strides[1] = {(cuuint64_t)head_dim * 2};
-  const cuuint32_t box[2] = {64, (cuuint32_t)(block_size < kBN ? block_size : kBN)};
-  const cuuint32_t estr[2] = {1, 1};
+  // The cache rows [rows, head_dim] seen as (64 columns, 8 rows, head_dim / 64
+  // atoms, rows / 8 groups): a box of whole groups lands as the tile layout
+  // above, every atom of every group in one copy.
+  const int atoms = head_dim / 64;
+  const int run = block_size < kBN ? block_size : kBN;
+  const cuuint64_t dims[4] = {64, 8, (cuuint64_t)atoms, (cuuint64_t)(rows / 8)};
+  const cuuint64_t strides[3] = {(cuuint64_t)head_dim * 2, 128, (cuuint64_t)head_dim * 2 * 8};
+  const cuuint32_t box[4] = {64, 8, (cuuint32_t)atoms, (cuuint32_t)(run / 8)};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
   const CUresult r = fn(map,
                         dtype == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                           : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
-                        2, const_cast<void*>(base), dims, strides, box, estr,
+                        4, const_cast<void*>(base), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
