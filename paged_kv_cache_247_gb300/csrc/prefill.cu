@@ -52,11 +52,15 @@ namespace {
 constexpr int kBM = 128;  // rows of a tile: MMA M
 constexpr int kBN = 64;   // keys per tile: N of Q K^T, K of P V
 constexpr int kSoftmaxWarps = 8;  // two warpgroups share each row (half the columns each)
+// Warps 8..13: K producers (8, 12) and V producers (10, 13), each pair
+// taking alternate tiles, and the two MMA issuers (9, 11).
 constexpr int kKProducerWarp = kSoftmaxWarps;
 constexpr int kMmaWarp = kSoftmaxWarps + 1;  // issues Q K^T; owns the tensor memory
 constexpr int kVProducerWarp = kSoftmaxWarps + 2;
 constexpr int kPvWarp = kSoftmaxWarps + 3;   // issues P V
-constexpr int kPrefillThreads = (kSoftmaxWarps + 4) * 32;
+constexpr int kKProducerWarp2 = kSoftmaxWarps + 4;
+constexpr int kVProducerWarp2 = kSoftmaxWarps + 5;
+constexpr int kPrefillThreads = (kSoftmaxWarps + 6) * 32;
 constexpr int kSoftmaxThreads = kSoftmaxWarps * 32;
 constexpr int kKStages = 5;  // K is released as soon as its Q K^T is done,
 constexpr int kVStages = 4;  // V only after its P V: separate rings
@@ -311,12 +315,16 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
   const uint32_t tmem_q = tmem + L::kColQ;
   const uint32_t tmem_p = tmem + L::kColP;
 
-  if (warp == kKProducerWarp || warp == kVProducerWarp) {
+  if (warp == kKProducerWarp || warp == kVProducerWarp || warp == kKProducerWarp2 ||
+      warp == kVProducerWarp2) {
     // ----------------------------------------------------- K and V producers
-    // One warp streams K tiles, another V tiles, each into its own ring.
+    // Two warps stream K tiles and two V tiles, each operand into its own
+    // ring, each warp of a pair taking every other tile: a TMA copy costs
+    // its issuing warp tens of cycles, and the two warps issue in parallel.
     // Each tile's keys are loaded as runs of R rows; a run never crosses a
     // block boundary (R divides both the block size and the tile).
-    const bool is_k = warp == kKProducerWarp;
+    const bool is_k = warp == kKProducerWarp || warp == kKProducerWarp2;
+    const int first = (warp == kKProducerWarp2 || warp == kVProducerWarp2) ? 1 : 0;
     const int nstages = is_k ? kKStages : kVStages;
     uint64_t* full = is_k ? k_full : v_full;
     uint64_t* empty = is_k ? k_empty : v_empty;
@@ -326,7 +334,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     const int R = B < kBN ? B : kBN;
     const int32_t* trow = p.block_tables + (size_t)s * p.max_blocks_per_seq;
     // Lane l copies run l (all of its columns) with one TMA copy.  The
-    // block-table entry of the next tile is read before this tile's copies
+    // block-table entry of this warp's next tile is read before this tile's copies
     // are issued, so its latency is spent while the warp waits for the next
     // free slot.
     const int seg = lane;
@@ -334,15 +342,15 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       const int key = t * kBN + seg * R;
       return (seg < kBN / R && t < n_tiles && key < ctx) ? __ldg(trow + key / B) : 0;
     };
-    int phys_next = table_entry(0);
-    for (int i = 0; i < n_tiles; ++i) {
+    int phys_next = table_entry(first);
+    for (int i = first; i < n_tiles; i += 2) {
       const int st = i % nstages;
       if (i >= nstages && !mbar_wait_warp(&empty[st], ((i / nstages) - 1) & 1, p.status)) break;
       const int key0 = i * kBN;
       const int nvalid = min(ctx, key0 + kBN) - key0;
       const int nseg = (nvalid + R - 1) / R;
       int phys = phys_next;
-      phys_next = table_entry(i + 1);
+      phys_next = table_entry(i + 2);
       if (lane == 0)
         mbar_arrive_expect_tx(&full[st], (uint32_t)nseg * R * D * (uint32_t)sizeof(T));
       __syncwarp();
