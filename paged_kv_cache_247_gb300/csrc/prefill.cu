@@ -7,35 +7,31 @@
 // the block table ("Only 20.4% of your KV cache held actual tokens", section
 // "The page table, relocated into attention"; prompt chunks: "The KV cache is
 // a systems problem", section "Memory savings change the scheduling
-// question").  Unlike decode this is a dense contraction: a tile of 128
-// (query, head) rows against 128 keys is a 128x128xD product, twice.
+// question").  Unlike decode this is a dense contraction.
 //
-// One CTA owns (sequence, KV head, tile of query rows).  Rows are
+// One CTA owns (sequence, KV head, two tiles of 128 query rows).  Rows are
 // (query, head-of-group) pairs, so every head of a KV group shares each K/V
-// tile (grouped-query attention packs into the MMA's M dimension).
+// tile (grouped-query attention packs into the MMA's M dimension), and the
+// two row tiles share every K/V tile the CTA loads.
 //
-//   warps 8, 10  producers: per key tile, read the tile's block ids and
-//            load every (block, head) run of K (warp 8, 4-stage ring) and of
-//            V (warp 10, 3-stage ring) with 2-D TMA (cp.async.bulk.tensor,
-//            128-byte swizzle).
-//   warp 9   MMA issuer (one thread): S = Q K^T into tensor memory and,
-//            once the softmax warps have written P, O += P V (V as an
-//            MN-major operand), each issued as soon as ready; completion via
-//            tcgen05.commit on mbarriers.
-//            The warp also allocates and frees the tensor memory.
-//   warps 0-7  softmax, two warpgroups: thread (wg, r) owns half of row r
-//            of S (tcgen05.ld), applies the causal mask, exchanges the
-//            half-row max through shared memory, keeps the running max and
-//            its half of the sum in base 2, rescales its half of the O row
-//            in tensor memory when the max grows, and writes its half of the
-//            P row (same 16-bit type as V) into shared memory in the
-//            swizzled K-major layout the next MMA reads.  At the end the two
-//            halves' sums are combined and each stores its half of O.
+//   warps 8, 10  producers, alternate 128-key tiles: read the tile's block
+//            ids, then load every (block, head) run of K and of V with one
+//            4-D TMA copy each (cp.async.bulk.tensor, 128-byte swizzle).
+//   warp 9   issues S_t = Q_t K^T for both row tiles t (Q from shared
+//            memory); allocates and frees the tensor memory.
+//   warp 11  issues O_t += P_t V (P from tensor memory, V as an MN-major
+//            operand); clears V rows past the context first.
+//   warps 0-3, 4-7  softmax, one warpgroup per row tile and one thread per
+//            row: each writes its Q rows into shared memory, then per key
+//            tile reads its S row (tcgen05.ld), masks the diagonal, keeps the
+//            running max and sum in base 2 (lazy rescaling), writes P over S
+//            in tensor memory and rescales O when the max moved; at the end
+//            it normalises and stores its O row.
 //
-// Tensor memory: two S buffers in columns [0, 128), O in [128, 128 + D).
-// Key tiles are 64 wide; S and P are double-buffered and K and V have rings
-// of their own, so the tensor core runs S_(i+1) and P_i V_i while the softmax
-// warps work on tiles i and i+1.
+// Tensor memory: row tile t has S/P in columns [128 t, 128 t + 128) and O
+// in [256 + D t, 256 + D (t + 1)).  While one row tile's softmax runs, the
+// tensor core computes the other tile's S or P V, so the two chains
+// S -> softmax -> P V interleave.
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -49,49 +45,43 @@
 namespace pkv {
 namespace {
 
-constexpr int kBM = 128;  // rows of a tile: MMA M
-constexpr int kBN = 64;   // keys per tile: N of Q K^T, K of P V
-constexpr int kSoftmaxWarps = 8;  // two warpgroups share each row (half the columns each)
-// Warps 8..13: K producers (8, 12) and V producers (10, 13), each pair
-// taking alternate tiles, and the two MMA issuers (9, 11).
-constexpr int kKProducerWarp = kSoftmaxWarps;
-constexpr int kMmaWarp = kSoftmaxWarps + 1;  // issues Q K^T; owns the tensor memory
-constexpr int kVProducerWarp = kSoftmaxWarps + 2;
-constexpr int kPvWarp = kSoftmaxWarps + 3;   // issues P V
-constexpr int kKProducerWarp2 = kSoftmaxWarps + 4;
-constexpr int kVProducerWarp2 = kSoftmaxWarps + 5;
-constexpr int kPrefillThreads = (kSoftmaxWarps + 6) * 32;
-constexpr int kSoftmaxThreads = kSoftmaxWarps * 32;
-constexpr int kKStages = 5;  // K is released as soon as its Q K^T is done,
-constexpr int kVStages = 4;  // V only after its P V: separate rings
-constexpr int kBufs = 2;   // S (tensor memory) and P (shared memory) are double-buffered
+constexpr int kBM = 128;     // rows of a row tile: MMA M
+constexpr int kRowTiles = 2; // row tiles per CTA, one softmax warpgroup each
+constexpr int kBN = 128;     // keys per K/V tile: N of Q K^T, K of P V
+constexpr int kSoftmaxWarps = 4 * kRowTiles;
+constexpr int kProducerWarp0 = kSoftmaxWarps;      // even K/V tiles
+constexpr int kMmaWarp = kSoftmaxWarps + 1;        // Q K^T; owns the tensor memory
+constexpr int kProducerWarp1 = kSoftmaxWarps + 2;  // odd K/V tiles
+constexpr int kPvWarp = kSoftmaxWarps + 3;         // P V
+constexpr int kPrefillThreads = (kSoftmaxWarps + 4) * 32;
+constexpr int kStages = 2;      // K ring and V ring depth: one slot per producer warp
 constexpr int kTmemCols = 512;
-constexpr int kBarSlots = 32;  // mbarriers reserved in shared memory
-constexpr int kKvAtom = kBN * 128;  // 64 columns (128 bytes) of the 64 key rows of a tile
+constexpr int kBarSlots = 32;   // mbarriers reserved in shared memory
 
-// A K or V tile in shared memory: groups of 8 key rows, kGroup bytes apart;
-// within a group, one 1024-byte 128-byte-swizzled atom per 64 columns.  A
-// single TMA copy fills any number of whole groups with both atoms.
+// Shared-memory tiles (Q, K and V alike): groups of 8 rows, kGroup bytes
+// apart; within a group, one 1024-byte 128-byte-swizzled atom per 64
+// columns.  This is the K-major operand layout with SBO = kGroup, and, for
+// V, the MN-major one with LBO = 1024 and SBO = kGroup.  A single TMA copy
+// fills any number of whole groups with all their atoms.
 template <int D>
 struct PrefillSmem {
-  static constexpr int kAtoms = D / 64;  // 64-column atoms per row
+  static constexpr int kAtoms = D / 64;
   static constexpr int kGroup = kAtoms * 1024;
-  static constexpr int kKvTile = kAtoms * kKvAtom;
-  static constexpr int kK = 0;
-  static constexpr int kV = kK + kKStages * kKvTile;
-  // row-max exchange [2 tiles][2 halves][128] and row-sum exchange [2][128] floats
-  static constexpr int kRed = kV + kVStages * kKvTile;
-  static constexpr int kBar = kRed + 3 * 2 * kBM * 4;
+  static constexpr int kQTile = (kBM / 8) * kGroup;
+  static constexpr int kKvTile = (kBN / 8) * kGroup;
+  static constexpr int kQ = 0;
+  static constexpr int kK = kQ + kRowTiles * kQTile;
+  static constexpr int kV = kK + kStages * kKvTile;
+  static constexpr int kBar = kV + kStages * kKvTile;
   static constexpr int kTmemSlot = kBar + kBarSlots * 8;
   // + 1024-byte alignment slack; at least 116 KiB so that one CTA (which
   // takes all of tensor memory) is resident per SM
   static constexpr int kBytes =
       kTmemSlot + 16 + 1024 > 116 * 1024 ? kTmemSlot + 16 + 1024 : 116 * 1024;
-  // tensor-memory columns: S buffers, O, Q (bf16/fp16 pairs), P buffers
-  static constexpr int kColO = kBufs * kBN;
-  static constexpr int kColQ = kColO + D;
-  static constexpr int kColP = kColQ + D / 2;
-  static_assert(kColP + kBufs * kBN / 2 <= kTmemCols, "tensor memory overflow");
+  static_assert(kBytes <= 227 * 1024, "shared memory overflow");
+  // tensor-memory columns
+  static constexpr int kColO = kRowTiles * kBN;
+  static_assert(kColO + kRowTiles * D <= kTmemCols, "tensor memory overflow");
 };
 
 struct PrefillParams {
@@ -127,6 +117,15 @@ __device__ __forceinline__ uint32_t instr_desc(bool bf16, bool b_mn_major, int n
   const uint32_t ab = bf16 ? 1u : 0u;
   return (1u << 4) | (ab << 7) | (ab << 10) | ((b_mn_major ? 1u : 0u) << 16) |
          ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+}
+
+// D (+)= A.B with both operands described by shared-memory descriptors.
+__device__ __forceinline__ void mma_f16_ss(uint32_t d_tmem, uint64_t a, uint64_t b,
+                                           uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
 }
 
 // D (+)= A.B with the A operand read from tensor memory (row r in lane r,
@@ -207,15 +206,6 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-__device__ __forceinline__ void tmem_st16u(uint32_t taddr, const uint32_t (&w)[16]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
-      "%13,%14,%15,%16};" ::"r"(taddr),
-      "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7]),
-      "r"(w[8]), "r"(w[9]), "r"(w[10]), "r"(w[11]), "r"(w[12]), "r"(w[13]), "r"(w[14]), "r"(w[15])
-      : "memory");
-}
-
 __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
@@ -230,6 +220,36 @@ __device__ __forceinline__ void tma_load_group(void* dst, const CUtensorMap* map
       : "memory");
 }
 
+// 32 consecutive 32-bit columns of packed pairs into this thread's lane.
+__device__ __forceinline__ void tmem_st32u(uint32_t taddr, const uint32_t* w) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+      "%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(
+          taddr),
+      "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7]),
+      "r"(w[8]), "r"(w[9]), "r"(w[10]), "r"(w[11]), "r"(w[12]), "r"(w[13]), "r"(w[14]),
+      "r"(w[15]), "r"(w[16]), "r"(w[17]), "r"(w[18]), "r"(w[19]), "r"(w[20]), "r"(w[21]),
+      "r"(w[22]), "r"(w[23]), "r"(w[24]), "r"(w[25]), "r"(w[26]), "r"(w[27]), "r"(w[28]),
+      "r"(w[29]), "r"(w[30]), "r"(w[31])
+      : "memory");
+}
+
+// Wait for a barrier phase for at most the wait limit, whatever the sticky
+// timeout flag says: used only to let this CTA's own copies and MMAs finish
+// before it exits.
+__device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity) {
+  const unsigned long long t0 = global_ns();
+  while (!mbar_try_wait(bar, parity) && global_ns() - t0 <= kWaitLimitNs) {
+  }
+}
+
+// Byte offset of 16-byte chunk c of row r in a tile of the layout above.
+template <int D>
+__device__ __forceinline__ uint32_t tile_chunk_offset(int r, int c) {
+  return (uint32_t)((r >> 3) * PrefillSmem<D>::kGroup + (c >> 3) * 1024 + (r & 7) * 128 +
+                    (((c & 7) ^ (r & 7)) << 4));
+}
+
 // ---- the kernel -----------------------------------------------------------
 
 template <typename T, int D>
@@ -237,35 +257,32 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     paged_prefill_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap kmap,
                          const __grid_constant__ CUtensorMap vmap) {
   using L = PrefillSmem<D>;
-  constexpr int kAtoms = L::kAtoms;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem =
       reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  unsigned char* sQ = smem + L::kQ;
   unsigned char* sK = smem + L::kK;
   unsigned char* sV = smem + L::kV;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBar);
-  uint64_t* k_full = bars;                   // K stage landed (TMA transaction bytes)
-  uint64_t* k_empty = k_full + kKStages;     // K stage consumed by Q K^T (MMA commit)
-  uint64_t* v_full = k_empty + kKStages;     // V stage landed
-  uint64_t* v_empty = v_full + kVStages;     // V stage consumed by P V
-  uint64_t* q_full = v_empty + kVStages;     // Q written to tensor memory (softmax threads)
-  uint64_t* s_full = q_full + 1;             // S buffer computed (MMA commit)
-  uint64_t* s_free = s_full + kBufs;         // S buffer read (softmax threads)
-  uint64_t* p_full = s_free + kBufs;         // P buffer written (softmax threads)
-  uint64_t* pv_done = p_full + kBufs;        // P V of that buffer finished (MMA commit)
-  static_assert(2 * kKStages + 2 * kVStages + 1 + 4 * kBufs <= kBarSlots,
-                "barrier area too small");
+  uint64_t* k_full = bars;                    // K slot landed (TMA transaction bytes)
+  uint64_t* k_empty = k_full + kStages;       // K slot consumed by both Q K^T (MMA commit)
+  uint64_t* v_full = k_empty + kStages;       // V slot landed
+  uint64_t* v_empty = v_full + kStages;       // V slot consumed by both P V
+  uint64_t* q_full = v_empty + kStages;       // [t] Q rows of tile t in shared memory
+  uint64_t* s_full = q_full + kRowTiles;      // [t] S_t computed (MMA commit)
+  uint64_t* p_full = s_full + kRowTiles;      // [t] P_t written, O_t rescaled (softmax)
+  uint64_t* pv_done = p_full + kRowTiles;     // [t] O_t += P_t V finished (MMA commit)
+  uint64_t* drain = pv_done + kRowTiles;      // [2] each issuer's last MMAs finished
+  static_assert(4 * kStages + 4 * kRowTiles + 2 <= kBarSlots, "barrier area too small");
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kTmemSlot);
-  float* red = reinterpret_cast<float*>(smem + L::kRed);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int qt = blockIdx.x;
   const int kvh = blockIdx.y;
   const int s = blockIdx.z;
   const int G = p.group;
   const int Gp = p.group_pow2;
-  const int qpt = kBM / Gp;  // queries per tile
+  const int qpt = kBM / Gp;  // queries per row tile
 
   const int q0 = p.query_start[s];
   const int nq = p.query_start[s + 1] - q0;
@@ -273,32 +290,37 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
   const long long cap_ll = min((long long)p.max_context_len,
                                (long long)p.max_blocks_per_seq * p.block_size);
   if (ctx < nq || ctx > cap_ll) {
-    if (threadIdx.x == 0 && qt == 0) atomicOr(p.status, PKV_DEV_BAD_CONTEXT_LEN);
+    if (threadIdx.x == 0 && blockIdx.x == 0) atomicOr(p.status, PKV_DEV_BAD_CONTEXT_LEN);
     if (ctx < nq || nq <= 0) return;  // nothing sensible to attend to
     ctx = (int)cap_ll;
   }
-  const int j_first = qt * qpt;
-  if (j_first >= nq) return;  // this tile has no queries
-  const int j_last = min(nq, j_first + qpt) - 1;
-  const int pos_max = ctx - nq + j_last;
-  const int n_tiles = pos_max / kBN + 1;
+  const int j0 = blockIdx.x * kRowTiles * qpt;  // first query of the CTA
+  if (j0 >= nq) return;                         // no queries here
+  // Key tiles each row tile needs (up to its last query's position); row
+  // tile 1 ends later, or is empty.
+  int n_t[kRowTiles];
+#pragma unroll
+  for (int t = 0; t < kRowTiles; ++t) {
+    const int jf = j0 + t * qpt;
+    n_t[t] = jf < nq ? (ctx - nq + min(nq, jf + qpt) - 1) / kBN + 1 : 0;
+  }
+  const int n_tiles = max(n_t[0], n_t[1]);
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kKStages; ++i) {
+    for (int i = 0; i < kStages; ++i) {
       mbar_init(&k_full[i], 1);
       mbar_init(&k_empty[i], 1);
-    }
-    for (int i = 0; i < kVStages; ++i) {
       mbar_init(&v_full[i], 1);
       mbar_init(&v_empty[i], 1);
     }
-    mbar_init(q_full, kSoftmaxThreads);
-    for (int b = 0; b < kBufs; ++b) {
-      mbar_init(&s_full[b], 1);
-      mbar_init(&s_free[b], kSoftmaxThreads);
-      mbar_init(&p_full[b], kSoftmaxThreads);
-      mbar_init(&pv_done[b], 1);
+    for (int t = 0; t < kRowTiles; ++t) {
+      mbar_init(&q_full[t], kBM);
+      mbar_init(&s_full[t], 1);
+      mbar_init(&p_full[t], kBM);
+      mbar_init(&pv_done[t], 1);
     }
+    mbar_init(&drain[0], 1);
+    mbar_init(&drain[1], 1);
     fence_barrier_init();
   }
   if (warp == kMmaWarp) {
@@ -311,185 +333,206 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tmem_o = tmem + L::kColO;  // S buffers at columns [0, 128)
-  const uint32_t tmem_q = tmem + L::kColQ;
-  const uint32_t tmem_p = tmem + L::kColP;
 
-  if (warp == kKProducerWarp || warp == kVProducerWarp || warp == kKProducerWarp2 ||
-      warp == kVProducerWarp2) {
-    // ----------------------------------------------------- K and V producers
-    // Two warps stream K tiles and two V tiles, each operand into its own
-    // ring, each warp of a pair taking every other tile: a TMA copy costs
-    // its issuing warp tens of cycles, and the two warps issue in parallel.
-    // Each tile's keys are loaded as runs of R rows; a run never crosses a
-    // block boundary (R divides both the block size and the tile).
-    const bool is_k = warp == kKProducerWarp || warp == kKProducerWarp2;
-    const int first = (warp == kKProducerWarp2 || warp == kVProducerWarp2) ? 1 : 0;
-    const int nstages = is_k ? kKStages : kVStages;
-    uint64_t* full = is_k ? k_full : v_full;
-    uint64_t* empty = is_k ? k_empty : v_empty;
-    unsigned char* ring = is_k ? sK : sV;
-    const CUtensorMap* map = is_k ? &kmap : &vmap;
+  if (warp == kProducerWarp0 || warp == kProducerWarp1) {
+    // ------------------------------------------------------------ producers
+    // Each warp loads K and then V of every other key tile into its slot of
+    // the two rings.  A tile's keys are runs of R rows that never cross a
+    // block boundary (R divides the block size and the tile); lane l copies
+    // run l with one TMA copy per operand.  The block-table entry of the
+    // warp's next tile is read before this tile's copies are issued, so its
+    // latency is spent while the warp waits for a free slot.
+    const int first = warp == kProducerWarp1 ? 1 : 0;
     const int B = p.block_size;
     const int R = B < kBN ? B : kBN;
     const int32_t* trow = p.block_tables + (size_t)s * p.max_blocks_per_seq;
-    // Lane l copies run l (all of its columns) with one TMA copy.  The
-    // block-table entry of this warp's next tile is read before this tile's copies
-    // are issued, so its latency is spent while the warp waits for the next
-    // free slot.
     const int seg = lane;
     auto table_entry = [&](int t) -> int {
       const int key = t * kBN + seg * R;
       return (seg < kBN / R && t < n_tiles && key < ctx) ? __ldg(trow + key / B) : 0;
     };
     int phys_next = table_entry(first);
+    int last_k = -1, last_v = -1;  // last tiles whose copies this warp issued
     for (int i = first; i < n_tiles; i += 2) {
-      const int st = i % nstages;
-      if (i >= nstages && !mbar_wait_warp(&empty[st], ((i / nstages) - 1) & 1, p.status)) break;
+      const int st = i % kStages;
+      const uint32_t ph = ((i / kStages) - 1) & 1;
+      if (i >= kStages && !mbar_wait_warp(&k_empty[st], ph, p.status)) break;
       const int key0 = i * kBN;
       const int nvalid = min(ctx, key0 + kBN) - key0;
       const int nseg = (nvalid + R - 1) / R;
+      const uint32_t bytes = (uint32_t)nseg * R * D * (uint32_t)sizeof(T);
       int phys = phys_next;
       phys_next = table_entry(i + 2);
-      if (lane == 0)
-        mbar_arrive_expect_tx(&full[st], (uint32_t)nseg * R * D * (uint32_t)sizeof(T));
-      __syncwarp();
-      if (seg < nseg) {
-        if ((unsigned)phys >= (unsigned)p.num_blocks) {
-          atomicOr(p.status, PKV_DEV_BAD_BLOCK_ID);
-          phys = 0;
-        }
-        const int key = key0 + seg * R;
-        const int y = (phys * p.num_kv_heads + kvh) * B + key % B;  // a multiple of 8
-        tma_load_group(ring + st * L::kKvTile + seg * (R / 8) * L::kGroup, map, y / 8, &full[st]);
+      if ((unsigned)phys >= (unsigned)p.num_blocks) {
+        if (seg < nseg) atomicOr(p.status, PKV_DEV_BAD_BLOCK_ID);
+        phys = 0;
       }
+      const int key = key0 + seg * R;
+      const int g = ((phys * p.num_kv_heads + kvh) * B + key % B) / 8;  // 8-row group
+      const uint32_t dst = (uint32_t)(st * L::kKvTile + seg * (R / 8) * L::kGroup);
+      if (lane == 0) mbar_arrive_expect_tx(&k_full[st], bytes);
+      __syncwarp();
+      if (seg < nseg) tma_load_group(sK + dst, &kmap, g, &k_full[st]);
+      last_k = i;
+      if (i >= kStages && !mbar_wait_warp(&v_empty[st], ph, p.status)) break;
+      if (lane == 0) mbar_arrive_expect_tx(&v_full[st], bytes);
+      __syncwarp();
+      if (seg < nseg) tma_load_group(sV + dst, &vmap, g, &v_full[st]);
+      last_v = i;
     }
-  } else if (warp == kMmaWarp || warp == kPvWarp) {
-    // ------------------------------------------------------- MMA issuers
-    // One thread issues the chain S_i = Q K_i^T, another P_j V_j.  A single
-    // thread issues a tcgen05.mma (or commit) only every ~50 cycles whatever
-    // its size, while S_i with N = 64 keeps the tensor core busy for 32
-    // cycles per k-step: two issuers keep it fed, and neither chain waits
-    // behind the other.  Each commit tracks only its own thread's MMAs.
+    // Copies still in flight at exit (only after a timeout) land before the
+    // CTA leaves: wait, bounded, for the last slots this warp filled.
+    if (last_k >= 0) mbar_drain(&k_full[last_k % kStages], (last_k / kStages) & 1);
+    if (last_v >= 0) mbar_drain(&v_full[last_v % kStages], (last_v / kStages) & 1);
+    __syncwarp();
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------ Q K^T issuer
+    // S_t of key tile i overwrites P_t of tile i - 1, so it waits for that
+    // P V; row tile 0 goes first and its softmax overlaps tile 1's MMAs.
     if (lane == 0) {
       constexpr bool bf16 = std::is_same<T, __nv_bfloat16>::value;
-      if (warp == kMmaWarp) {
-        const uint32_t idesc_s = instr_desc(bf16, false, kBN, kBM);
-        const uint32_t aK = smem_addr(sK);
-        bool ok = mbar_wait(q_full, 0, p.status);
-        for (int i = 0; ok && i < n_tiles; ++i) {
-          const int st = i % kKStages, b = i % kBufs;
-          if (!mbar_wait(&k_full[st], (i / kKStages) & 1, p.status)) break;
-          if (i >= kBufs && !mbar_wait(&s_free[b], ((i / kBufs) - 1) & 1, p.status)) break;
+      const uint32_t idesc_s = instr_desc(bf16, false, kBN, kBM);
+      const uint32_t aQ = smem_addr(sQ), aK = smem_addr(sK);
+      bool ok = true;
+      for (int i = 0; ok && i < n_tiles; ++i) {
+        const int st = i % kStages;
+        if (!mbar_wait(&k_full[st], (i / kStages) & 1, p.status)) break;
+#pragma unroll
+        for (int t = 0; t < kRowTiles; ++t) {
+          if (i >= n_t[t]) continue;
+          const bool ready = i == 0 ? mbar_wait(&q_full[t], 0, p.status)
+                                    : mbar_wait(&pv_done[t], (i - 1) & 1, p.status);
+          if (!ready) {
+            ok = false;
+            break;
+          }
           tc_fence_after();
 #pragma unroll
-          for (int ks = 0; ks < D / 16; ++ks)
-            mma_f16_ta(tmem + b * kBN, tmem_q + ks * 8,
-                       smem_desc(aK + st * L::kKvTile + (ks / 4) * 1024 + (ks % 4) * 32, 16,
-                                 L::kGroup),
-                       idesc_s, ks > 0);
-          mma_commit(&s_full[b]);
-          mma_commit(&k_empty[st]);
+          for (int ks = 0; ks < D / 16; ++ks) {
+            const uint32_t koff = (ks / 4) * 1024 + (ks % 4) * 32;
+            mma_f16_ss(tmem + t * kBN,
+                       smem_desc(aQ + t * L::kQTile + koff, 16, L::kGroup),
+                       smem_desc(aK + st * L::kKvTile + koff, 16, L::kGroup), idesc_s, ks > 0);
+          }
+          mma_commit(&s_full[t]);
         }
-      } else {
-        const uint32_t idesc_o = instr_desc(bf16, true, D, kBM);
-        const uint32_t aV = smem_addr(sV);
-        for (int j = 0; j < n_tiles; ++j) {
-          const int bj = j % kBufs, stj = j % kVStages;
-          if (!mbar_wait(&p_full[bj], (j / kBufs) & 1, p.status)) break;
-          if (!mbar_wait(&v_full[stj], (j / kVStages) & 1, p.status)) break;
+        if (ok) mma_commit(&k_empty[st]);
+      }
+      mma_commit(&drain[0]);
+      mbar_drain(&drain[0], 0);
+    }
+    __syncwarp();
+  } else if (warp == kPvWarp) {
+    // --------------------------------------------------------- P V issuer
+    constexpr bool bf16 = std::is_same<T, __nv_bfloat16>::value;
+    const uint32_t idesc_o = instr_desc(bf16, true, D, kBM);
+    const uint32_t aV = smem_addr(sV);
+    bool ok = true;
+    for (int i = 0; ok && i < n_tiles; ++i) {
+      const int st = i % kStages;
+      if (!mbar_wait_warp(&v_full[st], (i / kStages) & 1, p.status)) break;
+      // Key rows past the context (the tail of the last block, or rows no
+      // run was loaded into) must not feed NaN or stale values into P V
+      // (their P is 0, but 0 * NaN is NaN): this warp clears them first.
+      if (i * kBN + kBN > ctx) {
+        for (int r = max(ctx - i * kBN, 0) + lane; r < kBN; r += 32)
+#pragma unroll
+          for (int c = 0; c < D / 8; ++c)
+            *reinterpret_cast<uint4*>(sV + st * L::kKvTile + tile_chunk_offset<D>(r, c)) =
+                make_uint4(0, 0, 0, 0);
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+      }
+#pragma unroll
+      for (int t = 0; t < kRowTiles; ++t) {
+        if (i >= n_t[t]) continue;
+        if (!mbar_wait_warp(&p_full[t], i & 1, p.status)) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
           tc_fence_after();
           // V as an MN-major operand: 8-key groups kGroup bytes apart,
           // 64-column atoms 1024 bytes apart.
 #pragma unroll
           for (int ks = 0; ks < kBN / 16; ++ks)
-            mma_f16_ta(tmem_o, tmem_p + bj * (kBN / 2) + ks * 8,
-                       smem_desc(aV + stj * L::kKvTile + ks * 2 * L::kGroup, 1024, L::kGroup),
-                       idesc_o,
-                       (j > 0 || ks > 0) ? 1u : 0u);
-          mma_commit(&pv_done[bj]);
-          mma_commit(&v_empty[stj]);
+            mma_f16_ta(tmem + L::kColO + t * D, tmem + t * kBN + ks * 8,
+                       smem_desc(aV + st * L::kKvTile + ks * 2 * L::kGroup, 1024, L::kGroup),
+                       idesc_o, (i > 0 || ks > 0) ? 1u : 0u);
+          mma_commit(&pv_done[t]);
         }
+        __syncwarp();
       }
+      if (ok && lane == 0) mma_commit(&v_empty[st]);
+    }
+    if (lane == 0) {
+      mma_commit(&drain[1]);
+      mbar_drain(&drain[1], 0);
     }
     __syncwarp();
-  } else {
-    // ---------------------------------------------- softmax / epilogue (rows)
-    // Thread (wg, r): row r of the tile, columns [wg * half, (wg + 1) * half)
-    // of S, P and O, with half = 32 keys of S/P and D / 2 columns of O.
-    constexpr int kHalfS = kBN / 2;
-    constexpr int kHalfO = D / 2;
-    const int wg = warp >> 2;
+  } else if (warp < kSoftmaxWarps) {
+    // ------------------------------------------- softmax / epilogue (rows)
+    const int t = warp / 4;                 // row tile of this warpgroup
     const int r = threadIdx.x & (kBM - 1);  // row of the tile == TMEM lane
-    const int jq = j_first + r / Gp;
+    const int nt = n_t[t];
+    const int jq = j0 + t * qpt + r / Gp;
     const int g = r % Gp;
     const bool row_valid = (r / Gp) < qpt && jq < nq && g < G;
     const int pos = row_valid ? ctx - nq + jq : -1;
     const size_t row_elem =
         ((size_t)(q0 + (row_valid ? jq : 0)) * p.num_q_heads + kvh * G + (row_valid ? g : 0)) * D;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t tmem_s = tmem + t * kBN + lane_base;
+    const uint32_t tmem_o = tmem + L::kColO + t * D + lane_base;
 
-    // This thread's half of the Q row into tensor memory (the A operand of
-    // Q K^T): D/2 elements as D/4 columns of packed pairs.
+    // This row of Q into shared memory, in the K-major operand layout.
     {
-      const uint4* src = reinterpret_cast<const uint4*>(static_cast<const T*>(p.q) + row_elem) +
-                         wg * (D / 16);
-      uint32_t w[16];
+      const uint4* src = reinterpret_cast<const uint4*>(static_cast<const T*>(p.q) + row_elem);
+      unsigned char* dst = sQ + t * L::kQTile;
 #pragma unroll
-      for (int part = 0; part < D / 64; ++part) {
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const uint4 v = row_valid ? src[part * 4 + c] : make_uint4(0, 0, 0, 0);
-          w[c * 4 + 0] = v.x;
-          w[c * 4 + 1] = v.y;
-          w[c * 4 + 2] = v.z;
-          w[c * 4 + 3] = v.w;
-        }
-        tmem_st16u(tmem_q + wg * (D / 4) + part * 16 + lane_base, w);
+      for (int c = 0; c < D / 8; ++c) {
+        const uint4 v = row_valid ? src[c] : make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4*>(dst + tile_chunk_offset<D>(r, c)) = v;
       }
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(q_full);
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      mbar_arrive(&q_full[t]);
     }
 
-    float m_run = -CUDART_INF_F, l_run = 0.f;  // l_run: this half's share of the row sum
+    float m_run = -CUDART_INF_F, l_run = 0.f;
     bool ok = true;
-    for (int i = 0; i < n_tiles; ++i) {
-      const int b = i % kBufs;
-      // A wait that gives up (never expected) leaves ok false and the loop
-      // running without further waits, so that both halves still meet at
-      // every named barrier below.
-      if (ok && !mbar_wait_warp(&s_full[b], (i / kBufs) & 1, p.status)) ok = false;
+    for (int i = 0; i < nt; ++i) {
+      // A wait that gives up (never expected) leaves ok false; the loop then
+      // runs on without waiting and nothing it computes is stored.
+      if (ok && !mbar_wait_warp(&s_full[t], i & 1, p.status)) ok = false;
       tc_fence_after();
-      float sv[kHalfS];
-      tmem_ld32f(tmem + b * kBN + wg * kHalfS + lane_base, sv);
+      float sv[kBN];
+#pragma unroll
+      for (int c = 0; c < kBN / 32; ++c) tmem_ld32f(tmem_s + c * 32, sv + c * 32);
       tmem_wait_ld_bind(sv);
-      tc_fence_before();
-      mbar_arrive(&s_free[b]);
+      tmem_wait_ld_bind(sv + 32);
+      tmem_wait_ld_bind(sv + 64);
+      tmem_wait_ld_bind(sv + 96);
 
       // Causal mask, only on tiles where some row of the warp sees keys past
       // its position (the diagonal); elsewhere every key is visible.
-      const int key0 = i * kBN + wg * kHalfS;
-      if (__any_sync(0xffffffffu, key0 + kHalfS - 1 > pos)) {
+      const int key0 = i * kBN;
+      if (__any_sync(0xffffffffu, key0 + kBN - 1 > pos)) {
 #pragma unroll
-        for (int c = 0; c < kHalfS; ++c)
+        for (int c = 0; c < kBN; ++c)
           if (key0 + c > pos) sv[c] = -CUDART_INF_F;
       }
-      // Half-row max with 8 independent chains, then the other half's via
-      // shared memory (scaling by qscale > 0 commutes with the max).
+      // Row max with 8 independent chains (scaling by qscale > 0 commutes
+      // with the max).
       float mx[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k) mx[k] = sv[k];
 #pragma unroll
-      for (int c = 8; c < kHalfS; ++c) mx[c & 7] = fmaxf(mx[c & 7], sv[c]);
+      for (int c = 8; c < kBN; ++c) mx[c & 7] = fmaxf(mx[c & 7], sv[c]);
 #pragma unroll
       for (int k = 4; k >= 1; k >>= 1)
 #pragma unroll
         for (int j = 0; j < k; ++j) mx[j] = fmaxf(mx[j], mx[j + k]);
-      float* red_i = red + (i & 1) * 2 * kBM;
-      red_i[wg * kBM + r] = mx[0];
-      named_barrier_sync(1, kSoftmaxThreads);
-      const float mt = fmaxf(mx[0], red_i[(wg ^ 1) * kBM + r]) * p.qscale;
+      const float mt = mx[0] * p.qscale;
       // Lazy rescaling: the running max moves only when this tile exceeds it
       // by more than 8 (base 2), so P stays <= 2^8 and O is rescaled rarely.
       // Numerator and denominator share the same max, so the result is exact.
@@ -501,12 +544,13 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       float sm[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k) sm[k] = 0.f;
+      uint32_t w[kBN / 2];
 #pragma unroll
-      for (int c = 0; c < kHalfS; c += 2) {
+      for (int c = 0; c < kBN; c += 2) {
         const float2 x = __ffma2_rn(make_float2(sv[c], sv[c + 1]), qs2, nm2);
-        sv[c] = ex2(x.x);
-        sv[c + 1] = ex2(x.y);
-        sm[(c >> 1) & 7] += sv[c] + sv[c + 1];
+        const float e0 = ex2(x.x), e1 = ex2(x.y);
+        sm[(c >> 1) & 7] += e0 + e1;
+        w[c >> 1] = Cvt<T>::from_float2(e0, e1);
       }
 #pragma unroll
       for (int k = 4; k >= 1; k >>= 1)
@@ -515,86 +559,50 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       l_run = l_run * alpha + sm[0];
       m_run = m_new;
 
-      // P buffer b is free once the P V of tile i-2 is done.
-      if (ok && i >= kBufs && !mbar_wait_warp(&pv_done[b], ((i / kBufs) - 1) & 1, p.status))
-        ok = false;
-      // Rescaling O needs every earlier P V finished (the last is tile i-1).
+      // P (rounded to the operand type) over the first half of S's columns.
+      tmem_st32u(tmem_s, w);
+      tmem_st32u(tmem_s + 32, w + 32);
+      // O_t is quiescent here: S_t of this tile was issued only after the
+      // previous P V into O_t had finished.
       if (i > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-        const int bp = (i - 1) % kBufs;
-        if (ok && !mbar_wait_warp(&pv_done[bp], ((i - 1) / kBufs) & 1, p.status)) ok = false;
-        tc_fence_after();
         const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll
-        for (int c = 0; c < kHalfO / 32; ++c) {
-          float t[32];
-          const uint32_t ta = tmem_o + wg * kHalfO + lane_base + c * 32;
-          tmem_ld32f(ta, t);
-          tmem_wait_ld_bind(t);
+        for (int c = 0; c < D / 32; ++c) {
+          float o[32];
+          tmem_ld32f(tmem_o + c * 32, o);
+          tmem_wait_ld_bind(o);
 #pragma unroll
           for (int k = 0; k < 32; k += 2) {
-            const float2 y = __fmul2_rn(make_float2(t[k], t[k + 1]), a2);
-            t[k] = y.x;
-            t[k + 1] = y.y;
+            const float2 y = __fmul2_rn(make_float2(o[k], o[k + 1]), a2);
+            o[k] = y.x;
+            o[k + 1] = y.y;
           }
-          tmem_st32(ta, t);
+          tmem_st32(tmem_o + c * 32, o);
         }
-        tmem_wait_st();
       }
-      // This half of the P row, rounded to the operand type, into tensor
-      // memory (the A operand of P V).
-      {
-        uint32_t w[16];
-#pragma unroll
-        for (int c = 0; c < kHalfS / 2; ++c) w[c] = Cvt<T>::from_float2(sv[2 * c], sv[2 * c + 1]);
-        tmem_st16u(tmem_p + b * (kBN / 2) + wg * (kHalfS / 2) + lane_base, w);
-        tmem_wait_st();
-      }
-      // Key rows past the context (the tail of the last block, or rows no
-      // block was loaded into) must not feed NaN or stale values into P V.
-      if (i * kBN + kBN > ctx) {
-        // V of this tile must have landed before its tail rows are cleared.
-        if (ok && !mbar_wait_warp(&v_full[i % kVStages], (i / kVStages) & 1, p.status)) ok = false;
-      }
-      if (wg == 0 && r < kBN && i * kBN + r >= ctx) {
-        const int st = i % kVStages;
-#pragma unroll
-        for (int a = 0; a < kAtoms; ++a)
-#pragma unroll
-          for (int c = 0; c < 8; ++c)
-            *reinterpret_cast<uint4*>(sV + st * L::kKvTile + (r / 8) * L::kGroup + a * 1024 +
-                                      (r % 8) * 128 + c * 16) =
-                make_uint4(0, 0, 0, 0);
-      }
-      if (i * kBN + kBN > ctx)  // make the cleared V rows visible to the tensor core
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(&p_full[b]);
+      mbar_arrive(&p_full[t]);
     }
 
-    // The row sum is split between the two halves.
-    float* red_l = red + 2 * 2 * kBM;
-    red_l[wg * kBM + r] = l_run;
-    named_barrier_sync(1, kSoftmaxThreads);
-    const float l_row = l_run + red_l[(wg ^ 1) * kBM + r];
-    const int bl = (n_tiles - 1) % kBufs;
-    if (ok && mbar_wait_warp(&pv_done[bl], ((n_tiles - 1) / kBufs) & 1, p.status)) {
+    if (nt > 0 && ok && mbar_wait_warp(&pv_done[t], (nt - 1) & 1, p.status)) {
       tc_fence_after();
-      const float inv = l_row > 0.f ? 1.f / l_row : 0.f;
-      T* orow = static_cast<T*>(p.out) + row_elem + wg * kHalfO;
+      const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+      T* orow = static_cast<T*>(p.out) + row_elem;
 #pragma unroll
-      for (int c = 0; c < kHalfO / 32; ++c) {
-        float t[32];
-        tmem_ld32f(tmem_o + wg * kHalfO + lane_base + c * 32, t);
-        tmem_wait_ld_bind(t);
+      for (int c = 0; c < D / 32; ++c) {
+        float o[32];
+        tmem_ld32f(tmem_o + c * 32, o);
+        tmem_wait_ld_bind(o);
         if (row_valid) {
 #pragma unroll
           for (int k = 0; k < 32; k += 8) {
-            uint4 w;
-            w.x = Cvt<T>::from_float2(t[k] * inv, t[k + 1] * inv);
-            w.y = Cvt<T>::from_float2(t[k + 2] * inv, t[k + 3] * inv);
-            w.z = Cvt<T>::from_float2(t[k + 4] * inv, t[k + 5] * inv);
-            w.w = Cvt<T>::from_float2(t[k + 6] * inv, t[k + 7] * inv);
-            *reinterpret_cast<uint4*>(orow + c * 32 + k) = w;
+            uint4 v;
+            v.x = Cvt<T>::from_float2(o[k] * inv, o[k + 1] * inv);
+            v.y = Cvt<T>::from_float2(o[k + 2] * inv, o[k + 3] * inv);
+            v.z = Cvt<T>::from_float2(o[k + 4] * inv, o[k + 5] * inv);
+            v.w = Cvt<T>::from_float2(o[k + 6] * inv, o[k + 7] * inv);
+            *reinterpret_cast<uint4*>(orow + c * 32 + k) = v;
           }
         }
       }
@@ -627,8 +635,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 2-D view of a cache: rows (block, head, slot), columns head_dim; boxes of
-// 64 columns x min(block_size, 64) rows, 128-byte swizzle.
+// 4-D view of a cache for TMA: see below; boxes of min(block_size, 128)
+// rows, 128-byte swizzle.
 bool make_cache_map(CUtensorMap* map, const void* base, int dtype, long long rows, int head_dim,
                     int block_size) {
   PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
@@ -700,8 +708,8 @@ cudaError_t launch_paged_prefill(const PrefillArgs& a, cudaStream_t stream, bool
   p.block_size = a.block_size;
   p.num_blocks = a.num_blocks;
   p.qscale = a.scale * 1.4426950408889634f;
-  const int qpt = kBM / gp;
-  const int q_tiles = (a.max_query_len + qpt - 1) / qpt;
+  const int rows_q = kRowTiles * (kBM / gp);  // queries per CTA
+  const int q_tiles = (a.max_query_len + rows_q - 1) / rows_q;
   if (a.dtype == PKV_F16) {
     return a.head_dim == 64
                ? launch_prefill_typed<__half, 64>(p, km, vm, q_tiles, a.num_seqs, stream)
