@@ -153,24 +153,6 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
-      "%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(
-          taddr),
-      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
-      "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
-      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
-      "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
-      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
-      "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])),
-      "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])),
-      "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
-      "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
-      "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
-      "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
-      : "memory");
-}
 
 // 32 consecutive 32-bit columns of this thread's TMEM lane, loaded straight
 // into float registers, and a wait that names them, so that no use of the
@@ -204,6 +186,46 @@ __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+// max(a, b, c) in one instruction.
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// 16 consecutive 32-bit columns of this thread's lane, the wait that binds
+// them, and the store back.
+__device__ __forceinline__ void tmem_ld16f(uint32_t taddr, float* v) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15}, [%16];"
+      : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3]), "=f"(v[4]), "=f"(v[5]), "=f"(v[6]),
+        "=f"(v[7]), "=f"(v[8]), "=f"(v[9]), "=f"(v[10]), "=f"(v[11]), "=f"(v[12]), "=f"(v[13]),
+        "=f"(v[14]), "=f"(v[15])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_wait_ld_bind16(float* v) {
+  asm volatile(
+      "tcgen05.wait::ld.sync.aligned;"
+      : "+f"(v[0]), "+f"(v[1]), "+f"(v[2]), "+f"(v[3]), "+f"(v[4]), "+f"(v[5]), "+f"(v[6]),
+        "+f"(v[7]), "+f"(v[8]), "+f"(v[9]), "+f"(v[10]), "+f"(v[11]), "+f"(v[12]), "+f"(v[13]),
+        "+f"(v[14]), "+f"(v[15])
+      :
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st16f(uint32_t taddr, const float* v) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+      "%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+      "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+      "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+      "r"(__float_as_uint(v[15]))
+      : "memory");
 }
 
 __device__ __forceinline__ void tmem_wait_st() {
@@ -270,10 +292,11 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
   uint64_t* v_empty = v_full + kStages;       // V slot consumed by both P V
   uint64_t* q_full = v_empty + kStages;       // [t] Q rows of tile t in shared memory
   uint64_t* s_full = q_full + kRowTiles;      // [t] S_t computed (MMA commit)
-  uint64_t* p_full = s_full + kRowTiles;      // [t] P_t written, O_t rescaled (softmax)
-  uint64_t* pv_done = p_full + kRowTiles;     // [t] O_t += P_t V finished (MMA commit)
+  uint64_t* p_full = s_full + kRowTiles;      // [t][h] keys of half h of P_t written
+                                              // (after O_t was rescaled; softmax)
+  uint64_t* pv_done = p_full + 2 * kRowTiles; // [t] O_t += P_t V finished (MMA commit)
   uint64_t* drain = pv_done + kRowTiles;      // [2] each issuer's last MMAs finished
-  static_assert(4 * kStages + 4 * kRowTiles + 2 <= kBarSlots, "barrier area too small");
+  static_assert(4 * kStages + 5 * kRowTiles + 2 <= kBarSlots, "barrier area too small");
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kTmemSlot);
 
   const int warp = threadIdx.x >> 5;
@@ -316,7 +339,8 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     for (int t = 0; t < kRowTiles; ++t) {
       mbar_init(&q_full[t], kBM);
       mbar_init(&s_full[t], 1);
-      mbar_init(&p_full[t], kBM);
+      mbar_init(&p_full[2 * t], kBM);
+      mbar_init(&p_full[2 * t + 1], kBM);
       mbar_init(&pv_done[t], 1);
     }
     mbar_init(&drain[0], 1);
@@ -446,21 +470,28 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
 #pragma unroll
       for (int t = 0; t < kRowTiles; ++t) {
         if (i >= n_t[t]) continue;
-        if (!mbar_wait_warp(&p_full[t], i & 1, p.status)) {
-          ok = false;
-          break;
-        }
-        if (lane == 0) {
-          tc_fence_after();
-          // V as an MN-major operand: 8-key groups kGroup bytes apart,
-          // 64-column atoms 1024 bytes apart.
+        // P arrives in two halves of the keys; the first half's MMAs run
+        // while the softmax computes the second.
 #pragma unroll
-          for (int ks = 0; ks < kBN / 16; ++ks)
-            mma_f16_ta(tmem + L::kColO + t * D, tmem + t * kBN + ks * 8,
-                       smem_desc(aV + st * L::kKvTile + ks * 2 * L::kGroup, 1024, L::kGroup),
-                       idesc_o, (i > 0 || ks > 0) ? 1u : 0u);
-          mma_commit(&pv_done[t]);
+        for (int h = 0; h < 2; ++h) {
+          if (!mbar_wait_warp(&p_full[2 * t + h], i & 1, p.status)) {
+            ok = false;
+            break;
+          }
+          if (lane == 0) {
+            tc_fence_after();
+            // V as an MN-major operand: 8-key groups kGroup bytes apart,
+            // 64-column atoms 1024 bytes apart.
+#pragma unroll
+            for (int ks = h * kBN / 32; ks < (h + 1) * kBN / 32; ++ks)
+              mma_f16_ta(tmem + L::kColO + t * D, tmem + t * kBN + ks * 8,
+                         smem_desc(aV + st * L::kKvTile + ks * 2 * L::kGroup, 1024, L::kGroup),
+                         idesc_o, (i > 0 || ks > 0) ? 1u : 0u);
+          }
+          __syncwarp();
         }
+        if (!ok) break;
+        if (lane == 0) mma_commit(&pv_done[t]);
         __syncwarp();
       }
       if (ok && lane == 0) mma_commit(&v_empty[st]);
@@ -505,34 +536,42 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       // runs on without waiting and nothing it computes is stored.
       if (ok && !mbar_wait_warp(&s_full[t], i & 1, p.status)) ok = false;
       tc_fence_after();
-      float sv[kBN];
-#pragma unroll
-      for (int c = 0; c < kBN / 32; ++c) tmem_ld32f(tmem_s + c * 32, sv + c * 32);
-      tmem_wait_ld_bind(sv);
-      tmem_wait_ld_bind(sv + 32);
-      tmem_wait_ld_bind(sv + 64);
-      tmem_wait_ld_bind(sv + 96);
-
       // Causal mask, only on tiles where some row of the warp sees keys past
       // its position (the diagonal); elsewhere every key is visible.
       const int key0 = i * kBN;
-      if (__any_sync(0xffffffffu, key0 + kBN - 1 > pos)) {
+      const bool diag = __any_sync(0xffffffffu, key0 + kBN - 1 > pos);
+      // First pass over the S row: its maximum.  The exponentials re-read
+      // S from tensor memory half a row at a time, which keeps the live
+      // registers to half a row.
+      float mt;
+      {
+        float sv[kBN];
 #pragma unroll
-        for (int c = 0; c < kBN; ++c)
-          if (key0 + c > pos) sv[c] = -CUDART_INF_F;
-      }
+        for (int c = 0; c < kBN / 32; ++c) tmem_ld32f(tmem_s + c * 32, sv + c * 32);
+#pragma unroll
+        for (int c = 0; c < kBN / 32; ++c) tmem_wait_ld_bind(sv + c * 32);
+        if (diag) {
+#pragma unroll
+          for (int c = 0; c < kBN; ++c)
+            if (key0 + c > pos) sv[c] = -CUDART_INF_F;
+        }
       // Row max with 8 independent chains (scaling by qscale > 0 commutes
       // with the max).
       float mx[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k) mx[k] = sv[k];
+      constexpr int kTriples = (kBN - 8) / 16;  // columns 8 .. 8 + 16 kTriples - 1, in threes
 #pragma unroll
-      for (int c = 8; c < kBN; ++c) mx[c & 7] = fmaxf(mx[c & 7], sv[c]);
+      for (int c = 0; c < kTriples; ++c)
 #pragma unroll
-      for (int k = 4; k >= 1; k >>= 1)
+        for (int k = 0; k < 8; ++k) mx[k] = fmax3(mx[k], sv[8 + 16 * c + k], sv[16 + 16 * c + k]);
 #pragma unroll
-        for (int j = 0; j < k; ++j) mx[j] = fmaxf(mx[j], mx[j + k]);
-      const float mt = mx[0] * p.qscale;
+      for (int c = 8 + 16 * kTriples; c < kBN; c += 8)
+#pragma unroll
+        for (int k = 0; k < 8; ++k) mx[k] = fmaxf(mx[k], sv[c + k]);
+        mt = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])) *
+             p.qscale;
+      }
       // Lazy rescaling: the running max moves only when this tile exceeds it
       // by more than 8 (base 2), so P stays <= 2^8 and O is rescaled rarely.
       // Numerator and denominator share the same max, so the result is exact.
@@ -541,48 +580,62 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       const float negm = (m_new == -CUDART_INF_F) ? 0.f : -m_new;
       const float2 qs2 = make_float2(p.qscale, p.qscale);
       const float2 nm2 = make_float2(negm, negm);
-      float sm[8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) sm[k] = 0.f;
-      uint32_t w[kBN / 2];
-#pragma unroll
-      for (int c = 0; c < kBN; c += 2) {
-        const float2 x = __ffma2_rn(make_float2(sv[c], sv[c + 1]), qs2, nm2);
-        const float e0 = ex2(x.x), e1 = ex2(x.y);
-        sm[(c >> 1) & 7] += e0 + e1;
-        w[c >> 1] = Cvt<T>::from_float2(e0, e1);
-      }
-#pragma unroll
-      for (int k = 4; k >= 1; k >>= 1)
-#pragma unroll
-        for (int j = 0; j < k; ++j) sm[j] += sm[j + k];
-      l_run = l_run * alpha + sm[0];
-      m_run = m_new;
-
-      // P (rounded to the operand type) over the first half of S's columns.
-      tmem_st32u(tmem_s, w);
-      tmem_st32u(tmem_s + 32, w + 32);
-      // O_t is quiescent here: S_t of this tile was issued only after the
-      // previous P V into O_t had finished.
+      // O_t is quiescent here (S_t of this tile was issued only after the
+      // previous P V into O_t had finished): rescale it, if the max moved,
+      // before any P of this tile is released.
       if (i > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
         const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          float o[32];
-          tmem_ld32f(tmem_o + c * 32, o);
-          tmem_wait_ld_bind(o);
+        for (int c = 0; c < D / 16; ++c) {
+          float o[16];
+          tmem_ld16f(tmem_o + c * 16, o);
+          tmem_wait_ld_bind16(o);
 #pragma unroll
-          for (int k = 0; k < 32; k += 2) {
+          for (int k = 0; k < 16; k += 2) {
             const float2 y = __fmul2_rn(make_float2(o[k], o[k + 1]), a2);
             o[k] = y.x;
             o[k + 1] = y.y;
           }
-          tmem_st32(tmem_o + c * 32, o);
+          tmem_st16f(tmem_o + c * 16, o);
         }
       }
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(&p_full[t]);
+      // P, rounded to the operand type, over the first half of S's columns,
+      // computed and released in two halves of the keys.
+      float2 sm[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) sm[k] = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        // Keys [64 h, 64 h + 64): S columns 64 h .. 64 h + 63, still intact (P
+        // of the first half went to columns 0..31).
+        float sv[kBN / 2];
+        tmem_ld32f(tmem_s + h * (kBN / 2), sv);
+        tmem_ld32f(tmem_s + h * (kBN / 2) + 32, sv + 32);
+        tmem_wait_ld_bind(sv);
+        tmem_wait_ld_bind(sv + 32);
+        if (diag) {
+#pragma unroll
+          for (int c = 0; c < kBN / 2; ++c)
+            if (key0 + h * (kBN / 2) + c > pos) sv[c] = -CUDART_INF_F;
+        }
+        uint32_t w[kBN / 4];
+#pragma unroll
+        for (int c = 0; c < kBN / 2; c += 2) {
+          const float2 x = __ffma2_rn(make_float2(sv[c], sv[c + 1]), qs2, nm2);
+          float2 e;
+          e.x = ex2(x.x);
+          e.y = ex2(x.y);
+          sm[(c >> 1) & 3] = __fadd2_rn(sm[(c >> 1) & 3], e);
+          w[c >> 1] = Cvt<T>::from_float2(e.x, e.y);
+        }
+        tmem_st32u(tmem_s + h * (kBN / 4), w);
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&p_full[2 * t + h]);
+      }
+      sm[0] = __fadd2_rn(__fadd2_rn(sm[0], sm[1]), __fadd2_rn(sm[2], sm[3]));
+      l_run = l_run * alpha + (sm[0].x + sm[0].y);
+      m_run = m_new;
     }
 
     if (nt > 0 && ok && mbar_wait_warp(&pv_done[t], (nt - 1) & 1, p.status)) {
