@@ -76,7 +76,7 @@ def source_hash(*names):
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(kernel_key, workload):
+def ncu_traffic(kernel_key, workload, sources=("decode.cu", "common.cuh")):
     """DRAM bytes per launch from a committed ncu summary, if it was taken on
     the current kernel source (else None)."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
@@ -85,7 +85,7 @@ def ncu_traffic(kernel_key, workload):
             rec = json.load(f)[workload][kernel_key]
     except (OSError, KeyError, ValueError):
         return None
-    if rec.get("source_hash") != source_hash("decode.cu", "common.cuh"):
+    if rec.get("source_hash") != source_hash(*sources):
         return None
     return rec.get("dram_bytes_per_launch")
 
@@ -579,7 +579,8 @@ def run_prefill(args, rank, world, local_rank):
                      "achieved": round(tflops, 2), "peak": peak, "peak_kind": kind,
                      "unit": "TFLOP/s", "frac": round(tflops / peak, 4),
                      "frac_issued": round(issued / (ms * 1e-3) / 1e12 / peak, 4),
-                     "traffic": None},
+                     "traffic": ncu_traffic("paged_prefill_kernel", "prefill",
+                                            ("prefill.cu", "common.cuh")) if S == w["num_seqs"] else None},
         "e2e": {"value": round(flops / (e2e_ms * 1e-3) / 1e12 * world, 2), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": q_host.numel() * 2, "d2h_bytes_per_step": out_host.numel() * 2},
         "gpu_launches": K, "clocks": clock_rec,

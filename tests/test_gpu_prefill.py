@@ -79,3 +79,33 @@ def test_long_prompt_chunks(cuda_device):
         case.context_lens.fill_(done)
         q, out, ref, qs = _run(case, [chunk], seed=done)
         assert_within_tol(out, ref, torch.bfloat16, f"chunk ending at {done}")
+
+
+def test_prefill_full_size_sampled(cuda_device):
+    """The bench's workload (8 sequences x 2,048-query chunks over 4,096 tokens,
+    32 q / 8 kv heads, D = 128, B = 16, bf16) in the bench's launch, checked on
+    sampled outputs: causal attention of the query at position p is decode
+    attention over positions 0..p, which the oracle computes for one query
+    from that sequence's own blocks."""
+    case, q, qs = W.prefill_chunks(device=cuda_device)
+    w = W.PREFILL_CHUNKS
+    out = torch.full_like(q, float("nan"))
+    pkv.paged_attn_prefill(out, q, qs, case.k_cache, case.v_cache, case.block_tables,
+                           case.context_lens, case.scale, case.max_context_len, w["chunk"])
+    torch.cuda.synchronize()
+    assert not torch.isnan(out).any()
+    S, L, B = w["num_seqs"], w["chunk"], w["block_size"]
+    rng = np.random.default_rng(11)
+    # the first and last query of a sequence, both row tiles of a CTA, and random ones
+    picks = [(0, 0), (S - 1, L - 1), (1, 63), (2, 64), (3, 1000)]
+    picks += [(int(rng.integers(S)), int(rng.integers(L))) for _ in range(7)]
+    tables = case.block_tables.cpu().numpy()
+    for s, j in picks:
+        p = int(case.context_lens[s]) - L + j
+        nb = -(-(p + 1) // B)
+        blocks = torch.from_numpy(tables[s, :nb].astype(np.int64)).to(cuda_device)
+        k_sub, v_sub = to_f64(case.k_cache[blocks]), to_f64(case.v_cache[blocks])
+        row = int(qs[s]) + j
+        ref = oracle.paged_decode_attention(to_f64(q[row:row + 1]), k_sub, v_sub,
+                                            np.arange(nb)[None, :], np.array([p + 1]), case.scale)
+        assert_within_tol(out[row:row + 1], ref, torch.bfloat16, f"prefill seq {s} query {j}")
