@@ -217,6 +217,66 @@ def contiguous_baseline(pkv, case, out, part, dev, stream, iters):
             "partition_size": part, "iters": iters}
 
 
+def cache_ops_bench(pkv, case, dev, stream, peak, iters=30, fill_blocks=400, cow_pairs=112):
+    """The two cache-maintenance kernels on their large instances, each call
+    timed alone with CUDA events after reading a buffer larger than L2:
+    a prompt fill (kv_append of fill_blocks whole blocks, block_size tokens
+    each, into blocks drawn at random from the pool) and a copy-on-write batch
+    (block_copy of cow_pairs distinct source -> destination blocks).  Bytes
+    moved = everything read plus everything written."""
+    S, Hq, D = case.q.shape
+    Hkv, B, NB = case.k_cache.shape[1], case.block_size, case.k_cache.shape[0]
+    e = case.q.element_size()
+    gen = torch.Generator(device="cpu")
+    gen.manual_seed(1234)
+    perm = torch.randperm(NB, generator=gen)
+    n_fill = min(fill_blocks, NB)
+    T = n_fill * B
+    slots = (perm[:n_fill, None] * B + torch.arange(B)[None, :]).reshape(-1).to(dev)
+    k_new = torch.randn((T, Hkv, D), generator=gen).to(case.q.dtype).to(dev)
+    v_new = torch.randn((T, Hkv, D), generator=gen).to(case.q.dtype).to(dev)
+    n_cow = min(cow_pairs, NB // 2)
+    pairs = torch.stack([perm[:n_cow], perm[n_cow:2 * n_cow]], dim=1).to(torch.int64).to(dev)
+    kc, vc = case.k_cache.clone(), case.v_cache.clone()
+    # L2 is flushed by reading 256 MiB (a write would leave dirty lines whose
+    # write-back would compete with the timed call for DRAM bandwidth)
+    flush = torch.ones(32 << 20, dtype=torch.float64, device=dev)
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        total = 0.0
+        for _ in range(iters):
+            flush.sum()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            torch.cuda.synchronize()
+            total += a.elapsed_time(b)
+        return total / iters
+
+    pkv.device_status(clear=True)
+    t_app = timed(lambda: pkv.kv_append(k_new, v_new, kc, vc, slots))
+    t_cow = timed(lambda: pkv.block_copy(kc, vc, pairs))
+    if pkv.device_status(clear=True) != 0:
+        raise RuntimeError("device status flags during the cache-operation bench")
+    b_app = 2 * (2 * T * Hkv * D * e)          # K and V rows read, then written
+    b_cow = 2 * (2 * n_cow * Hkv * B * D * e)  # K and V blocks read, then written
+    del kc, vc, flush
+    torch.cuda.empty_cache()
+
+    def rec(ms, nbytes, what):
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        return {"what": what, "bytes_moved": nbytes, "ms": round(ms, 5), "GB/s": round(gbs, 1),
+                "frac_of_peak": round(gbs / peak, 4)}
+
+    return {"kv_append_prompt_fill": rec(t_app, b_app, f"{T} tokens x {Hkv} heads into {n_fill} "
+                                         "random blocks"),
+            "block_copy_cow_batch": rec(t_cow, b_cow, f"{n_cow} block pairs, K and V"),
+            "l2": "flushed (256 MiB read) before every timed call", "iters": iters}
+
+
 # ------------------------------------------------------------- CPU legs --
 
 def oracle_sample_rate(case, k_new, v_new, slots, seconds, max_seqs=None):
@@ -421,6 +481,7 @@ def run_ours(args, rank, world, local_rank):
     # max_context_len and no block table; the ratio of the two decode times
     # is the cost of the indirection.
     contig = contiguous_baseline(pkv, case, out, part, dev, stream, max(20, K // 10))
+    cache_ops = cache_ops_bench(pkv, case, dev, stream, peak_hbm()[0])
 
     decode_b, append_b = step_bytes(case)
     ms_step = elapsed_ms / K
@@ -465,6 +526,7 @@ def run_ours(args, rank, world, local_rank):
         "path": args.path,
         "other_path": alt,
         "contiguous_baseline": contig,
+        "cache_ops": cache_ops,
         "gpu_launches": K * launches_per_step,
         "clocks": clock_rec,
     }

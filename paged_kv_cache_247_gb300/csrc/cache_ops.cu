@@ -24,6 +24,7 @@ namespace {
 
 constexpr int kCopyThreads = 256;
 constexpr int kUnroll = 4;
+constexpr int kCopyUnroll = 8;  // block_copy: 16 chunks (K and V) in flight per thread
 
 __device__ __forceinline__ uint4 load_stream(const uint4* p) {
   uint4 r;
@@ -95,19 +96,21 @@ __global__ void __launch_bounds__(kCopyThreads)
     const uint4* vs = v_cache + src * chunks_per_block;
     uint4* kd = k_cache + dst * chunks_per_block;
     uint4* vd = v_cache + dst * chunks_per_block;
-    for (long long c0 = (long long)blockIdx.x * kCopyThreads * kUnroll + threadIdx.x;
-         c0 < chunks_per_block; c0 += (long long)gridDim.x * kCopyThreads * kUnroll) {
-      uint4 rk[kUnroll], rv[kUnroll];
+    for (long long c0 = (long long)blockIdx.x * kCopyThreads * kCopyUnroll + threadIdx.x;
+         c0 < chunks_per_block; c0 += (long long)gridDim.x * kCopyThreads * kCopyUnroll) {
+      uint4 rk[kCopyUnroll], rv[kCopyUnroll];
 #pragma unroll
-      for (int u = 0; u < kUnroll; ++u) {
+      for (int u = 0; u < kCopyUnroll; ++u) {
         const long long c = c0 + u * kCopyThreads;
         if (c < chunks_per_block) {
-          rk[u] = ks[c];
-          rv[u] = vs[c];
+          // Sources are read-only for the whole launch (no destination may
+          // be a source in the same call), so the non-coherent path is safe.
+          rk[u] = load_stream(ks + c);
+          rv[u] = load_stream(vs + c);
         }
       }
 #pragma unroll
-      for (int u = 0; u < kUnroll; ++u) {
+      for (int u = 0; u < kCopyUnroll; ++u) {
         const long long c = c0 + u * kCopyThreads;
         if (c < chunks_per_block) {
           kd[c] = rk[u];
@@ -140,7 +143,7 @@ cudaError_t launch_block_copy(void* k_cache, void* v_cache, const int64_t* pairs
                               int num_blocks, size_t block_bytes, unsigned int* status,
                               cudaStream_t stream) {
   const long long cpb = (long long)(block_bytes / 16);
-  long long gx = (cpb + kCopyThreads * kUnroll - 1) / (kCopyThreads * kUnroll);
+  long long gx = (cpb + kCopyThreads * kCopyUnroll - 1) / (kCopyThreads * kCopyUnroll);
   if (gx > 65535) gx = 65535;
   const int gy = num_pairs < 65535 ? num_pairs : 65535;
   block_copy_kernel<<<dim3((unsigned)gx, gy), kCopyThreads, 0, stream>>>(
