@@ -106,3 +106,35 @@ def test_append_and_copy_host_validation(lib):
     assert lib.pkv_block_copy(None, None, None, 0, 4, 4096, None) == 0
     assert lib.pkv_block_copy(16, 16, 16, 2, 4, 4090, None) == 1
     assert lib.pkv_block_copy(16, 16, None, 2, 4, 4096, None) == 1
+
+
+def _prefill(lib, **over):
+    a = dict(out=16, q=16, qs=16, mql=8, k=16, v=16, tables=16, mbps=4, lens=16, maxctx=64, S=2,
+             Hq=8, Hkv=2, D=128, B=16, NB=10, scale=0.1, dtype=1)
+    a.update(over)
+    return lib.pkv_paged_attn_prefill(a["out"], a["q"], a["qs"], a["mql"], a["k"], a["v"],
+                                      a["tables"], a["mbps"], a["lens"], a["maxctx"], a["S"],
+                                      a["Hq"], a["Hkv"], a["D"], a["B"], a["NB"], a["scale"],
+                                      a["dtype"], None)
+
+
+@pytest.mark.parametrize("over,expect", [
+    (dict(Hq=6, Hkv=4), 1),             # Hq not a multiple of Hkv
+    (dict(D=96), 2),                    # head_dim not built
+    (dict(B=24), 2),                    # block size not built
+    (dict(B=4), 2),                     # runs shorter than an 8-row TMA group
+    (dict(dtype=7), 1),
+    (dict(Hq=256, Hkv=1), 2),           # group larger than a 128-row tile
+    (dict(mql=-1), 1),
+    (dict(scale=float("nan")), 1),
+    (dict(qs=None), 1),
+    (dict(k=8), 1),                     # misaligned cache
+    (dict(qs=2), 1),                    # misaligned int32 offsets
+    (dict(mbps=3), 1),                  # 3 * 16 < 64 = max context
+    (dict(NB=0), 1),
+    (dict(S=70000), 2),                 # grid limit
+    (dict(S=0, q=None), 0),             # empty batch is a no-op
+    (dict(mql=0, q=None), 0),           # no queries: a no-op
+])
+def test_prefill_host_validation(lib, over, expect):
+    assert _prefill(lib, **over) == expect
