@@ -260,7 +260,8 @@ pkv_status_t pkv_contiguous_attn_decode(
  *   num_q_heads / num_kv_heads <= 128
  * Other arguments as pkv_paged_attn_decode.  Errors: PKV_ERR_INVALID_ARG,
  * PKV_ERR_UNSUPPORTED (also when the caches cannot be described to the
- * tensor-memory-access unit), PKV_ERR_CUDA.
+ * tensor-memory-access unit, or when num_seqs * num_kv_heads * query tiles
+ * exceeds 2^31 - 1), PKV_ERR_CUDA.
  * ---------------------------------------------------------------------- */
 pkv_status_t pkv_paged_attn_prefill(
     void* out, const void* q, const int32_t* query_start, int max_query_len,

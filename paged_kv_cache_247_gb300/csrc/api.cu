@@ -390,9 +390,9 @@ pkv_status_t pkv_paged_attn_prefill(void* out, const void* q, const int32_t* que
   a.dtype = dtype;
   cudaError_t err = status_word(&a.status);
   if (err != cudaSuccess) return cuda_fail(err);
-  bool map_failed = false;
-  err = pkv::launch_paged_prefill(a, reinterpret_cast<cudaStream_t>(stream), &map_failed);
-  if (map_failed) return PKV_ERR_UNSUPPORTED;
+  bool unsupported = false;
+  err = pkv::launch_paged_prefill(a, reinterpret_cast<cudaStream_t>(stream), &unsupported);
+  if (unsupported) return PKV_ERR_UNSUPPORTED;
   if (err != cudaSuccess) return cuda_fail(err);
   return PKV_OK;
 }

@@ -78,8 +78,9 @@ struct PrefillArgs {
   unsigned int* status;
 };
 
-// map_failed is set when the tensor maps of the caches cannot be encoded.
-cudaError_t launch_paged_prefill(const PrefillArgs& a, cudaStream_t stream, bool* map_failed);
+// unsupported is set when the tensor maps of the caches cannot be encoded or
+// the work needs more CTAs than a 1-D grid holds.
+cudaError_t launch_paged_prefill(const PrefillArgs& a, cudaStream_t stream, bool* unsupported);
 
 cudaError_t launch_kv_append(const void* k, const void* v, void* k_cache, void* v_cache,
                              const int64_t* slot_mapping, int num_tokens, int num_kv_heads,

@@ -100,6 +100,8 @@ struct PrefillParams {
   int block_size;
   int num_blocks;
   float qscale;     // scale * log2(e)
+  int num_seqs;
+  int q_tiles;      // CTAs per (sequence, KV head)
 };
 
 // ---- tcgen05 helpers ------------------------------------------------------
@@ -301,8 +303,14 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int kvh = blockIdx.y;
-  const int s = blockIdx.z;
+  // Work item -> (query tile, KV head, sequence).  Items are numbered so
+  // that the hardware starts the latest query tiles (the longest causal
+  // spans) of every (sequence, head) first and the shortest last, which
+  // keeps the final wave short.
+  const int pairs = p.num_kv_heads * p.num_seqs;
+  const int qt = p.q_tiles - 1 - (int)(blockIdx.x / pairs);
+  const int kvh = (int)(blockIdx.x % pairs) % p.num_kv_heads;
+  const int s = (int)(blockIdx.x % pairs) / p.num_kv_heads;
   const int G = p.group;
   const int Gp = p.group_pow2;
   const int qpt = kBM / Gp;  // queries per row tile
@@ -313,11 +321,11 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
   const long long cap_ll = min((long long)p.max_context_len,
                                (long long)p.max_blocks_per_seq * p.block_size);
   if (ctx < nq || ctx > cap_ll) {
-    if (threadIdx.x == 0 && blockIdx.x == 0) atomicOr(p.status, PKV_DEV_BAD_CONTEXT_LEN);
+    if (threadIdx.x == 0 && qt == 0) atomicOr(p.status, PKV_DEV_BAD_CONTEXT_LEN);
     if (ctx < nq || nq <= 0) return;  // nothing sensible to attend to
     ctx = (int)cap_ll;
   }
-  const int j0 = blockIdx.x * kRowTiles * qpt;  // first query of the CTA
+  const int j0 = qt * kRowTiles * qpt;  // first query of the CTA
   if (j0 >= nq) return;                         // no queries here
   // Key tiles each row tile needs (up to its last query's position); row
   // tile 1 ends later, or is empty.
@@ -727,20 +735,20 @@ cudaError_t launch_prefill_typed(const PrefillParams& p, const CUtensorMap& km,
     if (err != cudaSuccess) return err;
     if (dev < 64) __atomic_fetch_or(&configured, 1ull << dev, __ATOMIC_RELEASE);
   }
-  const dim3 grid(q_tiles, p.num_kv_heads, num_seqs);
+  const dim3 grid((unsigned)((long long)q_tiles * p.num_kv_heads * num_seqs));
   paged_prefill_kernel<T, D><<<grid, kPrefillThreads, L::kBytes, stream>>>(p, km, vm);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_paged_prefill(const PrefillArgs& a, cudaStream_t stream, bool* map_failed) {
-  *map_failed = false;
+cudaError_t launch_paged_prefill(const PrefillArgs& a, cudaStream_t stream, bool* unsupported) {
+  *unsupported = false;
   CUtensorMap km, vm;
   const long long rows = (long long)a.num_blocks * a.num_kv_heads * a.block_size;
   if (!make_cache_map(&km, a.k_cache, a.dtype, rows, a.head_dim, a.block_size) ||
       !make_cache_map(&vm, a.v_cache, a.dtype, rows, a.head_dim, a.block_size)) {
-    *map_failed = true;
+    *unsupported = true;
     return cudaErrorInvalidValue;
   }
   int gp = 1;
@@ -763,6 +771,12 @@ cudaError_t launch_paged_prefill(const PrefillArgs& a, cudaStream_t stream, bool
   p.qscale = a.scale * 1.4426950408889634f;
   const int rows_q = kRowTiles * (kBM / gp);  // queries per CTA
   const int q_tiles = (a.max_query_len + rows_q - 1) / rows_q;
+  if ((long long)q_tiles * a.num_kv_heads * a.num_seqs > 0x7fffffffLL) {
+    *unsupported = true;  // more work items than a 1-D grid holds: unsupported
+    return cudaErrorInvalidValue;
+  }
+  p.num_seqs = a.num_seqs;
+  p.q_tiles = q_tiles;
   if (a.dtype == PKV_F16) {
     return a.head_dim == 64
                ? launch_prefill_typed<__half, 64>(p, km, vm, q_tiles, a.num_seqs, stream)
