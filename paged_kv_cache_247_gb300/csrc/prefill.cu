@@ -23,10 +23,15 @@
 //            operand); clears V rows past the context first.
 //   warps 0-3, 4-7  softmax, one warpgroup per row tile and one thread per
 //            row: each writes its Q rows into shared memory, then per key
-//            tile reads its S row (tcgen05.ld), masks the diagonal, keeps the
-//            running max and sum in base 2 (lazy rescaling), writes P over S
-//            in tensor memory and rescales O when the max moved; at the end
-//            it normalises and stores its O row.
+//            tile reads its S row (tcgen05.ld) for the row max (diagonal
+//            masked), keeps the running max and sum in base 2 (lazy
+//            rescaling, O rescaled in place when the max moved), then
+//            re-reads S half a row at a time for the exponentials and writes
+//            each half of P over S in tensor memory, releasing it to P V at
+//            once; at the end it normalises and stores its O row.
+//
+// Work items (one per CTA) are (query tile, KV head, sequence), launched
+// latest query tile first: the longest causal spans start early.
 //
 // Tensor memory: row tile t has S/P in columns [128 t, 128 t + 128) and O
 // in [256 + D t, 256 + D (t + 1)).  While one row tile's softmax runs, the
