@@ -529,15 +529,18 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     const uint32_t tmem_s = tmem + t * kBN + lane_base;
     const uint32_t tmem_o = tmem + L::kColO + t * D + lane_base;
 
-    // This row of Q into shared memory, in the K-major operand layout.
+    // This row of Q into shared memory, in the K-major operand layout: all
+    // of the row's loads are issued before the first store, so the row costs
+    // one memory latency, not one per 16 bytes.
     {
       const uint4* src = reinterpret_cast<const uint4*>(static_cast<const T*>(p.q) + row_elem);
       unsigned char* dst = sQ + t * L::kQTile;
+      uint4 v[D / 8];
 #pragma unroll
-      for (int c = 0; c < D / 8; ++c) {
-        const uint4 v = row_valid ? src[c] : make_uint4(0, 0, 0, 0);
-        *reinterpret_cast<uint4*>(dst + tile_chunk_offset<D>(r, c)) = v;
-      }
+      for (int c = 0; c < D / 8; ++c) v[c] = row_valid ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+      for (int c = 0; c < D / 8; ++c)
+        *reinterpret_cast<uint4*>(dst + tile_chunk_offset<D>(r, c)) = v[c];
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       mbar_arrive(&q_full[t]);
     }
