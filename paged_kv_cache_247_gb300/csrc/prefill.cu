@@ -30,8 +30,10 @@
 //            each half of P over S in tensor memory, releasing it to P V at
 //            once; at the end it normalises and stores its O row.
 //
-// Work items (one per CTA) are (query tile, KV head, sequence), launched
-// latest query tile first: the longest causal spans start early.
+// Work items (one per CTA) are (query tile, KV head, sequence).  The (sequence,
+// KV head) pairs go in groups of about one wave of items, and within a group
+// the latest query tiles (the longest causal spans) start first: CTAs that
+// run together share K/V in L2, and the final wave holds short items.
 //
 // Tensor memory: row tile t has S/P in columns [128 t, 128 t + 128) and O
 // in [256 + D t, 256 + D (t + 1)).  While one row tile's softmax runs, the
@@ -42,6 +44,7 @@
 #include <cudaTypedefs.h>
 #include <math_constants.h>
 
+#include <algorithm>
 #include <type_traits>
 
 #include "common.cuh"
@@ -106,7 +109,8 @@ struct PrefillParams {
   int num_blocks;
   float qscale;     // scale * log2(e)
   int num_seqs;
-  int q_tiles;      // CTAs per (sequence, KV head)
+  int q_tiles;          // CTAs per (sequence, KV head)
+  int pairs_per_group;  // (sequence, KV head) pairs whose items are launched together
 };
 
 // ---- tcgen05 helpers ------------------------------------------------------
@@ -308,14 +312,20 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  // Work item -> (query tile, KV head, sequence).  Items are numbered so
-  // that the hardware starts the latest query tiles (the longest causal
-  // spans) of every (sequence, head) first and the shortest last, which
-  // keeps the final wave short.
+  // Work item -> (query tile, KV head, sequence).  The (sequence, head)
+  // pairs are taken in groups of about one wave of work items; within a
+  // group the hardware starts the latest query tiles (the longest causal
+  // spans) first and the shortest last.  CTAs running together then share
+  // a few pairs' K/V in L2, and the final wave holds short items.
   const int pairs = p.num_kv_heads * p.num_seqs;
-  const int qt = p.q_tiles - 1 - (int)(blockIdx.x / pairs);
-  const int kvh = (int)(blockIdx.x % pairs) % p.num_kv_heads;
-  const int s = (int)(blockIdx.x % pairs) / p.num_kv_heads;
+  const int per_group = p.pairs_per_group * p.q_tiles;
+  const int grp = (int)(blockIdx.x / per_group);
+  const int gsize = min(p.pairs_per_group, pairs - grp * p.pairs_per_group);
+  const int rem = (int)(blockIdx.x - (unsigned)(grp * per_group));
+  const int qt = p.q_tiles - 1 - rem / gsize;
+  const int pair = grp * p.pairs_per_group + rem % gsize;
+  const int kvh = pair % p.num_kv_heads;
+  const int s = pair / p.num_kv_heads;
   const int G = p.group;
   const int Gp = p.group_pow2;
   const int qpt = kBM / Gp;  // queries per row tile
@@ -785,6 +795,10 @@ cudaError_t launch_paged_prefill(const PrefillArgs& a, cudaStream_t stream, bool
   }
   p.num_seqs = a.num_seqs;
   p.q_tiles = q_tiles;
+  // About one wave of CTAs per group (152 SMs on GB300; the exact count only
+  // shapes the order, not the result).
+  const int pairs = a.num_kv_heads * a.num_seqs;
+  p.pairs_per_group = std::max(1, std::min(pairs, 152 / std::max(1, q_tiles)));
   if (a.dtype == PKV_F16) {
     return a.head_dim == 64
                ? launch_prefill_typed<__half, 64>(p, km, vm, q_tiles, a.num_seqs, stream)
