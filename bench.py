@@ -47,7 +47,7 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=5000)
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="opt13b", choices=["opt13b", "gqa4k", "prefill"])
+    ap.add_argument("--workload", default="opt13b", choices=["opt13b", "gqa4k", "prefill", "sweep"])
     ap.add_argument("--partition", type=int, default=0, help="tokens per partition (0 = library)")
     ap.add_argument("--path", default="fused", choices=["fused", "separate"],
                     help="one fused append+decode launch, or kv_append then decode")
@@ -674,6 +674,79 @@ def run_prefill(args, rank, world, local_rank):
         print(json.dumps(line), flush=True)
 
 
+def run_sweep(args, rank, world, local_rank):
+    """Decode over the block-size / batch / context grid: each call timed
+    alone with CUDA events after reading 256 MiB (small cases fit in L2),
+    algorithmic bytes / time against the HBM peak."""
+    import paged_kv_cache_247_gb300 as pkv
+    from paged_kv_cache_247_gb300 import build as _build
+    from paged_kv_cache_247_gb300 import workloads as W
+    if rank == 0 or not os.path.exists(_build.LIB):
+        _build.build_library()
+    if world > 1:
+        torch.distributed.barrier()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    peak, peak_kind = peak_hbm()
+    flush = torch.ones(32 << 20, dtype=torch.float64, device=dev)
+    sw = W.SWEEP
+    rows = []
+    clocks = ClockSampler(dev.index if dev.index is not None else 0)
+    clocks.start()
+    for B in sw["block_sizes"]:
+        for S in sw["batches"]:
+            for ctx in sw["ctxs"]:
+                case = W.sweep_decode(B, S, ctx, device=dev)
+                Sq, Hq, D = case.q.shape
+                Hkv = case.k_cache.shape[1]
+                part = pkv.decode_partition_size(Sq, Hq, Hkv, D, case.max_context_len)
+                ws = torch.empty(max(16, pkv.decode_workspace_size(Sq, Hq, Hkv, D,
+                                                                   case.max_context_len, part)),
+                                 dtype=torch.uint8, device=dev)
+                out = torch.empty_like(case.q)
+
+                def call():
+                    pkv.paged_attn_decode(out, case.q, case.k_cache, case.v_cache,
+                                          case.block_tables, case.context_lens, case.scale,
+                                          case.max_context_len, partition_size=part, workspace=ws)
+                for _ in range(max(3, args.warmup)):
+                    call()
+                total = 0.0
+                iters = max(5, min(args.steps, 30))
+                for _ in range(iters):
+                    flush.sum()
+                    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    a.record(stream)
+                    call()
+                    b.record(stream)
+                    torch.cuda.synchronize()
+                    total += a.elapsed_time(b)
+                ms = total / iters
+                nbytes = step_bytes(case)[0]
+                gbs = nbytes / (ms * 1e-3) / 1e9
+                rows.append({"block_size": B, "num_seqs": S, "ctx": ctx, "partition": part,
+                             "kv_bytes": int(nbytes), "ms": round(ms, 5), "GB/s": round(gbs, 1),
+                             "frac": round(gbs / peak, 4)})
+                del case, ws, out
+                torch.cuda.empty_cache()
+    clock_rec = clocks.stop()
+    if pkv.device_status(clear=True) != 0:
+        raise RuntimeError("device status flags during the sweep")
+    ref = next(r for r in rows if r["block_size"] == 16 and r["num_seqs"] == 64 and r["ctx"] == 8192)
+    if rank == 0:
+        print(json.dumps({
+            "metric": "paged decode attention HBM GB/s across block sizes, batches and contexts",
+            "value": ref["GB/s"], "unit": "GB/s", "n_gpus": world, "steps": iters,
+            "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": "decode sweep: 32q/8kv, D=128, bf16; value at B=16, 64 seqs, "
+                                   "ctx 8192", "l2": "flushed (256 MiB read) before every call"},
+            "roofline": {"bound": "hbm", "achieved": ref["GB/s"], "peak": peak, "unit": "GB/s",
+                         "frac": ref["frac"], "peak_kind": peak_kind, "traffic": None},
+            "sweep": rows, "clocks": clock_rec}), flush=True)
+
+
 def main():
     args = parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -689,6 +762,13 @@ def main():
                                       "the reference arm is timed on the decode workloads"}))
             else:
                 run_prefill(args, rank, world, local_rank)
+        elif args.workload == "sweep":
+            if args.impl == "reference":
+                if rank == 0:
+                    print(json.dumps({"impl": "reference", "unavailable":
+                                      "the reference arm is timed on the decode workloads"}))
+            else:
+                run_sweep(args, rank, world, local_rank)
         elif args.impl == "reference":
             run_reference(args, rank, world)
         else:
