@@ -109,3 +109,34 @@ def test_prefill_full_size_sampled(cuda_device):
         ref = oracle.paged_decode_attention(to_f64(q[row:row + 1]), k_sub, v_sub,
                                             np.arange(nb)[None, :], np.array([p + 1]), case.scale)
         assert_within_tol(out[row:row + 1], ref, torch.bfloat16, f"prefill seq {s} query {j}")
+
+
+def test_prefill_empty_chunks_and_bad_context(cuda_device):
+    """Sequences without queries leave nothing to do; a context shorter than
+    its chunk is flagged (PKV_DEV_BAD_CONTEXT_LEN = 2) and skipped, while the
+    other sequences are still computed exactly."""
+    lens = [40, 300, 0, 129]
+    case = W.make_decode_case(21, len(lens), 8, 2, 128, 16, "bf16", lens, pool_factor=1.2,
+                              poison=True, device=cuda_device)
+    chunks = [0, 33, 0, 129]
+    q, out, ref, qs = _run(case, chunks, seed=4)
+    assert_within_tol(out, ref, torch.bfloat16, "prefill with empty chunks")
+    assert pkv.device_status(clear=True) == 0
+    # sequence 0 now claims 41 queries against a 40-token context
+    chunks = [41, 33, 0, 129]
+    qs2 = np.concatenate([[0], np.cumsum(chunks)]).astype(np.int32)
+    gen = torch.Generator(device=cuda_device).manual_seed(9)
+    q2 = torch.randn((int(qs2[-1]), 8, 128), generator=gen, device=cuda_device).to(torch.bfloat16)
+    out2 = torch.full_like(q2, float("nan"))
+    pkv.paged_attn_prefill(out2, q2, torch.from_numpy(qs2).to(cuda_device), case.k_cache,
+                           case.v_cache, case.block_tables, case.context_lens, case.scale,
+                           case.max_context_len, 129)
+    assert pkv.device_status(clear=True) == 2
+    assert torch.isnan(out2[:41]).all()  # the bad sequence is not written
+    ok_lens = case.context_lens.cpu().numpy().copy()
+    ok_lens[0] = 41
+    ref2 = oracle.paged_prefill_attention(to_f64(q2[41:]), to_f64(case.k_cache),
+                                          to_f64(case.v_cache),
+                                          case.block_tables.cpu().numpy()[1:], ok_lens[1:],
+                                          qs2[1:] - 41, case.scale)
+    assert_within_tol(out2[41:], ref2, torch.bfloat16, "prefill next to a bad sequence")
