@@ -90,6 +90,15 @@ def ncu_traffic(kernel_key, workload, sources=("decode.cu", "common.cuh")):
     return rec.get("dram_bytes_per_launch")
 
 
+def max_over_ranks(ms, world):
+    """The slowest rank's time: every rank returns the same value (gloo or
+    NCCL all-reduce MAX; a no-op on one rank)."""
+    t = torch.tensor([float(ms)], dtype=torch.float64)
+    if world > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
 class ClockSampler:
     """nvidia-smi sampling every 100 ms in the background."""
 
@@ -434,10 +443,7 @@ def run_ours(args, rank, world, local_rank):
     if flags:
         raise RuntimeError(f"device status flags {flags} during the bench")
 
-    t = torch.tensor([elapsed_ms], dtype=torch.float64)
-    if world > 1:
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-    elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(elapsed_ms, world)
 
     # The other path, briefly, for comparison (not the headline).
     other = "separate" if args.path == "fused" else "fused"
@@ -608,10 +614,7 @@ def run_prefill(args, rank, world, local_rank):
     if pkv.device_status(clear=True):
         raise RuntimeError("device status flags during the prefill bench")
     ms = a.elapsed_time(b) / K
-    t = torch.tensor([ms], dtype=torch.float64)
-    if world > 1:
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-    ms = float(t.item())
+    ms = max_over_ranks(ms, world)
     lens = case.context_lens.cpu().tolist()
     flops = prefill_flops(lens, [w["chunk"]] * S, Hq, D)
     tflops = flops / (ms * 1e-3) / 1e12
