@@ -70,7 +70,7 @@ typedef enum { PKV_F16 = 0, PKV_BF16 = 1 } pkv_dtype_t;
 #define PKV_DEV_BAD_BLOCK_ID 1u     /* a table entry or copy pair outside [0, num_blocks) */
 #define PKV_DEV_BAD_CONTEXT_LEN 2u  /* context_lens[s] < 0 or > max_context_len or > table row */
 #define PKV_DEV_BAD_SLOT 4u         /* slot_mapping[t] >= num_blocks * block_size */
-#define PKV_DEV_WAIT_TIMEOUT 8u     /* a wait on an in-flight copy gave up (never expected) */
+#define PKV_DEV_WAIT_TIMEOUT 8u     /* a bounded wait inside a kernel gave up (never expected) */
 
 /* Human-readable name of a status code (static string). */
 const char* pkv_status_string(pkv_status_t status);
@@ -319,6 +319,20 @@ pkv_status_t pkv_block_copy(
  * Synchronises `stream` first so that flags from work already enqueued on it
  * are visible.  flags may be NULL when only clearing. */
 pkv_status_t pkv_device_status(uint32_t* flags, int clear, pkv_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Diagnostic for the kernels' bounded waits.
+ *
+ * Every wait inside the decode and prefill kernels (on the CTA's own copies,
+ * MMA completions and warps) gives up after a limit (2 s), raises
+ * PKV_DEV_WAIT_TIMEOUT in the device status word and lets the kernel end,
+ * so that a wait that cannot complete never hangs the GPU.  This call
+ * enqueues one such wait on a barrier that nothing completes: it returns
+ * PKV_OK at once, the kernel ends after the limit, and pkv_device_status()
+ * then reports PKV_DEV_WAIT_TIMEOUT.  The context stays usable.  Not part of
+ * the hot path.
+ * ---------------------------------------------------------------------- */
+pkv_status_t pkv_debug_wait_timeout(pkv_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * Host-side refcounted block allocator (not on the device path).

@@ -24,7 +24,9 @@ from .ops import (  # noqa: F401
     contiguous_attn_decode,
     kv_append,
     block_copy,
+    check_copy_pairs,
     device_status,
+    debug_wait_timeout,
     decode_workspace_size,
     decode_partition_size,
 )

@@ -60,6 +60,7 @@ SIGNATURES = {
                               c_int, c_int, c_int, c_int, c_void_p]),
     "pkv_block_copy": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_int, c_size_t, c_void_p]),
     "pkv_device_status": (c_int, [P_u32, c_int, c_void_p]),
+    "pkv_debug_wait_timeout": (c_int, [c_void_p]),
     "pkv_alloc_create": (c_int, [c_int, c_int, ctypes.POINTER(c_void_p)]),
     "pkv_alloc_destroy": (None, [c_void_p]),
     "pkv_alloc_add_seq": (c_int, [c_void_p, c_int64, c_int]),

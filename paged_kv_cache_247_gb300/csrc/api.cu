@@ -461,6 +461,15 @@ pkv_status_t pkv_device_status(uint32_t* flags, int clear, pkv_stream_t stream) 
   return PKV_OK;
 }
 
+pkv_status_t pkv_debug_wait_timeout(pkv_stream_t stream) {
+  unsigned int* status = nullptr;
+  cudaError_t err = status_word(&status);
+  if (err != cudaSuccess) return cuda_fail(err);
+  err = pkv::launch_wait_probe(status, reinterpret_cast<cudaStream_t>(stream));
+  if (err != cudaSuccess) return cuda_fail(err);
+  return PKV_OK;
+}
+
 }  // extern "C"
 
 // ---------------------------------------------------------------------------

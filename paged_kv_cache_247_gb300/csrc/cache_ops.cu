@@ -121,7 +121,26 @@ __global__ void __launch_bounds__(kCopyThreads)
   }
 }
 
+// Diagnostic: thread 0 waits on an mbarrier that nothing arrives on, with
+// the same bounded wait the decode and prefill pipelines use.  The wait
+// gives up after the limit, raises PKV_DEV_WAIT_TIMEOUT and returns, so the
+// kernel ends and the context stays usable.
+__global__ void wait_probe_kernel(unsigned int* status) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) (void)mbar_wait(&bar, 0, status);
+}
+
 }  // namespace
+
+cudaError_t launch_wait_probe(unsigned int* status, cudaStream_t stream) {
+  wait_probe_kernel<<<1, 32, 0, stream>>>(status);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_kv_append(const void* k, const void* v, void* k_cache, void* v_cache,
                              const int64_t* slot_mapping, int num_tokens, int num_kv_heads,

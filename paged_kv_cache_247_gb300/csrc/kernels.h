@@ -91,4 +91,8 @@ cudaError_t launch_block_copy(void* k_cache, void* v_cache, const int64_t* pairs
                               int num_pairs, int num_blocks, size_t block_bytes,
                               unsigned int* status, cudaStream_t stream);
 
+// Diagnostic: one bounded wait on an mbarrier that nothing completes; it
+// gives up after the wait limit and raises PKV_DEV_WAIT_TIMEOUT.
+cudaError_t launch_wait_probe(unsigned int* status, cudaStream_t stream);
+
 }  // namespace pkv

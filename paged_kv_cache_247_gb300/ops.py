@@ -7,6 +7,7 @@ happens in the library's kernels; nothing here computes a result.
 
 import ctypes
 
+import numpy as np
 import torch
 
 from . import _lib
@@ -212,9 +213,24 @@ def kv_append(k, v, k_cache, v_cache, slot_mapping):
     _lib.check(st, "pkv_kv_append")
 
 
-def block_copy(k_cache, v_cache, src_dst_pairs):
+def check_copy_pairs(pairs, num_blocks):
+    """Raise ValueError unless ``pairs`` ([P, 2] ids, host data) is a valid
+    block_copy batch: ids in [0, num_blocks), destinations distinct, and no
+    destination also a source (the pairs are copied in parallel)."""
+    pairs = np.asarray(pairs, dtype=np.int64).reshape(-1, 2)
+    if pairs.size and (pairs.min() < 0 or pairs.max() >= num_blocks):
+        raise ValueError("block id outside [0, num_blocks)")
+    dst = pairs[:, 1]
+    if len(np.unique(dst)) != len(dst):
+        raise ValueError("destinations must be distinct")
+    if np.intersect1d(dst, pairs[:, 0]).size:
+        raise ValueError("a destination is also a source")
+
+
+def block_copy(k_cache, v_cache, src_dst_pairs, validate=False):
     """Copy whole physical blocks ``src -> dst`` (int64 [P, 2] CUDA tensor) in
-    both caches."""
+    both caches.  ``validate=True`` reads the pairs back to the host and
+    checks them first (see check_copy_pairs; this synchronises)."""
     _cuda(k_cache, "k_cache", ndim=4)
     _cuda(v_cache, "v_cache", k_cache.dtype, 4)
     _cuda(src_dst_pairs, "src_dst_pairs", torch.int64)
@@ -223,11 +239,21 @@ def block_copy(k_cache, v_cache, src_dst_pairs):
     if src_dst_pairs.dim() != 2 or src_dst_pairs.shape[1] != 2:
         raise ValueError("src_dst_pairs must be [P, 2]")
     NB = k_cache.shape[0]
+    if validate:
+        check_copy_pairs(src_dst_pairs.cpu().numpy(), NB)
     block_bytes = k_cache[0].numel() * k_cache.element_size()
     st = _lib.load().pkv_block_copy(
         k_cache.data_ptr(), v_cache.data_ptr(), src_dst_pairs.data_ptr(),
         src_dst_pairs.shape[0], NB, block_bytes, _stream_handle(k_cache.device))
     _lib.check(st, "pkv_block_copy")
+
+
+def debug_wait_timeout(device=None):
+    """Enqueue one kernel whose bounded wait cannot complete: after the wait
+    limit (2 s) it raises PKV_DEV_WAIT_TIMEOUT and ends (a check of the
+    kernels' timeout path; the context stays usable)."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    _lib.check(_lib.load().pkv_debug_wait_timeout(_stream_handle(dev)), "pkv_debug_wait_timeout")
 
 
 def device_status(clear=False, device=None):

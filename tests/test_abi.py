@@ -6,6 +6,7 @@ import ctypes
 import os
 import re
 
+import numpy as np
 import pytest
 
 from paged_kv_cache_247_gb300 import _lib as L
@@ -138,3 +139,14 @@ def _prefill(lib, **over):
 ])
 def test_prefill_host_validation(lib, over, expect):
     assert _prefill(lib, **over) == expect
+
+
+def test_copy_pair_validation():
+    from paged_kv_cache_247_gb300.ops import check_copy_pairs
+    check_copy_pairs([[0, 5], [1, 6], [2, 7]], 8)
+    check_copy_pairs(np.zeros((0, 2), dtype=np.int64), 8)
+    for bad in ([[0, 5], [1, 5]],        # destination twice
+                [[0, 5], [5, 6]],        # 5 is a destination and a source
+                [[0, 8]], [[-1, 3]]):    # ids outside the pool
+        with pytest.raises(ValueError):
+            check_copy_pairs(bad, 8)
