@@ -390,6 +390,7 @@ pkv_status_t pkv_paged_attn_prefill(void* out, const void* q, const int32_t* que
   a.dtype = dtype;
   cudaError_t err = status_word(&a.status);
   if (err != cudaSuccess) return cuda_fail(err);
+  a.sm_count = sm_count() > 0 ? sm_count() : kAssumedSms;
   bool unsupported = false;
   err = pkv::launch_paged_prefill(a, reinterpret_cast<cudaStream_t>(stream), &unsupported);
   if (unsupported) return PKV_ERR_UNSUPPORTED;

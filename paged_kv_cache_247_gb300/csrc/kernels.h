@@ -76,6 +76,7 @@ struct PrefillArgs {
   float scale;
   int dtype;
   unsigned int* status;
+  int sm_count;  // SMs of the device (sizes the launch order's groups)
 };
 
 // unsupported is set when the tensor maps of the caches cannot be encoded or

@@ -795,10 +795,10 @@ cudaError_t launch_paged_prefill(const PrefillArgs& a, cudaStream_t stream, bool
   }
   p.num_seqs = a.num_seqs;
   p.q_tiles = q_tiles;
-  // About one wave of CTAs per group (152 SMs on GB300; the exact count only
-  // shapes the order, not the result).
+  // About one wave of CTAs (one per SM) per group; the count only shapes
+  // the order, not the result.
   const int pairs = a.num_kv_heads * a.num_seqs;
-  p.pairs_per_group = std::max(1, std::min(pairs, 152 / std::max(1, q_tiles)));
+  p.pairs_per_group = std::max(1, std::min(pairs, a.sm_count / std::max(1, q_tiles)));
   if (a.dtype == PKV_F16) {
     return a.head_dim == 64
                ? launch_prefill_typed<__half, 64>(p, km, vm, q_tiles, a.num_seqs, stream)
