@@ -47,7 +47,7 @@ def _run(case, chunks, seed):
 @pytest.mark.parametrize("dtype,hq,hkv,D,B", [
     ("bf16", 8, 8, 128, 16), ("fp16", 8, 8, 128, 16), ("bf16", 32, 8, 128, 16),
     ("fp16", 16, 2, 64, 8), ("bf16", 12, 4, 128, 128), ("bf16", 6, 2, 64, 32),
-    ("fp16", 4, 4, 64, 64)])
+    ("fp16", 4, 4, 64, 64), ("bf16", 32, 1, 128, 16), ("fp16", 24, 4, 64, 32)])
 def test_prefill_matches_oracle(cuda_device, dtype, hq, hkv, D, B):
     lens = [1, 17, 130, 300, 64, 257]
     chunks = [1, 17, 130, 45, 1, 200]   # whole prompt, partial chunks, single queries
