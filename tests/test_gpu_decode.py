@@ -41,7 +41,7 @@ def test_tiny_workload_every_output(cuda_device):
 
 @pytest.mark.parametrize("dtype", ["fp16", "bf16"])
 @pytest.mark.parametrize("head_dim", [64, 128])
-@pytest.mark.parametrize("hq,hkv", [(4, 4), (8, 4), (12, 4), (8, 2), (16, 2), (6, 2)])
+@pytest.mark.parametrize("hq,hkv", [(4, 4), (8, 4), (12, 4), (8, 2), (16, 2), (6, 2), (32, 1)])
 def test_shapes_and_groups(cuda_device, dtype, head_dim, hq, hkv):
     lens = [1, 2, 15, 16, 17, 31, 32, 33, 63, 64, 65, 100, 127, 129, 250, 511, 700]
     case = W.make_decode_case(hq * 31 + hkv + head_dim, len(lens), hq, hkv, head_dim, 16, dtype,
