@@ -47,7 +47,7 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=5000)
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="opt13b", choices=["opt13b", "gqa4k", "prefill", "sweep"])
+    ap.add_argument("--workload", default="opt13b", choices=["opt13b", "gqa4k", "prefill", "sweep", "shared"])
     ap.add_argument("--partition", type=int, default=0, help="tokens per partition (0 = library)")
     ap.add_argument("--path", default="fused", choices=["fused", "separate"],
                     help="one fused append+decode launch, or kv_append then decode")
@@ -688,6 +688,165 @@ def run_prefill(args, rank, world, local_rank):
         print(json.dumps(line), flush=True)
 
 
+def run_shared(args, rank, world, local_rank):
+    """Parallel sampling with shared prompts (16 prompts x 8 samples): each
+    timed step is the whole serving step - the native allocator's next slots
+    and copy-on-write pairs and the block tables on the host, one staged copy
+    of the step's inputs to the device, the copies (if any) and the fused
+    append + decode launch, and the output read back.  Logical bytes are the
+    K/V every sample attends over; held bytes are the blocks the pool holds."""
+    import paged_kv_cache_247_gb300 as pkv
+    from paged_kv_cache_247_gb300 import build as _build
+    from paged_kv_cache_247_gb300 import workloads as W
+    if rank == 0 or not os.path.exists(_build.LIB):
+        _build.build_library()
+    if world > 1:
+        torch.distributed.barrier()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    w = W.SHARED_PREFIX
+    H, D, B, n = w["num_kv_heads"], w["head_dim"], w["block_size"], w["samples"]
+    dt = W.DTYPES[w["dtype"]]
+    e = torch.tensor([], dtype=dt).element_size()
+    prompts = W.shared_prefix_prompts()
+    S = len(prompts) * n
+    warm, K = max(3, args.warmup), args.steps
+    total_steps = warm + K
+    seq_ids = np.arange(S, dtype=np.int64)
+    nb = int(sum(-(-int(p) // B) for p in prompts) + S * (-(-total_steps // B) + 2))
+    kc = torch.zeros((nb, H, B, D), dtype=dt, device=dev)
+    vc = torch.zeros_like(kc)
+    alloc = pkv.BlockAllocator(nb, B)
+    for i, plen in enumerate(prompts.tolist()):
+        pk, pv = W.new_tokens(1000 + i, plen, H, D, w["dtype"], device=dev)
+        alloc.add_seq(i * n, plen)
+        pkv.kv_append(pk, pv, kc, vc, torch.from_numpy(alloc.seq_slots(i * n, 0, plen)).to(dev))
+        for j in range(1, n):
+            alloc.fork(i * n, i * n + j)
+    lens = prompts.repeat(n).astype(np.int64)
+    max_blocks = -(-int(lens.max() + total_steps) // B)
+    gen = torch.Generator(device="cpu").manual_seed(17)
+    q_h = torch.randn((S, H, D), generator=gen).to(dt)
+    k_h = torch.randn((S, H, D), generator=gen).to(dt)
+    v_h = torch.randn((S, H, D), generator=gen).to(dt)
+    # two pinned staging buffers (a step writes one while the other's copy
+    # may still run), each: q, k_new, v_new, tables, lengths, 256-byte aligned
+    parts = [("q", q_h.numel() * e), ("k", k_h.numel() * e), ("v", v_h.numel() * e),
+             ("tables", S * max_blocks * 4), ("lens", S * 4)]
+    offs, total = {}, 0
+    for name, nbytes in parts:
+        offs[name] = total
+        total += -(-nbytes // 256) * 256
+    stage_h = [torch.zeros(total, dtype=torch.uint8).pin_memory() for _ in range(2)]
+    stage_d = [torch.empty(total, dtype=torch.uint8, device=dev) for _ in range(2)]
+    done = [torch.cuda.Event(), torch.cuda.Event()]
+
+    def views(buf, name, dtype, shape):
+        nbytes = int(np.prod(shape)) * torch.tensor([], dtype=dtype).element_size()
+        return buf[offs[name]:offs[name] + nbytes].view(dtype).view(shape)
+
+    for b in range(2):
+        views(stage_h[b], "q", dt, q_h.shape).copy_(q_h)
+        views(stage_h[b], "k", dt, k_h.shape).copy_(k_h)
+        views(stage_h[b], "v", dt, v_h.shape).copy_(v_h)
+    out = torch.empty((S, H, D), dtype=dt, device=dev)
+    out_h = torch.empty((S, H, D), dtype=dt).pin_memory()
+    ws = torch.empty(max(16, pkv.decode_workspace_size(S, H, H, D, int(lens.max()) + total_steps + 1, 0)),
+                     dtype=torch.uint8, device=dev)
+    pairs_d = torch.empty((S, 2), dtype=torch.int64, device=dev)
+    stats = {"alloc_s": 0.0, "copies": 0, "logical_bytes": 0}
+    gpu_ev = []  # (start, end) of each timed step's device work
+    krn_ev = []  # (start, end) of each timed step's copies and fused launch
+
+    def step(i, ev=None):
+        b = i & 1
+        done[b].synchronize()  # the copy that last read this staging buffer has ended
+        t0 = time.perf_counter()
+        _, pairs = alloc.append_slots(seq_ids)
+        lens[:] += 1
+        tables = alloc.block_table(seq_ids, max_blocks)
+        stats["alloc_s"] += time.perf_counter() - t0
+        views(stage_h[b], "tables", torch.int32, (S, max_blocks)).copy_(torch.from_numpy(tables))
+        views(stage_h[b], "lens", torch.int32, (S,)).copy_(torch.from_numpy(lens.astype(np.int32)))
+        if ev is not None:
+            ev[0].record(stream)
+        stage_d[b].copy_(stage_h[b], non_blocking=True)
+        done[b].record(stream)
+        if len(pairs):
+            pairs_d[:len(pairs)].copy_(torch.from_numpy(pairs), non_blocking=True)
+        if ev is not None:
+            ev[2].record(stream)
+        if len(pairs):
+            pkv.block_copy(kc, vc, pairs_d[:len(pairs)])
+            stats["copies"] += len(pairs)
+        pkv.paged_attn_decode_append(
+            out, views(stage_d[b], "q", dt, q_h.shape), views(stage_d[b], "k", dt, k_h.shape),
+            views(stage_d[b], "v", dt, v_h.shape), kc, vc,
+            views(stage_d[b], "tables", torch.int32, (S, max_blocks)),
+            views(stage_d[b], "lens", torch.int32, (S,)), D ** -0.5, int(lens.max()), workspace=ws)
+        if ev is not None:
+            ev[3].record(stream)
+        out_h.copy_(out, non_blocking=True)
+        if ev is not None:
+            ev[1].record(stream)
+        stats["logical_bytes"] += int(lens.sum()) * 2 * H * D * e
+
+    pkv.device_status(clear=True)
+    t_cow = time.perf_counter()
+    step(0)  # the first divergent token: every sample of a partly filled prompt block copies
+    torch.cuda.synchronize()
+    t_cow = time.perf_counter() - t_cow
+    cow_pairs = stats["copies"]
+    for i in range(1, warm):
+        step(i)
+    torch.cuda.synchronize()
+    stats.update(alloc_s=0.0, copies=0, logical_bytes=0)
+    clocks = ClockSampler(dev.index if dev.index is not None else 0)
+    clocks.start()
+    time.sleep(0.3)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(warm, warm + K):
+        ev = tuple(torch.cuda.Event(enable_timing=True) for _ in range(4))
+        gpu_ev.append(ev)
+        step(i, ev)
+    torch.cuda.synchronize()
+    elapsed = max_over_ranks(time.perf_counter() - t0, world)
+    gpu_ms = float(np.mean([ev[0].elapsed_time(ev[1]) for ev in gpu_ev]))
+    krn_ms = float(np.mean([ev[2].elapsed_time(ev[3]) for ev in gpu_ev]))
+    clock_rec = clocks.stop()
+    if pkv.device_status(clear=True) != 0:
+        raise RuntimeError("device status flags during the shared-prefix bench")
+    st = alloc.stats()
+    held = st["used_blocks"] * B * 2 * H * D * e
+    logical_gbs = stats["logical_bytes"] / elapsed / 1e9
+    if rank == 0:
+        print(json.dumps({
+            "metric": "parallel-sampling serving step: logical K/V GB/s attended (whole step, "
+                      "allocator on the host included)",
+            "value": round(logical_gbs * world, 1), "unit": "GB/s", "n_gpus": world, "steps": K,
+            "warmup": warm, "ms_per_step": round(1e3 * elapsed / K, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": w["dtype"], "data": "synthetic",
+            "config": {"workload": f"{len(prompts)} prompts (U[{w['prompt_lo']},{w['prompt_hi']}]) "
+                                   f"x {n} samples, {H} heads, D={D}, B={B}", "num_seqs": S,
+                       "timing": "host wall clock over the steps, device synchronised at both ends"},
+            "steps_per_s": round(K / elapsed, 1),
+            "device_ms_per_step": round(gpu_ms, 4),
+            "logical_gbs_device": round(stats["logical_bytes"] / K / (gpu_ms * 1e-3) / 1e9, 1),
+            "kernel_ms_per_step": round(krn_ms, 4),
+            "logical_gbs_kernel": round(stats["logical_bytes"] / K / (krn_ms * 1e-3) / 1e9, 1),
+            "allocator_us_per_step": round(1e6 * stats["alloc_s"] / K, 2),
+            "first_step": {"cow_pairs": cow_pairs, "ms": round(1e3 * t_cow, 3)},
+            "pool": {k: st[k] for k in st},
+            "held_kv_bytes": held,
+            "logical_kv_bytes_per_step": int(stats["logical_bytes"] / K),
+            "clocks": clock_rec}), flush=True)
+    alloc.close()
+
+
 def run_sweep(args, rank, world, local_rank):
     """Decode over the block-size / batch / context grid: each call timed
     alone with CUDA events after reading 256 MiB (small cases fit in L2),
@@ -776,6 +935,13 @@ def main():
                                       "the reference arm is timed on the decode workloads"}))
             else:
                 run_prefill(args, rank, world, local_rank)
+        elif args.workload == "shared":
+            if args.impl == "reference":
+                if rank == 0:
+                    print(json.dumps({"impl": "reference", "unavailable":
+                                      "the reference arm is timed on the decode workloads"}))
+            else:
+                run_shared(args, rank, world, local_rank)
         elif args.workload == "sweep":
             if args.impl == "reference":
                 if rank == 0:
