@@ -88,7 +88,10 @@ def test_auto_partition_policy(lib):
     assert part(8, 32, 8, 128, 100) == 128          # short context: one partition
     assert part(64, 40, 40, 128, 2048) == 2048      # 2560 units: enough CTAs unsplit
     assert part(256, 32, 8, 128, 4096) == 2048      # long contexts: 2048-token partitions
-    assert part(8, 32, 8, 128, 32768) == 2048
+    assert part(8, 32, 8, 128, 32768) == 1280       # 64 units: ~four waves of CTAs
+    assert part(8, 32, 8, 128, 8192) == 512
+    assert part(16, 32, 8, 128, 16384) == 1280
+    assert part(128, 32, 8, 128, 2048) == 1024      # 1024 units: two partitions
     assert part(8, 32, 8, 128, 1024) == 256         # 64 units: split finer to fill the GPU
     assert part(64, 32, 8, 128, 1024) == 1024       # 512 units: not worth splitting 1k
     for args in [(1, 1, 1, 64, 5), (3, 12, 4, 64, 100000), (200, 64, 8, 128, 777)]:
