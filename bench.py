@@ -76,7 +76,7 @@ def source_hash(*names):
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(kernel_key, workload, sources=("decode.cu", "common.cuh")):
+def ncu_traffic(kernel_key, workload, sources=("decode.cu", "common.cuh", "overlap.cuh")):
     """DRAM bytes per launch from a committed ncu summary, if it was taken on
     the current kernel source (else None)."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
@@ -226,6 +226,24 @@ def contiguous_baseline(pkv, case, out, part, dev, stream, iters):
             "partition_size": part, "iters": iters}
 
 
+def time_alone(fn, flush, stream, iters):
+    """Mean device time of fn() in ms, each call timed alone: read `flush`
+    (larger than L2) to evict the call's data, then hold the stream in a
+    bounded device-side wait (about 0.1-0.15 ms) so the host has queued the
+    call before the start event fires and its launch cost stays out."""
+    total = 0.0
+    for _ in range(iters):
+        flush.sum()
+        torch.cuda._sleep(300_000)  # clock cycles
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        total += a.elapsed_time(b)
+    return total / iters
+
+
 def cache_ops_bench(pkv, case, dev, stream, peak, iters=30, fill_blocks=400, cow_pairs=112):
     """The two cache-maintenance kernels on their large instances, each call
     timed alone with CUDA events after reading a buffer larger than L2:
@@ -254,16 +272,7 @@ def cache_ops_bench(pkv, case, dev, stream, peak, iters=30, fill_blocks=400, cow
     def timed(fn):
         for _ in range(3):
             fn()
-        total = 0.0
-        for _ in range(iters):
-            flush.sum()
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            fn()
-            b.record(stream)
-            torch.cuda.synchronize()
-            total += a.elapsed_time(b)
-        return total / iters
+        return time_alone(fn, flush, stream, iters)
 
     pkv.device_status(clear=True)
     t_app = timed(lambda: pkv.kv_append(k_new, v_new, kc, vc, slots))
@@ -283,7 +292,8 @@ def cache_ops_bench(pkv, case, dev, stream, peak, iters=30, fill_blocks=400, cow
     return {"kv_append_prompt_fill": rec(t_app, b_app, f"{T} tokens x {Hkv} heads into {n_fill} "
                                          "random blocks"),
             "block_copy_cow_batch": rec(t_cow, b_cow, f"{n_cow} block pairs, K and V"),
-            "l2": "flushed (256 MiB read) before every timed call", "iters": iters}
+            "l2": "flushed (256 MiB read) before every timed call",
+            "launch": "queued behind a device-side wait, outside the timed region", "iters": iters}
 
 
 # ------------------------------------------------------------- CPU legs --
@@ -711,7 +721,9 @@ def run_shared(args, rank, world, local_rank):
     e = torch.tensor([], dtype=dt).element_size()
     prompts = W.shared_prefix_prompts()
     S = len(prompts) * n
-    warm, K = max(3, args.warmup), args.steps
+    # The workload is a fixed number of decode steps (contexts grow by one
+    # token a step): a few untimed steps, then the workload's steps timed.
+    warm, K = max(3, min(args.warmup, 10)), min(args.steps, w["steps"])
     total_steps = warm + K
     seq_ids = np.arange(S, dtype=np.int64)
     nb = int(sum(-(-int(p) // B) for p in prompts) + S * (-(-total_steps // B) + 2))
@@ -832,6 +844,8 @@ def run_shared(args, rank, world, local_rank):
             "scaling": "weak", "vs_baseline": None, "dtype": w["dtype"], "data": "synthetic",
             "config": {"workload": f"{len(prompts)} prompts (U[{w['prompt_lo']},{w['prompt_hi']}]) "
                                    f"x {n} samples, {H} heads, D={D}, B={B}", "num_seqs": S,
+                       "decode_steps": f"{warm} untimed, then {K} timed; every context grows "
+                                       "by one token a step",
                        "timing": "host wall clock over the steps, device synchronised at both ends"},
             "steps_per_s": round(K / elapsed, 1),
             "device_ms_per_step": round(gpu_ms, 4),
@@ -885,17 +899,8 @@ def run_sweep(args, rank, world, local_rank):
                                           case.max_context_len, partition_size=part, workspace=ws)
                 for _ in range(max(3, args.warmup)):
                     call()
-                total = 0.0
                 iters = max(5, min(args.steps, 30))
-                for _ in range(iters):
-                    flush.sum()
-                    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                    a.record(stream)
-                    call()
-                    b.record(stream)
-                    torch.cuda.synchronize()
-                    total += a.elapsed_time(b)
-                ms = total / iters
+                ms = time_alone(call, flush, stream, iters)
                 nbytes = step_bytes(case)[0]
                 gbs = nbytes / (ms * 1e-3) / 1e9
                 rows.append({"block_size": B, "num_seqs": S, "ctx": ctx, "partition": part,
@@ -914,7 +919,8 @@ def run_sweep(args, rank, world, local_rank):
             "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": "decode sweep: 32q/8kv, D=128, bf16; value at B=16, 64 seqs, "
-                                   "ctx 8192", "l2": "flushed (256 MiB read) before every call"},
+                                   "ctx 8192", "l2": "flushed (256 MiB read) before every call",
+                       "launch": "queued behind a device-side wait, outside the timed region"},
             "roofline": {"bound": "hbm", "achieved": ref["GB/s"], "peak": peak, "unit": "GB/s",
                          "frac": ref["frac"], "peak_kind": peak_kind, "traffic": None},
             "sweep": rows, "clocks": clock_rec}), flush=True)

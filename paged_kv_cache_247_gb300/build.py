@@ -21,7 +21,8 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libpagedkv.so")
 
 SOURCES = ["api.cu", "decode.cu", "prefill.cu", "cache_ops.cu", "allocator.cpp"]
-HEADERS = [os.path.join(CSRC, "common.cuh"), os.path.join(CSRC, "kernels.h"),
+HEADERS = [os.path.join(CSRC, "common.cuh"), os.path.join(CSRC, "overlap.cuh"),
+           os.path.join(CSRC, "kernels.h"),
            os.path.join(INCLUDE, "pagedkv.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xptxas", "-v",

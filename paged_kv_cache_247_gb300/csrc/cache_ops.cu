@@ -17,6 +17,7 @@
 // keeps several loads in flight before it stores.
 
 #include "common.cuh"
+#include "overlap.cuh"
 #include "kernels.h"
 
 namespace pkv {
@@ -42,6 +43,8 @@ __global__ void __launch_bounds__(kCopyThreads)
                      const int64_t* __restrict__ slot_mapping, int num_tokens, int row_chunks,
                      int log2_cpr, int num_kv_heads, int block_size, long long num_slots,
                      unsigned int* status) {
+  grid_dep_wait();
+  grid_dep_launch_dependents();
   const int cpr_mask = (1 << log2_cpr) - 1;
   for (int t = blockIdx.y; t < num_tokens; t += gridDim.y) {
     const long long slot = slot_mapping[t];
@@ -85,6 +88,8 @@ __global__ void __launch_bounds__(kCopyThreads)
     block_copy_kernel(uint4* k_cache, uint4* v_cache, const int64_t* __restrict__ pairs,
                       int num_pairs, long long chunks_per_block, int num_blocks,
                       unsigned int* status) {
+  grid_dep_wait();
+  grid_dep_launch_dependents();
   for (int i = blockIdx.y; i < num_pairs; i += gridDim.y) {
     const long long src = pairs[2 * i];
     const long long dst = pairs[2 * i + 1];
@@ -151,11 +156,11 @@ cudaError_t launch_kv_append(const void* k, const void* v, void* k_cache, void* 
   const int row_chunks = num_kv_heads * cpr;
   const int gx = (row_chunks + kCopyThreads * kUnroll - 1) / (kCopyThreads * kUnroll);
   const int gy = num_tokens < 65535 ? num_tokens : 65535;
-  kv_append_kernel<<<dim3(gx, gy), kCopyThreads, 0, stream>>>(
+  return launch_overlapped(
+      kv_append_kernel, dim3(gx, gy), dim3(kCopyThreads), 0, stream,
       static_cast<const uint4*>(k), static_cast<const uint4*>(v), static_cast<uint4*>(k_cache),
       static_cast<uint4*>(v_cache), slot_mapping, num_tokens, row_chunks, log2_cpr, num_kv_heads,
       block_size, (long long)num_blocks * block_size, status);
-  return cudaGetLastError();
 }
 
 cudaError_t launch_block_copy(void* k_cache, void* v_cache, const int64_t* pairs, int num_pairs,
@@ -165,10 +170,9 @@ cudaError_t launch_block_copy(void* k_cache, void* v_cache, const int64_t* pairs
   long long gx = (cpb + kCopyThreads * kCopyUnroll - 1) / (kCopyThreads * kCopyUnroll);
   if (gx > 65535) gx = 65535;
   const int gy = num_pairs < 65535 ? num_pairs : 65535;
-  block_copy_kernel<<<dim3((unsigned)gx, gy), kCopyThreads, 0, stream>>>(
-      static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), pairs, num_pairs, cpb,
-      num_blocks, status);
-  return cudaGetLastError();
+  return launch_overlapped(block_copy_kernel, dim3((unsigned)gx, gy), dim3(kCopyThreads), 0,
+                           stream, static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache),
+                           pairs, num_pairs, cpb, num_blocks, status);
 }
 
 }  // namespace pkv

@@ -34,6 +34,7 @@
 #include <math_constants.h>
 
 #include "common.cuh"
+#include "overlap.cuh"
 #include "kernels.h"
 
 namespace pkv {
@@ -143,6 +144,7 @@ __global__ void __launch_bounds__(SmemLayout<T, D, GT>::kThreads, LayoutFor<D, G
   const int h0 = kvh * p.group + hc * GT;
   const int nh = min(GT, p.group - hc * GT);
 
+  grid_dep_wait();
   int ctx = p.context_lens[s];
   const long long cap_ll = min((long long)p.max_context_len,
                                (long long)p.max_blocks_per_seq * p.block_size);
@@ -428,6 +430,10 @@ __global__ void __launch_bounds__(SmemLayout<T, D, GT>::kThreads, LayoutFor<D, G
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[stg]);
   }
+  // The next kernel on the stream may be placed now (it waits for this
+  // grid to finish); triggered this late, its CTAs are resident only during
+  // this grid's last epilogues rather than through its whole last wave.
+  grid_dep_launch_dependents();
 
   // The row groups of a warp share its running max: add their sums.
 #pragma unroll
@@ -507,6 +513,8 @@ __global__ void __launch_bounds__(128) paged_decode_reduce_kernel(const DecodePa
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int pair = blockIdx.x * 4 + warp;
+  grid_dep_wait();
+  grid_dep_launch_dependents();
   if (pair >= p.num_seqs * p.num_q_heads) return;
   const int s = pair / p.num_q_heads;
   int ctx = p.context_lens[s];
@@ -591,12 +599,12 @@ cudaError_t launch_typed(const DecodeParams& p, cudaStream_t stream) {
   cudaError_t err = configure<T, D, GT, kPaged>();
   if (err != cudaSuccess) return err;
   const dim3 grid(p.num_parts, p.num_kv_heads * p.head_chunks, p.num_seqs);
-  paged_decode_kernel<T, D, GT, kPaged><<<grid, L::kThreads, L::kBytes, stream>>>(p);
-  err = cudaGetLastError();
+  err = launch_overlapped(paged_decode_kernel<T, D, GT, kPaged>, grid, dim3(L::kThreads),
+                          L::kBytes, stream, p);
   if (err != cudaSuccess || p.num_parts <= 1) return err;
   const int pairs = p.num_seqs * p.num_q_heads;
-  paged_decode_reduce_kernel<T, D><<<(pairs + 3) / 4, 128, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_overlapped(paged_decode_reduce_kernel<T, D>, dim3((pairs + 3) / 4), dim3(128),
+                           0, stream, p);
 }
 
 template <typename T, int D, bool kPaged>
