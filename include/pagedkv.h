@@ -29,6 +29,13 @@
  *     NULL is the legacy default stream) and returns without synchronising.
  *     Argument checks happen on the host before anything is enqueued; a call
  *     that returns an error has enqueued nothing.
+ *   - Stream order is kept as for any kernel.  The decode, append and copy
+ *     kernels are launched with programmatic stream serialization: their
+ *     blocks may be placed on the GPU while the previous kernel on the stream
+ *     is still running, but each waits for that kernel to finish (and for its
+ *     writes to be visible) before it reads or writes memory.  A kernel the
+ *     caller launches after them without that attribute starts after they
+ *     finish, as usual.
  *   - Problems only visible on the device (a block id outside the pool, a
  *     context length beyond the table, a slot beyond the pool) never fault:
  *     the offending access is skipped or redirected to block 0, the result is
