@@ -246,6 +246,48 @@ def time_alone(fn, flush, stream, iters):
     return total / iters
 
 
+def pipelined_steps(stream, n_steps, copy_in, compute, copy_out):
+    """Mean ms per step of a double-buffered serving loop, on the device
+    clock.  copy_in(b) fills input buffer b on a copy stream, compute(b)
+    reads input b and writes output b on `stream`, copy_out(b) reads output
+    b back on a second copy stream.  Step i+1's inputs go in, and step i's
+    output comes out, while the compute stream moves on; each buffer is
+    reused only after the step that last touched it is done with it."""
+    dev = stream.device
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    in_ready = [torch.cuda.Event() for _ in range(2)]
+    done = [torch.cuda.Event() for _ in range(2)]
+    out_done = [torch.cuda.Event() for _ in range(2)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    s_in.wait_event(t0)
+    with torch.cuda.stream(s_in):
+        copy_in(0)
+    in_ready[0].record(s_in)
+    for i in range(n_steps):
+        b = i & 1
+        stream.wait_event(in_ready[b])
+        if i >= 2:
+            stream.wait_event(out_done[b])  # step i-2's output has been read back
+        with torch.cuda.stream(stream):
+            compute(b)
+        done[b].record(stream)
+        if i + 1 < n_steps:
+            if i >= 1:
+                s_in.wait_event(done[1 - b])  # step i-1 has read that input buffer
+            with torch.cuda.stream(s_in):
+                copy_in(1 - b)
+            in_ready[1 - b].record(s_in)
+        s_out.wait_event(done[b])
+        with torch.cuda.stream(s_out):
+            copy_out(b)
+        out_done[b].record(s_out)
+    stream.wait_event(out_done[(n_steps - 1) & 1])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    return t0.elapsed_time(t1) / n_steps
+
+
 def cache_ops_bench(pkv, case, dev, stream, peak, iters=30, fill_blocks=400, cow_pairs=112):
     """The two cache-maintenance kernels on their large instances, each call
     timed alone with CUDA events after reading a buffer larger than L2:
@@ -401,18 +443,19 @@ def run_ours(args, rank, world, local_rank):
     split = -(-case.max_context_len // part) > 1
     stream = torch.cuda.current_stream(dev)
 
-    def enqueue(path, qd, kd, vd, sd, td, ld, ev=None):
+    def enqueue(path, qd, kd, vd, sd, td, ld, ev=None, o=None):
         """One step on the stream: append the new token and attend."""
+        o = out if o is None else o
         if path == "separate":
             pkv.kv_append(kd, vd, case.k_cache, case.v_cache, sd)
         if ev is not None:
             ev[0].record(stream)
         if path == "separate":
-            pkv.paged_attn_decode(out, qd, case.k_cache, case.v_cache, td, ld, case.scale,
+            pkv.paged_attn_decode(o, qd, case.k_cache, case.v_cache, td, ld, case.scale,
                                   case.max_context_len, partition_size=args.partition,
                                   workspace=workspace)
         else:
-            pkv.paged_attn_decode_append(out, qd, kd, vd, case.k_cache, case.v_cache, td, ld,
+            pkv.paged_attn_decode_append(o, qd, kd, vd, case.k_cache, case.v_cache, td, ld,
                                          case.scale, case.max_context_len,
                                          partition_size=args.partition, workspace=workspace)
         if ev is not None:
@@ -472,44 +515,61 @@ def run_ours(args, rank, world, local_rank):
 
     # End to end through the C ABI with host buffers: every step copies its
     # inputs (q, new K/V, slots, tables, lengths) from pinned host memory and
-    # reads the output back.
-    # The step's inputs sit in one pinned staging buffer (each 256-byte
-    # aligned), so a step is one host-to-device copy, the launch(es), and
-    # one device-to-host copy of the output.
+    # reads the output back.  The step's inputs sit in one pinned staging
+    # buffer (each 256-byte aligned), so a step is one host-to-device copy,
+    # the launch(es), and one device-to-host copy of the output.  As a
+    # serving loop would, the copies run on streams of their own with two
+    # staging and two output buffers: step i+1's inputs are copied in and
+    # step i's output copied out while the next step computes.  The serial
+    # form (copy in, launch, copy out, one after another on one stream) is
+    # reported beside it.
     srcs = (("q", case.q), ("k", k_new), ("v", v_new), ("slots", slots),
             ("tables", case.block_tables), ("lens", case.context_lens))
+    names = [n for n, _ in srcs]
     offs, total = {}, 0
     for n, x in srcs:
         offs[n] = total
         total += -(-x.numel() * x.element_size() // 256) * 256
-    stage_host = torch.zeros(total, dtype=torch.uint8).pin_memory()
-    stage_dev = torch.empty(total, dtype=torch.uint8, device=dev)
-    dev_in = {}
-    for n, x in srcs:
-        nb = x.numel() * x.element_size()
-        stage_host[offs[n]:offs[n] + nb].copy_(x.cpu().contiguous().view(-1).view(torch.uint8))
-        dev_in[n] = stage_dev[offs[n]:offs[n] + nb].view(x.dtype).view(x.shape)
-    out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    stage_host = [torch.zeros(total, dtype=torch.uint8).pin_memory() for _ in range(2)]
+    stage_dev = [torch.empty(total, dtype=torch.uint8, device=dev) for _ in range(2)]
+    dev_in = [{}, {}]
+    for bb in range(2):
+        for n, x in srcs:
+            nb = x.numel() * x.element_size()
+            stage_host[bb][offs[n]:offs[n] + nb].copy_(x.cpu().contiguous().view(-1).view(torch.uint8))
+            dev_in[bb][n] = stage_dev[bb][offs[n]:offs[n] + nb].view(x.dtype).view(x.shape)
+    outs = [out, torch.empty_like(out)]
+    out_host = [torch.empty(out.shape, dtype=out.dtype).pin_memory() for _ in range(2)]
     h2d = sum(x.numel() * x.element_size() for _, x in srcs)
-    d2h = out_host.numel() * out_host.element_size()
+    d2h = out_host[0].numel() * out_host[0].element_size()
     K_e2e = max(10, K // 4)
 
-    def e2e_step():
-        stage_dev.copy_(stage_host, non_blocking=True)
-        enqueue(args.path, dev_in["q"], dev_in["k"], dev_in["v"], dev_in["slots"],
-                dev_in["tables"], dev_in["lens"])
-        out_host.copy_(out, non_blocking=True)
+    def e2e_serial_step():
+        stage_dev[0].copy_(stage_host[0], non_blocking=True)
+        enqueue(args.path, *[dev_in[0][n] for n in names])
+        out_host[0].copy_(out, non_blocking=True)
+
+    def e2e_pipelined(n_steps):
+        return pipelined_steps(
+            stream, n_steps,
+            lambda bb: stage_dev[bb].copy_(stage_host[bb], non_blocking=True),
+            lambda bb: enqueue(args.path, *[dev_in[bb][n] for n in names], o=outs[bb]),
+            lambda bb: out_host[bb].copy_(outs[bb], non_blocking=True))
 
     for _ in range(3):
-        e2e_step()
+        e2e_serial_step()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(K_e2e):
-        e2e_step()
+        e2e_serial_step()
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / K_e2e
+    e2e_serial_ms = e0.elapsed_time(e1) / K_e2e
+    e2e_pipelined(4)
+    e2e_ms = e2e_pipelined(K_e2e)
+    if not torch.equal(out_host[(K_e2e - 1) & 1], out.cpu()):
+        raise RuntimeError("pipelined end-to-end output differs from the device output")
 
     # Contiguous baseline: the same tokens with each sequence reserved at
     # max_context_len and no block table; the ratio of the two decode times
@@ -557,7 +617,12 @@ def run_ours(args, rank, world, local_rank):
                      "launches_timed": f"{len(decode_ms)} of {K} (every {ev_every}th step)"},
         "e2e": {"value": round((decode_b + append_b) * world / (e2e_ms * 1e-3) / 1e9, 2),
                 "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": round(e2e_ms, 5)},
+                "ms_per_step": round(e2e_ms, 5),
+                "copies": "own streams, double-buffered: the next step's inputs in and this "
+                          "step's output out while the next step computes",
+                "serial_ms_per_step": round(e2e_serial_ms, 5),
+                "serial_value": round((decode_b + append_b) * world / (e2e_serial_ms * 1e-3) / 1e9,
+                                      2)},
         "path": args.path,
         "other_path": alt,
         "contiguous_baseline": contig,
@@ -647,20 +712,29 @@ def run_prefill(args, rank, world, local_rank):
             peak, kind = float(json.load(f)["bf16_tflops"]), "measured (MEASURED_PEAKS.json bf16_tflops, burst)"
     except (OSError, KeyError, ValueError):
         peak, kind = 1900.0, "fallback"
-    # end to end: queries in from pinned host memory, output back, each step
+    # end to end: queries in from pinned host memory, output back, each step;
+    # the copies run double-buffered on streams of their own (the serial form
+    # is reported beside it)
     q_host = q.cpu().pin_memory()
-    out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    q_dev = torch.empty_like(q)
+    out_host = [torch.empty(out.shape, dtype=out.dtype).pin_memory() for _ in range(2)]
+    q_dev = [torch.empty_like(q) for _ in range(2)]
+    outs = [out, torch.empty_like(out)]
     n_e2e = max(5, K // 4)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(n_e2e):
-        q_dev.copy_(q_host, non_blocking=True)
-        call(q_dev, out)
-        out_host.copy_(out, non_blocking=True)
+        q_dev[0].copy_(q_host, non_blocking=True)
+        call(q_dev[0], out)
+        out_host[0].copy_(out, non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / n_e2e
+    e2e_serial_ms = e0.elapsed_time(e1) / n_e2e
+    e2e_ms = pipelined_steps(stream, n_e2e,
+                             lambda bb: q_dev[bb].copy_(q_host, non_blocking=True),
+                             lambda bb: call(q_dev[bb], outs[bb]),
+                             lambda bb: out_host[bb].copy_(outs[bb], non_blocking=True))
+    if not torch.equal(out_host[(n_e2e - 1) & 1], out.cpu()):
+        raise RuntimeError("pipelined end-to-end output differs from the device output")
     line = {
         "metric": "paged chunked-prefill attention TFLOP/s (causal, algorithmic)",
         "value": round(tflops * world, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": K,
@@ -676,7 +750,12 @@ def run_prefill(args, rank, world, local_rank):
                      "traffic": ncu_traffic("paged_prefill_kernel", "prefill",
                                             ("prefill.cu", "common.cuh")) if S == w["num_seqs"] else None},
         "e2e": {"value": round(flops / (e2e_ms * 1e-3) / 1e12 * world, 2), "unit": "TFLOP/s",
-                "h2d_bytes_per_step": q_host.numel() * 2, "d2h_bytes_per_step": out_host.numel() * 2},
+                "h2d_bytes_per_step": q_host.numel() * 2,
+                "d2h_bytes_per_step": out_host[0].numel() * 2, "ms_per_step": round(e2e_ms, 5),
+                "copies": "own streams, double-buffered: the next step's queries in and this "
+                          "step's output out while the next step computes",
+                "serial_ms_per_step": round(e2e_serial_ms, 5),
+                "serial_value": round(flops / (e2e_serial_ms * 1e-3) / 1e12 * world, 2)},
         "gpu_launches": K, "clocks": clock_rec,
     }
     if rank == 0 and world == 1:
