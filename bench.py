@@ -321,6 +321,15 @@ def cache_ops_bench(pkv, case, dev, stream, peak, iters=30, fill_blocks=400, cow
     pkv.device_status(clear=True)
     t_app = timed(lambda: pkv.kv_append(k_new, v_new, kc, vc, slots))
     t_cow = timed(lambda: pkv.block_copy(kc, vc, pairs))
+    # For scale: torch's own device copy of the same number of bytes (one
+    # contiguous buffer read and written), timed the same way.
+    ref = {}
+    for name, nbytes in (("kv_append_prompt_fill", 2 * T * Hkv * D * e),
+                         ("block_copy_cow_batch", 2 * n_cow * Hkv * B * D * e)):
+        src = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        dst = torch.empty_like(src)
+        ref[name] = timed(lambda: dst.copy_(src))
+        del src, dst
     if pkv.device_status(clear=True) != 0:
         raise RuntimeError("device status flags during the cache-operation bench")
     b_app = 2 * (2 * T * Hkv * D * e)          # K and V rows read, then written
@@ -328,14 +337,16 @@ def cache_ops_bench(pkv, case, dev, stream, peak, iters=30, fill_blocks=400, cow
     del kc, vc, flush
     torch.cuda.empty_cache()
 
-    def rec(ms, nbytes, what):
+    def rec(ms, nbytes, what, key):
         gbs = nbytes / (ms * 1e-3) / 1e9
         return {"what": what, "bytes_moved": nbytes, "ms": round(ms, 5), "GB/s": round(gbs, 1),
-                "frac_of_peak": round(gbs / peak, 4)}
+                "frac_of_peak": round(gbs / peak, 4),
+                "torch_copy_same_bytes_ms": round(ref[key], 5)}
 
     return {"kv_append_prompt_fill": rec(t_app, b_app, f"{T} tokens x {Hkv} heads into {n_fill} "
-                                         "random blocks"),
-            "block_copy_cow_batch": rec(t_cow, b_cow, f"{n_cow} block pairs, K and V"),
+                                         "random blocks", "kv_append_prompt_fill"),
+            "block_copy_cow_batch": rec(t_cow, b_cow, f"{n_cow} block pairs, K and V",
+                                        "block_copy_cow_batch"),
             "l2": "flushed (256 MiB read) before every timed call",
             "launch": "queued behind a device-side wait, outside the timed region", "iters": iters}
 

@@ -529,6 +529,76 @@ __global__ void __launch_bounds__(128) paged_decode_reduce_kernel(const DecodePa
   if (np <= 1) return;  // written directly by the decode kernel
   const float* mrow = p.ws_m + (size_t)pair * p.num_parts;
   const float* lrow = p.ws_l + (size_t)pair * p.num_parts;
+  const float* orow = p.ws_o + (size_t)pair * p.num_parts * D + lane * EPL;
+  T* out = static_cast<T*>(p.out) + (size_t)pair * D + lane * EPL;
+  if (np <= 32) {
+    // Up to 32 partitions (every automatic choice up to 32k tokens): lane i
+    // holds partition i's (m, l), and every load of the warp (the maxima,
+    // the sums and the first partials) is issued before any is used, so the
+    // merge costs one memory round trip.  Same arithmetic, in the same
+    // order, as the general loop below.
+    constexpr int kPre = 4;
+    float pre[kPre][EPL];
+#pragma unroll
+    for (int i = 0; i < kPre; ++i)
+      if (i < np) {
+        if constexpr (EPL == 4) {
+          const float4 a = *reinterpret_cast<const float4*>(orow + (size_t)i * D);
+          pre[i][0] = a.x;
+          pre[i][1] = a.y;
+          pre[i][2] = a.z;
+          pre[i][3] = a.w;
+        } else {
+          const float2 a = *reinterpret_cast<const float2*>(orow + (size_t)i * D);
+          pre[i][0] = a.x;
+          pre[i][1] = a.y;
+        }
+      }
+    const float mi = lane < np ? mrow[lane] : -CUDART_INF_F;
+    const float li = lane < np ? lrow[lane] : 0.f;
+    float M = mi;
+#pragma unroll
+    for (int mk = 16; mk >= 1; mk >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, mk));
+    const float wi = lane < np ? li * exp2f(mi - M) : 0.f;
+    float Lsum = 0.f + wi;
+#pragma unroll
+    for (int mk = 16; mk >= 1; mk >>= 1) Lsum += __shfl_xor_sync(kFull, Lsum, mk);
+    const float inv = 1.f / Lsum;
+    float acc[EPL];
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
+#pragma unroll
+    for (int i = 0; i < kPre; ++i)
+      if (i < np) {
+        const float w = __shfl_sync(kFull, wi, i) * inv;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) acc[e] += w * pre[i][e];
+      }
+#pragma unroll 4
+    for (int i = kPre; i < np; ++i) {
+      const float w = __shfl_sync(kFull, wi, i) * inv;
+      if constexpr (EPL == 4) {
+        const float4 a = *reinterpret_cast<const float4*>(orow + (size_t)i * D);
+        acc[0] += w * a.x;
+        acc[1] += w * a.y;
+        acc[2] += w * a.z;
+        acc[3] += w * a.w;
+      } else {
+        const float2 a = *reinterpret_cast<const float2*>(orow + (size_t)i * D);
+        acc[0] += w * a.x;
+        acc[1] += w * a.y;
+      }
+    }
+    if constexpr (EPL == 4) {
+      uint2 pk;
+      pk.x = Cvt<T>::from_float2(acc[0], acc[1]);
+      pk.y = Cvt<T>::from_float2(acc[2], acc[3]);
+      *reinterpret_cast<uint2*>(out) = pk;
+    } else {
+      *reinterpret_cast<uint32_t*>(out) = Cvt<T>::from_float2(acc[0], acc[1]);
+    }
+    return;
+  }
   float M = -CUDART_INF_F;
   for (int i = lane; i < np; i += 32) M = fmaxf(M, mrow[i]);
 #pragma unroll
@@ -538,7 +608,6 @@ __global__ void __launch_bounds__(128) paged_decode_reduce_kernel(const DecodePa
 #pragma unroll
   for (int mk = 16; mk >= 1; mk >>= 1) Lsum += __shfl_xor_sync(kFull, Lsum, mk);
   const float inv = 1.f / Lsum;
-  const float* orow = p.ws_o + (size_t)pair * p.num_parts * D + lane * EPL;
   float acc[EPL];
 #pragma unroll
   for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
@@ -557,7 +626,6 @@ __global__ void __launch_bounds__(128) paged_decode_reduce_kernel(const DecodePa
       acc[1] += w * a.y;
     }
   }
-  T* out = static_cast<T*>(p.out) + (size_t)pair * D + lane * EPL;
   if constexpr (EPL == 4) {
     uint2 pk;
     pk.x = Cvt<T>::from_float2(acc[0], acc[1]);
