@@ -86,10 +86,10 @@ int round_partition(int tokens) {
 // Every partition costs a CTA start-up (barrier set-up, table window,
 // pipeline fill), a drain and a round trip of its partial result through the
 // workspace, so partitions are kept long (up to 2048 tokens; measured best on
-// GB300 for 1k-32k contexts) and contexts are split only as far as needed to
-// give about four waves of CTAs.  Batches with very few (sequence, KV head)
-// units split finer (down to 256 tokens) because idle SMs cost more than
-// partition overhead there.
+// GB300 for 1k-32k contexts).  Contexts are split into whole waves of CTAs
+// where a split allows it, otherwise only as far as needed to give about four
+// waves.  Batches with very few (sequence, KV head) units split finer (down to
+// 256 tokens) because idle SMs cost more than partition overhead there.
 int auto_partition(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
                    int max_context_len) {
   if (max_context_len <= kPartitionQuantum) return kPartitionQuantum;
@@ -101,12 +101,30 @@ int auto_partition(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim
   if (sms <= 0) sms = kAssumedSms;  // no device: assume a GB300
   if (per_sm <= 0) per_sm = kAssumedCtasPerSm;
   const long long slots = (long long)sms * per_sm;
-  // Four waves rather than two: on GB300 this gained up to 6 % (8 sequences x
-  // 8k tokens) and lost nowhere on 8-64 sequences x 1k-32k tokens, the last
-  // partial wave being a smaller share of the call.
   const long long target = 4 * slots;
-  const long long parts = units >= target ? 1 : (target + units - 1) / units;
   const int floor_tokens = units * 4 >= slots ? 1024 : 256;
+  if (units < target) {
+    // Prefer a split whose CTAs fill whole waves: units * p within 5 % below
+    // k waves of resident CTAs, for the fewest waves k that allows a
+    // partition of [floor_tokens, kMaxAutoPartition] tokens (a multiple of
+    // 32).  On GB300 a full single wave beat the four-wave split by 11 % (8
+    // sequences x 8k tokens) and two full waves by 6 % (16 x 8k).
+    for (long long k = 1; k <= 4; ++k) {
+      const long long p = k * slots / units;
+      if (p < 2) continue;
+      long long part = (max_context_len + p - 1) / p;
+      part = ((part + kPartitionQuantum - 1) / kPartitionQuantum) * kPartitionQuantum;
+      const long long ctas = units * ((max_context_len + part - 1) / part);
+      if (part < floor_tokens || part > kMaxAutoPartition || ctas > k * slots ||
+          ctas * 20 < k * slots * 19)
+        continue;
+      return (int)part;
+    }
+  }
+  // Otherwise split until about four waves of CTAs: on GB300 four waves beat
+  // two by up to 6 % and lost nowhere on 8-64 sequences x 1k-32k tokens, the
+  // last partial wave being a smaller share of the call.
+  const long long parts = units >= target ? 1 : (target + units - 1) / units;
   long long part = (max_context_len + parts - 1) / parts;
   part = ((part + 255) / 256) * 256;
   if (part < floor_tokens) part = floor_tokens;

@@ -88,9 +88,12 @@ def test_auto_partition_policy(lib):
     assert part(8, 32, 8, 128, 100) == 128          # short context: one partition
     assert part(64, 40, 40, 128, 2048) == 2048      # 2560 units: enough CTAs unsplit
     assert part(256, 32, 8, 128, 4096) == 2048      # long contexts: 2048-token partitions
-    assert part(8, 32, 8, 128, 32768) == 1280       # 64 units: ~four waves of CTAs
-    assert part(8, 32, 8, 128, 8192) == 512
-    assert part(16, 32, 8, 128, 16384) == 1280
+    # 64 or 128 units: the fewest whole waves of CTAs (within 5 % below k x 456)
+    assert part(8, 32, 8, 128, 8192) == 1184        # 7 parts: 448 CTAs, one wave
+    assert part(16, 32, 8, 128, 8192) == 1184       # 7 parts: 896 CTAs, two waves
+    assert part(8, 32, 8, 128, 32768) == 1568       # 21 parts: 1344 CTAs, three waves
+    assert part(16, 32, 8, 128, 16384) == 1184      # 14 parts: 1792 CTAs, four waves
+    assert part(32, 32, 8, 128, 4096) == 1024       # no whole-wave split: ~four waves
     assert part(128, 32, 8, 128, 2048) == 1024      # 1024 units: two partitions
     assert part(8, 32, 8, 128, 1024) == 256         # 64 units: split finer to fill the GPU
     assert part(64, 32, 8, 128, 1024) == 1024       # 512 units: not worth splitting 1k
