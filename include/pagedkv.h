@@ -41,9 +41,10 @@
  *     the offending access is skipped or redirected to block 0, the result is
  *     undefined, and a PKV_DEV_* flag is raised in a per-device status word
  *     read by pkv_device_status().
- *   - The kernels never spin on another block or another launch; the only
- *     waits are on their own copies into shared memory, each bounded in time
- *     (PKV_DEV_WAIT_TIMEOUT).
+ *   - The kernels never spin on another block or another launch.  Apart from
+ *     the wait for the previous kernel on the stream described above, the
+ *     only waits are on their own copies into shared memory, each bounded in
+ *     time (PKV_DEV_WAIT_TIMEOUT).
  */
 #ifndef PAGEDKV_H_
 #define PAGEDKV_H_
@@ -295,6 +296,9 @@ pkv_status_t pkv_paged_attn_prefill(
  *   slot_mapping  int64 [num_tokens]; flat slot = physical_block * B + offset
  * Slots must be distinct (two tokens writing one slot race).  A slot at or
  * beyond num_blocks * block_size is skipped and flags PKV_DEV_BAD_SLOT.
+ * Errors: PKV_ERR_INVALID_ARG (null or misaligned pointer, negative sizes,
+ * bad dtype), PKV_ERR_UNSUPPORTED (head_dim or block_size not built, or more
+ * than 2^31 16-byte chunks of K in one call: 32 GiB), PKV_ERR_CUDA.
  * ---------------------------------------------------------------------- */
 pkv_status_t pkv_kv_append(
     const void* k, const void* v, void* k_cache, void* v_cache,

@@ -432,7 +432,8 @@ pkv_status_t pkv_kv_append(const void* k, const void* v, void* k_cache, void* v_
   if (!aligned16(k) || !aligned16(v) || !aligned16(k_cache) || !aligned16(v_cache))
     return PKV_ERR_INVALID_ARG;
   if (reinterpret_cast<uintptr_t>(slot_mapping) & 7u) return PKV_ERR_INVALID_ARG;
-  if ((long long)num_kv_heads * head_dim * 2 / 16 > 0x7fffffffLL) return PKV_ERR_UNSUPPORTED;
+  if ((long long)num_tokens * num_kv_heads * head_dim * 2 / 16 > pkv::kMaxAppendChunks)
+    return PKV_ERR_UNSUPPORTED;
   unsigned int* status = nullptr;
   cudaError_t err = status_word(&status);
   if (err != cudaSuccess) return cuda_fail(err);

@@ -24,7 +24,7 @@ namespace pkv {
 namespace {
 
 constexpr int kCopyThreads = 256;
-constexpr int kUnroll = 4;
+constexpr int kUnroll = 2;
 constexpr int kCopyUnroll = 8;  // block_copy: 16 chunks (K and V) in flight per thread
 
 __device__ __forceinline__ uint4 load_stream(const uint4* p) {
@@ -35,51 +35,51 @@ __device__ __forceinline__ uint4 load_stream(const uint4* p) {
   return r;
 }
 
-// grid.x covers one token's Hkv * D row in chunks of 16 bytes, grid.y walks
-// tokens.  Chunk c of a token belongs to head c >> log2_cpr.
+// The (token, 16-byte chunk) pairs of the whole call form one index space,
+// chunk i being chunk i % row_chunks of token i / row_chunks (the source rows
+// are contiguous, so i also indexes k and v).  Every thread moves kUnroll
+// chunks of K and of V whatever the width of a token's row: 128 chunks for 8
+// heads of 128, 640 for 40.  Chunk c of a token belongs to head
+// c >> log2_cpr.  The data loads are issued first, since their addresses do
+// not depend on the slot; the slot reads then overlap them.
 __global__ void __launch_bounds__(kCopyThreads)
     kv_append_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v,
                      uint4* __restrict__ k_cache, uint4* __restrict__ v_cache,
-                     const int64_t* __restrict__ slot_mapping, int num_tokens, int row_chunks,
-                     int log2_cpr, int num_kv_heads, int block_size, long long num_slots,
-                     unsigned int* status) {
+                     const int64_t* __restrict__ slot_mapping, unsigned total_chunks,
+                     unsigned row_chunks, int log2_cpr, int num_kv_heads, int block_size,
+                     long long num_slots, unsigned int* status) {
   grid_dep_wait();
   grid_dep_launch_dependents();
-  const int cpr_mask = (1 << log2_cpr) - 1;
-  for (int t = blockIdx.y; t < num_tokens; t += gridDim.y) {
+  const unsigned cpr_mask = (1u << log2_cpr) - 1u;
+  const unsigned i0 = blockIdx.x * (unsigned)(kCopyThreads * kUnroll) + threadIdx.x;
+  uint4 rk[kUnroll], rv[kUnroll];
+#pragma unroll
+  for (int u = 0; u < kUnroll; ++u) {
+    const unsigned i = i0 + u * kCopyThreads;
+    if (i < total_chunks) {
+      rk[u] = load_stream(k + i);
+      rv[u] = load_stream(v + i);
+    }
+  }
+#pragma unroll
+  for (int u = 0; u < kUnroll; ++u) {
+    const unsigned i = i0 + u * kCopyThreads;
+    if (i >= total_chunks) continue;
+    const unsigned t = i / row_chunks;
+    const unsigned c = i - t * row_chunks;
     const long long slot = slot_mapping[t];
     if (slot < 0) continue;  // padding token
     if (slot >= num_slots) {
-      if (threadIdx.x == 0 && blockIdx.x == 0) atomicOr(status, PKV_DEV_BAD_SLOT);
+      if (c == 0) atomicOr(status, PKV_DEV_BAD_SLOT);
       continue;
     }
     const long long blk = slot / block_size;
     const long long off = slot - blk * block_size;
-    const uint4* ks = k + (size_t)t * row_chunks;
-    const uint4* vs = v + (size_t)t * row_chunks;
-    for (int c0 = blockIdx.x * kCopyThreads * kUnroll + threadIdx.x; c0 < row_chunks;
-         c0 += gridDim.x * kCopyThreads * kUnroll) {
-      uint4 rk[kUnroll], rv[kUnroll];
-#pragma unroll
-      for (int u = 0; u < kUnroll; ++u) {
-        const int c = c0 + u * kCopyThreads;
-        if (c < row_chunks) {
-          rk[u] = load_stream(ks + c);
-          rv[u] = load_stream(vs + c);
-        }
-      }
-#pragma unroll
-      for (int u = 0; u < kUnroll; ++u) {
-        const int c = c0 + u * kCopyThreads;
-        if (c < row_chunks) {
-          const int h = c >> log2_cpr;
-          const size_t dst =
-              ((((size_t)blk * num_kv_heads + h) * block_size + off) << log2_cpr) + (c & cpr_mask);
-          k_cache[dst] = rk[u];
-          v_cache[dst] = rv[u];
-        }
-      }
-    }
+    const size_t dst =
+        ((((size_t)blk * num_kv_heads + (c >> log2_cpr)) * block_size + off) << log2_cpr) +
+        (c & cpr_mask);
+    k_cache[dst] = rk[u];
+    v_cache[dst] = rv[u];
   }
 }
 
@@ -153,14 +153,16 @@ cudaError_t launch_kv_append(const void* k, const void* v, void* k_cache, void* 
                              unsigned int* status, cudaStream_t stream) {
   const int cpr = head_dim * 2 / 16;  // 16-byte chunks per head row
   const int log2_cpr = cpr == 8 ? 3 : 4;
-  const int row_chunks = num_kv_heads * cpr;
-  const int gx = (row_chunks + kCopyThreads * kUnroll - 1) / (kCopyThreads * kUnroll);
-  const int gy = num_tokens < 65535 ? num_tokens : 65535;
+  const long long row_chunks = (long long)num_kv_heads * cpr;
+  const long long total = (long long)num_tokens * row_chunks;
+  if (total > kMaxAppendChunks) return cudaErrorInvalidValue;  // rejected by the caller first
+  const long long span = kCopyThreads * kUnroll;
+  const unsigned gx = (unsigned)((total + span - 1) / span);
   return launch_overlapped(
-      kv_append_kernel, dim3(gx, gy), dim3(kCopyThreads), 0, stream,
+      kv_append_kernel, dim3(gx), dim3(kCopyThreads), 0, stream,
       static_cast<const uint4*>(k), static_cast<const uint4*>(v), static_cast<uint4*>(k_cache),
-      static_cast<uint4*>(v_cache), slot_mapping, num_tokens, row_chunks, log2_cpr, num_kv_heads,
-      block_size, (long long)num_blocks * block_size, status);
+      static_cast<uint4*>(v_cache), slot_mapping, (unsigned)total, (unsigned)row_chunks,
+      log2_cpr, num_kv_heads, block_size, (long long)num_blocks * block_size, status);
 }
 
 cudaError_t launch_block_copy(void* k_cache, void* v_cache, const int64_t* pairs, int num_pairs,

@@ -83,6 +83,10 @@ struct PrefillArgs {
 // the work needs more CTAs than a 1-D grid holds.
 cudaError_t launch_paged_prefill(const PrefillArgs& a, cudaStream_t stream, bool* unsupported);
 
+// kv_append indexes (token, 16-byte chunk) pairs with 32 bits: a call may move
+// at most this many chunks of K (and as many of V), 32 GiB each.
+constexpr long long kMaxAppendChunks = 1LL << 31;
+
 cudaError_t launch_kv_append(const void* k, const void* v, void* k_cache, void* v_cache,
                              const int64_t* slot_mapping, int num_tokens, int num_kv_heads,
                              int head_dim, int block_size, int num_blocks,

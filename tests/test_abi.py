@@ -110,6 +110,9 @@ def test_append_and_copy_host_validation(lib):
     assert lib.pkv_kv_append(16, 16, 16, 16, 16, 3, 8, 80, 16, 4, 0, None) == 2
     assert lib.pkv_kv_append(16, 16, 16, 16, 12, 3, 8, 128, 16, 4, 0, None) == 1
     assert lib.pkv_kv_append(16, 16, 16, 16, 16, -1, 8, 128, 16, 4, 0, None) == 1
+    # more than 2^31 16-byte chunks of K in one call (2^24 + 1 tokens x 8 heads x
+    # 128): refused on the host before anything touches the device
+    assert lib.pkv_kv_append(16, 16, 16, 16, 16, (1 << 24) + 1, 8, 128, 16, 4, 0, None) == 2
     assert lib.pkv_block_copy(None, None, None, 0, 4, 4096, None) == 0
     assert lib.pkv_block_copy(16, 16, 16, 2, 4, 4090, None) == 1
     assert lib.pkv_block_copy(16, 16, None, 2, 4, 4096, None) == 1
