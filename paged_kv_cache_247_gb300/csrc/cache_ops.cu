@@ -24,7 +24,7 @@ namespace pkv {
 namespace {
 
 constexpr int kCopyThreads = 256;
-constexpr int kUnroll = 2;
+constexpr int kUnroll = 2;      // kv_append: 2 chunks of K and 2 of V per thread
 constexpr int kCopyUnroll = 8;  // block_copy: 16 chunks (K and V) in flight per thread
 
 __device__ __forceinline__ uint4 load_stream(const uint4* p) {
