@@ -105,6 +105,23 @@ def test_auto_partition_policy(lib):
         assert ws == (0 if parts <= 1 else args[0] * args[1] * parts * (args[3] + 2) * 4)
 
 
+def test_auto_partition_properties(lib):
+    """Whatever branch picks it, the automatic partition is a positive multiple
+    of 32, at most 2048 tokens unless one partition covers the whole context,
+    and its workspace size matches the partition count it implies."""
+    part = lib.pkv_decode_partition_size
+    ws = lib.pkv_decode_workspace_size
+    for S in (1, 3, 8, 16, 37, 64, 128, 256, 1000):
+        for hq, hkv in ((8, 8), (32, 8), (40, 40), (12, 4), (64, 8)):
+            for ctx in (1, 31, 32, 33, 700, 1024, 2049, 5000, 8192, 32768, 100000):
+                p = part(S, hq, hkv, 128, ctx)
+                assert p > 0 and p % 32 == 0, (S, hq, hkv, ctx, p)
+                parts = -(-ctx // p)
+                assert p <= 2048 or parts == 1, (S, hq, hkv, ctx, p)
+                assert ws(S, hq, hkv, 128, ctx, 0) == (
+                    0 if parts <= 1 else S * hq * parts * (128 + 2) * 4), (S, hq, hkv, ctx, p)
+
+
 def test_append_and_copy_host_validation(lib):
     assert lib.pkv_kv_append(None, None, None, None, None, 0, 8, 128, 16, 4, 0, None) == 0
     assert lib.pkv_kv_append(16, 16, 16, 16, 16, 3, 8, 80, 16, 4, 0, None) == 2
