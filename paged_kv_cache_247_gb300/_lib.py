@@ -66,10 +66,12 @@ SIGNATURES = {
     "pkv_alloc_add_seq": (c_int, [c_void_p, c_int64, c_int]),
     "pkv_alloc_fork": (c_int, [c_void_p, c_int64, c_int64]),
     "pkv_alloc_append_slot": (c_int, [c_void_p, c_int64, P_i64, P_i64, P_i64]),
-    "pkv_alloc_append_slots": (c_int, [c_void_p, P_i64, c_int, P_i64, P_i64, P_int]),
+    # array arguments are passed as addresses (numpy's .ctypes.data), which
+    # costs half as much per call as building typed pointers
+    "pkv_alloc_append_slots": (c_int, [c_void_p, c_void_p, c_int, c_void_p, c_void_p, P_int]),
     "pkv_alloc_free_seq": (c_int, [c_void_p, c_int64]),
-    "pkv_alloc_block_table": (c_int, [c_void_p, P_i64, c_int, P_i32, c_int]),
-    "pkv_alloc_seq_slots": (c_int, [c_void_p, c_int64, c_int, c_int, P_i64]),
+    "pkv_alloc_block_table": (c_int, [c_void_p, c_void_p, c_int, c_void_p, c_int]),
+    "pkv_alloc_seq_slots": (c_int, [c_void_p, c_int64, c_int, c_int, c_void_p]),
     "pkv_alloc_seq_info": (c_int, [c_void_p, c_int64, P_int, P_int]),
     "pkv_alloc_refcount": (c_int, [c_void_p, c_int, P_int]),
     "pkv_alloc_stats": (c_int, [c_void_p, ctypes.POINTER(AllocStats)]),

@@ -11,8 +11,9 @@ class OutOfBlocks(_lib.PagedKVError):
     pass
 
 
-def _p64(a):
-    return a.ctypes.data_as(_lib.P_i64)
+def _addr(a):
+    """Address of a contiguous numpy array's data."""
+    return a.ctypes.data
 
 
 class BlockAllocator:
@@ -61,7 +62,7 @@ class BlockAllocator:
         slots = np.empty(n, dtype=np.int64)
         pairs = np.empty((max(n, 1), 2), dtype=np.int64)
         count = ctypes.c_int(0)
-        st = self._lib.pkv_alloc_append_slots(self._h, _p64(ids), n, _p64(slots), _p64(pairs),
+        st = self._lib.pkv_alloc_append_slots(self._h, _addr(ids), n, _addr(slots), _addr(pairs),
                                               ctypes.byref(count))
         self._check(st, "append_slots")
         return slots, pairs[:count.value].copy()
@@ -72,14 +73,13 @@ class BlockAllocator:
     def block_table(self, seq_ids, max_blocks):
         ids = np.ascontiguousarray(seq_ids, dtype=np.int64)
         out = np.empty((len(ids), max_blocks), dtype=np.int32)
-        st = self._lib.pkv_alloc_block_table(self._h, _p64(ids), len(ids),
-                                             out.ctypes.data_as(_lib.P_i32), max_blocks)
+        st = self._lib.pkv_alloc_block_table(self._h, _addr(ids), len(ids), _addr(out), max_blocks)
         self._check(st, "block_table")
         return out
 
     def seq_slots(self, seq_id, start, count):
         out = np.empty(count, dtype=np.int64)
-        self._check(self._lib.pkv_alloc_seq_slots(self._h, seq_id, start, count, _p64(out)),
+        self._check(self._lib.pkv_alloc_seq_slots(self._h, seq_id, start, count, _addr(out)),
                     "seq_slots")
         return out
 
