@@ -173,3 +173,185 @@ def test_random_branching_cancellation_reuse(seed):
     for s in list(hist):
         a.free_seq(s)
     assert len(a.free) == NB and not any(a.refcount)
+
+
+# ------------------------------------------- batched, all-or-nothing appends --
+#
+# append_slots is the batched form of append_slot ("Only 20.4% of your KV
+# cache held actual tokens", section "The part everyone forgets: pages enable
+# sharing, not just packing": a step reserves each sequence's next slot and
+# copies a shared partial block first; "The KV cache is a systems problem",
+# section "Shared prefixes need ownership rules").  Its pins do not trust its
+# own snapshot: a successful batch must act exactly like the same appends made
+# one at a time (state compared field by field, contents through the slot
+# model), and a failed batch must leave every field equal to a deep copy taken
+# before the call.
+
+import copy
+import inspect
+import types
+
+import oracle.allocator as oracle_allocator_module
+
+
+def _state(a):
+    return (list(a.free), list(a.refcount), {k: list(v) for k, v in a.tables.items()},
+            dict(a.lengths), a.cow_copies)
+
+
+def _shared_setup(cls, num_blocks=64, block_size=4):
+    """Two prompts, each forked, with partly filled last blocks (copy-on-write
+    pending) and one prompt that ends on a block boundary."""
+    a = cls(num_blocks, block_size)
+    pool = ContentPool(num_blocks, block_size)
+    hist = {}
+    tok = 0
+    for sid, n in ((0, 6), (2, 8), (4, 3)):
+        a.add_seq(sid, n)
+        hist[sid] = []
+        for t in range(n):
+            pool.write(a.slot_of(sid, t), tok)
+            hist[sid].append(tok)
+            tok += 1
+    for parent, child in ((0, 1), (2, 3), (4, 5), (4, 6)):
+        a.fork(parent, child)
+        hist[child] = list(hist[parent])
+    return a, pool, hist
+
+
+def _batch_matches_single_appends(cls):
+    """A batch equals the same append_slot calls one by one, and its slots and
+    pairs keep every sequence's history intact in the slot model."""
+    a, pool, hist = _shared_setup(cls)
+    b = copy.deepcopy(a)
+    order = [1, 0, 5, 3, 2, 6, 4]
+    tok = 1000
+    for rnd in range(6):  # crosses block boundaries and later copy-on-writes
+        slots, pairs = a.append_slots(order)
+        single_slots, single_pairs = [], []
+        for s in order:
+            slot, cs, cd = oracle_allocator_module.OracleAllocator.append_slot(b, s)
+            single_slots.append(slot)
+            if cs >= 0:
+                single_pairs.append([cs, cd])
+        if list(slots) != single_slots or [list(p) for p in pairs] != single_pairs:
+            return False
+        if _state(a) != _state(b):
+            return False
+        for src, dst in pairs:  # copies first, then the step's writes
+            pool.copy(src, dst)
+        for s, slot in zip(order, slots):
+            pool.write(slot, tok)
+            hist[s].append(tok)
+            tok += 1
+        for s, h in hist.items():
+            if pool.read(a.tables[s], a.lengths[s]) != h:
+                return False
+        if rnd == 0 and len(pairs) != 3:  # 0/1 and 4/5/6 share partial blocks
+            return False
+    return True
+
+
+def _failed_batch_restores(cls):
+    """Pool exhausted at the k-th sequence, and an unknown id last: the error
+    is raised and every field equals a deep copy taken before the call."""
+    # (1) exhausted: two free blocks, the third sequence needs one more
+    a = cls(6, 4)
+    for sid in range(4):
+        a.add_seq(sid, 4)  # blocks 0..3, each full
+    a.free_seq(1)
+    a.free_seq(3)          # free stack [5, 4, 1, 3]: pops 3, 1, 4, 5
+    a.add_seq(4, 5)        # blocks 3, 1, the last one partly filled ...
+    a.fork(4, 5)           # ... and shared, so seq 4 copies on its next write
+    snap = copy.deepcopy(_state(a))
+    if snap[0] != [5, 4] or snap[4] != 0:
+        return False
+    try:
+        a.append_slots([4, 0, 2])  # 4 copies (takes 4), 0 takes 5, 2 finds none
+        return False
+    except OracleOutOfBlocks:
+        pass
+    if _state(a) != snap:
+        return False
+    # (2) a larger pool: copy-on-write and fresh blocks happen, then an
+    # unknown sequence id ends the batch
+    a, _, _ = _shared_setup(cls, num_blocks=12)
+    for s in (0, 1, 4):  # consume and return a few blocks so the stack is out of order
+        a.append_slots([s])
+    a.free_seq(6)
+    a.add_seq(7, 4)
+    a.free_seq(7)
+    snap = copy.deepcopy(_state(a))
+    try:
+        a.append_slots([5, 2, 3, 0, 99])
+        return False
+    except KeyError:
+        pass
+    if _state(a) != snap:
+        return False
+    # (3) exhausted by a copy-on-write: nothing changes, not even the count
+    a = cls(3, 4)
+    a.add_seq(0, 5)
+    a.fork(0, 1)
+    a.add_seq(2, 1)
+    snap = copy.deepcopy(_state(a))
+    try:
+        a.append_slots([2, 0])  # 2 writes in place, 0 needs a copy: none free
+        return False
+    except OracleOutOfBlocks:
+        pass
+    return _state(a) == snap
+
+
+def _batch_pins_pass(cls):
+    # each planted mistake must make a pin return False, not crash it
+    return _batch_matches_single_appends(cls) and _failed_batch_restores(cls)
+
+
+def test_batch_pins_hold_for_the_oracle():
+    assert _batch_matches_single_appends(OracleAllocator)
+    assert _failed_batch_restores(OracleAllocator)
+
+
+def test_failed_batch_stack_is_out_of_order():
+    """The second failure case starts from a free stack of several distinct
+    ids, so a restore in the wrong order changes it."""
+    a, _, _ = _shared_setup(OracleAllocator, num_blocks=12)
+    for s in (0, 1, 4):
+        a.append_slots([s])
+    a.free_seq(6)
+    a.add_seq(7, 4)
+    a.free_seq(7)
+    assert len(a.free) >= 2 and a.free != list(reversed(a.free))
+
+
+def _mutated_allocator(old, new):
+    src = inspect.getsource(oracle_allocator_module)
+    assert old in src, old
+    mod = types.ModuleType("mutated_allocator")
+    exec(compile(src.replace(old, new), "mutated_allocator", "exec"), mod.__dict__)
+    # raise the same exception class as the real model, so that the pins see
+    # the mutant's errors exactly as they see the oracle's
+    mod.OracleOutOfBlocks = OracleOutOfBlocks
+    return mod.OracleAllocator
+
+
+@pytest.mark.parametrize("old,new", [
+    # the copy-on-write count is not restored
+    ("(self.free, self.refcount, self.tables, self.lengths, self.cow_copies) = saved",
+     "(self.free, self.refcount, self.tables, self.lengths, _) = saved"),
+    # the free stack comes back in the wrong order
+    ("saved = (list(self.free),", "saved = (list(reversed(self.free)),"),
+    # the tables are saved by reference, so appended blocks survive the restore
+    ("{k: list(v) for k, v in self.tables.items()}, dict(self.lengths)",
+     "dict(self.tables), dict(self.lengths)"),
+    # not all or nothing: the appends before the failure stay
+    ("(self.free, self.refcount, self.tables, self.lengths, self.cow_copies) = saved\n",
+     "pass\n"),
+    # copy pairs reported backwards
+    ("pairs.append([src, dst])", "pairs.append([dst, src])"),
+    # a batch that skips the copy-on-write bookkeeping of the last sequence
+    ("for s in seq_ids:", "for s in list(seq_ids)[:-1]:"),
+])
+def test_batch_planted_mistake_is_caught(old, new):
+    assert not _batch_pins_pass(_mutated_allocator(old, new))
