@@ -97,6 +97,15 @@ __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity,
   return __all_sync(0xffffffffu, ok);
 }
 
+// Wait for a barrier phase for at most the wait limit, whatever the sticky
+// timeout flag says: used only to let this CTA's own copies and MMAs finish
+// before it exits.
+__device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity) {
+  const unsigned long long t0 = global_ns();
+  while (!mbar_try_wait(bar, parity) && global_ns() - t0 <= kWaitLimitNs) {
+  }
+}
+
 // Bulk global -> shared copy completing on an mbarrier (bytes: multiple of
 // 16, both addresses 16-byte aligned).  The L2 policy marks the source as
 // streamed once (evict-first).

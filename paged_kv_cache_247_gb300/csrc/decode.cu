@@ -46,6 +46,20 @@ constexpr unsigned kFull = 0xffffffffu;
 
 constexpr int ilog2(int x) { return x <= 1 ? 0 : 1 + ilog2(x >> 1); }
 
+// After a timed-out wait the consumers stop early and the CTA would exit with
+// bulk copies still landing in its shared memory.  The producer calls this
+// before it returns: if a wait timed out anywhere, it waits (bounded) for the
+// stages it filled last, whose copies may still be in flight.  On the normal
+// path every stage has been consumed and the check is the only cost.
+template <int NSTAGE>
+__device__ __forceinline__ void drain_if_timed_out(uint64_t* full, int issued,
+                                                   const unsigned int* status) {
+  if (!timed_out(status)) return;
+  for (int it = issued > NSTAGE ? issued - NSTAGE : 0; it < issued; ++it)
+    mbar_drain(&full[it % NSTAGE], (it / NSTAGE) & 1);
+  __syncwarp();
+}
+
 template <int D>
 constexpr int stages_for() { return D >= 128 ? 4 : 8; }
 
@@ -186,6 +200,7 @@ __global__ void __launch_bounds__(SmemLayout<T, D, GT>::kThreads, LayoutFor<D, G
     if constexpr (!kPaged) {
       // Contiguous baseline: one run per stage, no table.
       const size_t seq_base = ((size_t)s * p.num_kv_heads + kvh) * (size_t)p.block_size * D;
+      int issued = 0;
       for (int it = 0; it < nstages; ++it) {
         const int stg = it % NSTAGE;
         if (it >= NSTAGE && !mbar_wait_warp(&empty[stg], ((it / NSTAGE) - 1) & 1, p.status)) break;
@@ -200,7 +215,9 @@ __global__ void __launch_bounds__(SmemLayout<T, D, GT>::kThreads, LayoutFor<D, G
                     &full[stg], policy);
         }
         __syncwarp();
+        issued = it + 1;
       }
+      drain_if_timed_out<NSTAGE>(full, issued, p.status);
       return;
     }
     const int log2B = p.log2_block;
@@ -222,6 +239,7 @@ __global__ void __launch_bounds__(SmemLayout<T, D, GT>::kThreads, LayoutFor<D, G
       new_chunk = reinterpret_cast<const uint4*>(
           static_cast<const T*>(new_is_v ? p.v_new : p.k_new) + row_off)[new_c];
     }
+    int issued = 0;
     for (int it = 0; it < nstages; ++it) {
       const int stg = it % NSTAGE;
       if (it >= NSTAGE && !mbar_wait_warp(&empty[stg], ((it / NSTAGE) - 1) & 1, p.status)) break;
@@ -290,7 +308,9 @@ __global__ void __launch_bounds__(SmemLayout<T, D, GT>::kThreads, LayoutFor<D, G
         bulk_load(Ks + stg * L::kStageElems + row * D, kbase + off, bytes, &full[stg], policy);
         bulk_load(Vs + stg * L::kStageElems + row * D, vbase + off, bytes, &full[stg], policy);
       }
+      issued = it + 1;
     }
+    drain_if_timed_out<NSTAGE>(full, issued, p.status);
     return;
   }
 

@@ -267,15 +267,6 @@ __device__ __forceinline__ void tmem_st32u(uint32_t taddr, const uint32_t* w) {
       : "memory");
 }
 
-// Wait for a barrier phase for at most the wait limit, whatever the sticky
-// timeout flag says: used only to let this CTA's own copies and MMAs finish
-// before it exits.
-__device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity) {
-  const unsigned long long t0 = global_ns();
-  while (!mbar_try_wait(bar, parity) && global_ns() - t0 <= kWaitLimitNs) {
-  }
-}
-
 // Byte offset of 16-byte chunk c of row r in a tile of the layout above.
 template <int D>
 __device__ __forceinline__ uint32_t tile_chunk_offset(int r, int c) {
