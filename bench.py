@@ -47,7 +47,13 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=5000)
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="opt13b", choices=["opt13b", "gqa4k", "prefill", "sweep", "shared"])
+    ap.add_argument("--workload", default="opt13b",
+                    choices=["opt13b", "gqa4k", "prefill", "sweep", "shared", "groups"])
+    ap.add_argument("--only", default=None,
+                    help="--workload sweep: one case as block_size,batch,ctx (for profiler "
+                         "captures)")
+    ap.add_argument("--group", type=int, default=0,
+                    help="one query-head group size for --workload groups (0 = all)")
     ap.add_argument("--partition", type=int, default=0, help="tokens per partition (0 = library)")
     ap.add_argument("--path", default="fused", choices=["fused", "separate"],
                     help="one fused append+decode launch, or kv_append then decode")
@@ -1122,9 +1128,12 @@ def run_sweep(args, rank, world, local_rank):
     rows = []
     clocks = ClockSampler(dev.index if dev.index is not None else 0)
     clocks.start()
+    only = tuple(int(x) for x in args.only.split(",")) if args.only else None
     for B in sw["block_sizes"]:
         for S in sw["batches"]:
             for ctx in sw["ctxs"]:
+                if only is not None and (B, S, ctx) != only:
+                    continue
                 case = W.sweep_decode(B, S, ctx, device=dev)
                 Sq, Hq, D = case.q.shape
                 Hkv = case.k_cache.shape[1]
@@ -1152,7 +1161,8 @@ def run_sweep(args, rank, world, local_rank):
     clock_rec = clocks.stop()
     if pkv.device_status(clear=True) != 0:
         raise RuntimeError("device status flags during the sweep")
-    ref = next(r for r in rows if r["block_size"] == 16 and r["num_seqs"] == 64 and r["ctx"] == 8192)
+    ref = next((r for r in rows if r["block_size"] == 16 and r["num_seqs"] == 64
+                and r["ctx"] == 8192), rows[-1])
     if rank == 0:
         print(json.dumps({
             "metric": "paged decode attention HBM GB/s across block sizes, batches and contexts",
@@ -1165,6 +1175,66 @@ def run_sweep(args, rank, world, local_rank):
             "roofline": {"bound": "hbm", "achieved": ref["GB/s"], "peak": peak, "unit": "GB/s",
                          "frac": ref["frac"], "peak_kind": peak_kind, "traffic": None},
             "sweep": rows, "clocks": clock_rec}), flush=True)
+
+
+def run_groups(args, rank, world, local_rank):
+    """Decode across query-head group sizes over one KV cache shape (8 KV heads
+    of 128, bf16, 4,096 tokens per sequence): each call timed alone after
+    reading 256 MiB; algorithmic bytes (each K/V byte once per KV head) /
+    time against the HBM peak.  `--group G` runs one size only (for profiler
+    captures)."""
+    import paged_kv_cache_247_gb300 as pkv
+    from paged_kv_cache_247_gb300 import build as _build
+    from paged_kv_cache_247_gb300 import workloads as W
+    if rank == 0 or not os.path.exists(_build.LIB):
+        _build.build_library()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    peak, peak_kind = peak_hbm()
+    flush = torch.ones(32 << 20, dtype=torch.float64, device=dev)
+    S = args.num_seqs or 32
+    groups = [args.group] if args.group else [1, 2, 4, 8, 16, 32]
+    rows = []
+    clocks = ClockSampler(dev.index if dev.index is not None else 0)
+    clocks.start()
+    for G in groups:
+        case = W.make_decode_case(6, S, 8 * G, 8, 128, 16, "bf16", [4096] * S, device=dev)
+        Sq, Hq, D = case.q.shape
+        part = args.partition or pkv.decode_partition_size(Sq, Hq, 8, D, case.max_context_len)
+        ws = torch.empty(max(16, pkv.decode_workspace_size(Sq, Hq, 8, D, case.max_context_len,
+                                                           part)), dtype=torch.uint8, device=dev)
+        out = torch.empty_like(case.q)
+
+        def call():
+            pkv.paged_attn_decode(out, case.q, case.k_cache, case.v_cache, case.block_tables,
+                                  case.context_lens, case.scale, case.max_context_len,
+                                  partition_size=part, workspace=ws)
+        for _ in range(max(3, args.warmup)):
+            call()
+        iters = max(5, min(args.steps, 30))
+        ms = time_alone(call, flush, stream, iters)
+        nbytes = step_bytes(case)[0]
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        rows.append({"group": G, "num_q_heads": Hq, "partition": part, "kv_bytes": int(nbytes),
+                     "ms": round(ms, 5), "GB/s": round(gbs, 1), "frac": round(gbs / peak, 4),
+                     "traffic": ncu_traffic(f"paged_decode_kernel:g{G}", "groups")})
+        del case, ws, out
+        torch.cuda.empty_cache()
+    clock_rec = clocks.stop()
+    if pkv.device_status(clear=True) != 0:
+        raise RuntimeError("device status flags during the group sweep")
+    if rank == 0:
+        print(json.dumps({
+            "metric": "paged decode attention HBM GB/s across query-head group sizes",
+            "value": rows[-1]["GB/s"], "unit": "GB/s", "n_gpus": world, "steps": iters,
+            "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": f"decode, {S} seqs x 4096 tokens, 8 KV heads of 128, bf16, "
+                                   f"B=16, query heads 8 x group", "l2": "flushed (256 MiB read) "
+                                   "before every call",
+                       "launch": "queued behind a device-side wait, outside the timed region"},
+            "groups": rows, "clocks": clock_rec}), flush=True)
 
 
 def main():
@@ -1189,6 +1259,13 @@ def main():
                                       "the reference arm is timed on the decode workloads"}))
             else:
                 run_shared(args, rank, world, local_rank)
+        elif args.workload == "groups":
+            if args.impl == "reference":
+                if rank == 0:
+                    print(json.dumps({"impl": "reference", "unavailable":
+                                      "the reference arm is timed on the decode workloads"}))
+            else:
+                run_groups(args, rank, world, local_rank)
         elif args.workload == "sweep":
             if args.impl == "reference":
                 if rank == 0:
