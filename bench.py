@@ -49,6 +49,9 @@ def parse_args():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="opt13b",
                     choices=["opt13b", "gqa4k", "prefill", "sweep", "shared", "groups"])
+    ap.add_argument("--decode-path", type=int, default=0, choices=[0, 1, 2],
+                    help="decode kernel: 0 = the library's choice, 1 = CUDA cores, "
+                         "2 = tensor cores where supported")
     ap.add_argument("--only", default=None,
                     help="--workload sweep: one case as block_size,batch,ctx (for profiler "
                          "captures)")
@@ -94,6 +97,12 @@ def ncu_traffic(kernel_key, workload, sources=("decode.cu", "common.cuh", "overl
     if rec.get("source_hash") != source_hash(*sources):
         return None
     return rec.get("dram_bytes_per_launch")
+
+
+def set_decode_path(args):
+    """Apply --decode-path (process-wide in the library)."""
+    from paged_kv_cache_247_gb300 import _lib
+    _lib.check(_lib.load().pkv_set_decode_path(args.decode_path), "pkv_set_decode_path")
 
 
 def max_over_ranks(ms, world):
@@ -773,6 +782,7 @@ def run_ours(args, rank, world, local_rank):
     from paged_kv_cache_247_gb300 import build as _build
     if rank == 0 or not os.path.exists(_build.LIB):
         _build.build_library()
+    set_decode_path(args)
     if world > 1:
         torch.distributed.barrier()
     dev = torch.device("cuda", local_rank)
@@ -809,6 +819,7 @@ def run_prefill(args, rank, world, local_rank):
     from paged_kv_cache_247_gb300 import workloads as W
     if rank == 0 or not os.path.exists(_build.LIB):
         _build.build_library()
+    set_decode_path(args)
     if world > 1:
         torch.distributed.barrier()
     dev = torch.device("cuda", local_rank)
@@ -942,6 +953,7 @@ def run_shared(args, rank, world, local_rank):
     from paged_kv_cache_247_gb300 import workloads as W
     if rank == 0 or not os.path.exists(_build.LIB):
         _build.build_library()
+    set_decode_path(args)
     if world > 1:
         torch.distributed.barrier()
     dev = torch.device("cuda", local_rank)
@@ -1117,6 +1129,7 @@ def run_sweep(args, rank, world, local_rank):
     from paged_kv_cache_247_gb300 import workloads as W
     if rank == 0 or not os.path.exists(_build.LIB):
         _build.build_library()
+    set_decode_path(args)
     if world > 1:
         torch.distributed.barrier()
     dev = torch.device("cuda", local_rank)
@@ -1188,6 +1201,7 @@ def run_groups(args, rank, world, local_rank):
     from paged_kv_cache_247_gb300 import workloads as W
     if rank == 0 or not os.path.exists(_build.LIB):
         _build.build_library()
+    set_decode_path(args)
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     stream = torch.cuda.current_stream(dev)

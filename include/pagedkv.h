@@ -102,7 +102,13 @@ int pkv_version(void);
  * over t < context_lens[s], where G = num_q_heads / num_kv_heads (query head
  * h reads KV head h / G) and K_s[t] = k_cache[block_tables[s][t / B]][.][t % B].
  * Logits, softmax and the weighted sum are fp32; out is rounded to dtype
- * (round to nearest even).  A sequence with context_lens[s] == 0 gets zeros.
+ * (round to nearest even).  On the tensor-core path (head_dim 128 and a group
+ * G of 8 to 32 query heads by default, see pkv_set_decode_path) the softmax
+ * weights are rounded to dtype before the weighted sum, which the tensor
+ * core accumulates in fp32 ([P3] "Calculate bytes per token before choosing
+ * a batch": groups of query heads share one KV head, and a group of G heads
+ * does 2 G flops per cache byte).  A sequence with context_lens[s] == 0 gets
+ * zeros.
  * Positions at or beyond context_lens[s] are never read, and neither are
  * table entries past ceil(context_lens[s] / B).
  *
@@ -204,10 +210,25 @@ pkv_status_t pkv_paged_attn_decode_noalloc(
     int partition_size, pkv_stream_t stream);
 
 /* Partition size the library picks for partition_size == 0 on the current
- * device (depends on its SM count).  Returns a positive multiple of 32, or
- * -1 for invalid arguments. */
+ * device (depends on its SM count and on the decode kernel the call will
+ * use).  Returns a positive multiple of 32, or -1 for invalid arguments. */
 int pkv_decode_partition_size(int num_seqs, int num_q_heads, int num_kv_heads,
                               int head_dim, int max_context_len);
+
+/* Which decode kernel the decode calls use, process-wide (a tuning and test
+ * control; the default suits every shape measured):
+ *   0  chosen per call (default): the tensor-core kernel for head_dim 128
+ *      and groups of 8 to 32 query heads, the CUDA-core kernel otherwise;
+ *   1  always the CUDA-core kernel;
+ *   2  the tensor-core kernel wherever it applies (head_dim 128, groups of 3
+ *      to 32, partition_size 0 or a multiple of 128), else the CUDA-core one.
+ * Both compute the same attention within the stated tolerance.  It changes
+ * the partition pkv_decode_partition_size and pkv_decode_workspace_size
+ * report, so set it before sizing a workspace, and not while another host
+ * thread issues decode calls.  Returns PKV_ERR_INVALID_ARG for other
+ * values. */
+pkv_status_t pkv_set_decode_path(int path);
+int pkv_get_decode_path(void);
 
 /* Workspace bytes pkv_paged_attn_decode needs for these sizes (0 when the
  * call will not split).  partition_size as in pkv_paged_attn_decode.

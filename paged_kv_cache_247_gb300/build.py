@@ -20,8 +20,9 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libpagedkv.so")
 
-SOURCES = ["api.cu", "decode.cu", "prefill.cu", "cache_ops.cu", "allocator.cpp"]
+SOURCES = ["api.cu", "decode.cu", "decode_tc.cu", "prefill.cu", "cache_ops.cu", "allocator.cpp"]
 HEADERS = [os.path.join(CSRC, "common.cuh"), os.path.join(CSRC, "overlap.cuh"),
+           os.path.join(CSRC, "tcgen05.cuh"),
            os.path.join(CSRC, "kernels.h"),
            os.path.join(INCLUDE, "pagedkv.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

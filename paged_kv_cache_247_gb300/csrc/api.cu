@@ -76,11 +76,6 @@ bool decode_shape_ok(int num_seqs, int num_q_heads, int num_kv_heads, int max_co
          num_q_heads % num_kv_heads == 0 && max_context_len >= 0;
 }
 
-int round_partition(int tokens) {
-  const int t = tokens < 1 ? 1 : tokens;
-  return ((t + kPartitionQuantum - 1) / kPartitionQuantum) * kPartitionQuantum;
-}
-
 // Tokens per partition when the caller leaves the choice to the library.
 //
 // Every partition costs a CTA start-up (barrier set-up, table window,
@@ -90,30 +85,25 @@ int round_partition(int tokens) {
 // where a split allows it, otherwise only as far as needed to give about four
 // waves.  Batches with very few (sequence, KV head) units split finer (down to
 // 256 tokens) because idle SMs cost more than partition overhead there.
-int auto_partition(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
-                   int max_context_len) {
-  if (max_context_len <= kPartitionQuantum) return kPartitionQuantum;
-  const int group = num_q_heads / num_kv_heads;
-  const int gt = pkv::decode_heads_per_cta(group);
-  const long long units = (long long)num_seqs * num_kv_heads * ((group + gt - 1) / gt);
-  int sms = sm_count();
-  int per_sm = sms ? pkv::decode_ctas_per_sm(head_dim, gt) : 0;
-  if (sms <= 0) sms = kAssumedSms;  // no device: assume a GB300
-  if (per_sm <= 0) per_sm = kAssumedCtasPerSm;
-  const long long slots = (long long)sms * per_sm;
+//
+// units: CTAs per partition index ((sequence, KV head[, head chunk]) triples);
+// slots: CTAs resident on the device at once; quantum: partitions are a
+// multiple of it.
+int partition_for(long long units, long long slots, int max_context_len, int quantum) {
+  if (max_context_len <= quantum) return quantum;
   const long long target = 4 * slots;
   const int floor_tokens = units * 4 >= slots ? 1024 : 256;
   if (units < target) {
     // Prefer a split whose CTAs fill whole waves: units * p within 5 % below
     // k waves of resident CTAs, for the fewest waves k that allows a
     // partition of [floor_tokens, kMaxAutoPartition] tokens (a multiple of
-    // 32).  On GB300 a full single wave beat the four-wave split by 11 % (8
-    // sequences x 8k tokens) and two full waves by 6 % (16 x 8k).
+    // the quantum).  On GB300 a full single wave beat the four-wave split by
+    // 11 % (8 sequences x 8k tokens) and two full waves by 6 % (16 x 8k).
     for (long long k = 1; k <= 4; ++k) {
       const long long p = k * slots / units;
       if (p < 2) continue;
       long long part = (max_context_len + p - 1) / p;
-      part = ((part + kPartitionQuantum - 1) / kPartitionQuantum) * kPartitionQuantum;
+      part = ((part + quantum - 1) / quantum) * quantum;
       const long long ctas = units * ((max_context_len + part - 1) / part);
       if (part < floor_tokens || part > kMaxAutoPartition || ctas > k * slots ||
           ctas * 20 < k * slots * 19)
@@ -129,8 +119,57 @@ int auto_partition(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim
   part = ((part + 255) / 256) * 256;
   if (part < floor_tokens) part = floor_tokens;
   if (part > kMaxAutoPartition) part = kMaxAutoPartition;
-  if (part >= max_context_len) return round_partition(max_context_len);
+  if (part >= max_context_len)
+    return (int)(((long long)max_context_len + quantum - 1) / quantum * quantum);
   return (int)part;
+}
+
+int device_sms() {
+  const int sms = sm_count();
+  return sms > 0 ? sms : kAssumedSms;  // no device: assume a GB300
+}
+
+// Partition of the CUDA-core decode kernel.
+int auto_partition(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                   int max_context_len) {
+  const int group = num_q_heads / num_kv_heads;
+  const int gt = pkv::decode_heads_per_cta(group);
+  const long long units = (long long)num_seqs * num_kv_heads * ((group + gt - 1) / gt);
+  int per_sm = sm_count() > 0 ? pkv::decode_ctas_per_sm(head_dim, gt) : 0;
+  if (per_sm <= 0) per_sm = kAssumedCtasPerSm;
+  return partition_for(units, (long long)device_sms() * per_sm, max_context_len,
+                       kPartitionQuantum);
+}
+
+// Which decode kernel runs: 0 = chosen per call, 1 = CUDA cores, 2 = tensor
+// cores (where supported).  Process-wide; see pkv_set_decode_path.
+int g_decode_path = 0;
+
+// The decode kernel and partition size of one call.  The CUDA-core kernel
+// streams K/V through its FMA pipes; from a group of 8 query heads on, the
+// group's 2 G flops per byte exceed what those deliver at the HBM rate, and
+// the tensor-core kernel (one CTA per SM, every head of the group per CTA)
+// takes the call.
+struct DecodePlan {
+  bool tc;
+  int partition;
+};
+
+DecodePlan decode_plan(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                       int max_context_len, int partition_size) {
+  const int group = num_q_heads / num_kv_heads;
+  const int path = __atomic_load_n(&g_decode_path, __ATOMIC_RELAXED);
+  bool tc = path == 2 || (path == 0 && group >= 8);
+  if (tc && !pkv::decode_tc_supported(head_dim, group,
+                                      partition_size ? partition_size
+                                                     : pkv::kTcPartitionQuantum))
+    tc = false;
+  if (partition_size) return {tc, partition_size};
+  if (!tc)
+    return {false, auto_partition(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                  max_context_len)};
+  const long long units = (long long)num_seqs * num_kv_heads;
+  return {true, partition_for(units, device_sms(), max_context_len, pkv::kTcPartitionQuantum)};
 }
 
 long long num_parts_for(int max_context_len, int partition) {
@@ -165,17 +204,24 @@ int pkv_decode_partition_size(int num_seqs, int num_q_heads, int num_kv_heads, i
                               int max_context_len) {
   if (!decode_shape_ok(num_seqs, num_q_heads, num_kv_heads, max_context_len)) return -1;
   if (head_dim != 64 && head_dim != 128) return -1;
-  return auto_partition(num_seqs, num_q_heads, num_kv_heads, head_dim, max_context_len);
+  return decode_plan(num_seqs, num_q_heads, num_kv_heads, head_dim, max_context_len, 0).partition;
 }
+
+pkv_status_t pkv_set_decode_path(int path) {
+  if (path < 0 || path > 2) return PKV_ERR_INVALID_ARG;
+  __atomic_store_n(&g_decode_path, path, __ATOMIC_RELAXED);
+  return PKV_OK;
+}
+
+int pkv_get_decode_path(void) { return __atomic_load_n(&g_decode_path, __ATOMIC_RELAXED); }
 
 size_t pkv_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
                                  int max_context_len, int partition_size) {
   if (!decode_shape_ok(num_seqs, num_q_heads, num_kv_heads, max_context_len)) return (size_t)-1;
   if (head_dim != 64 && head_dim != 128) return (size_t)-1;
   if (partition_size < 0 || partition_size % kPartitionQuantum) return (size_t)-1;
-  const int part = partition_size ? partition_size
-                                  : auto_partition(num_seqs, num_q_heads, num_kv_heads, head_dim,
-                                                   max_context_len);
+  const int part = decode_plan(num_seqs, num_q_heads, num_kv_heads, head_dim, max_context_len,
+                               partition_size).partition;
   const long long parts = num_parts_for(max_context_len, part);
   if (parts <= 1) return 0;
   return (size_t)num_seqs * num_q_heads * parts * (head_dim + 2) * sizeof(float);
@@ -214,14 +260,16 @@ pkv_status_t paged_decode_impl(void* out, const void* q, const void* k_new, cons
 
   const int group = num_q_heads / num_kv_heads;
   const int gt = pkv::decode_heads_per_cta(group);
-  const int head_chunks = (group + gt - 1) / gt;
-  const int part = partition_size ? partition_size
-                                  : auto_partition(num_seqs, num_q_heads, num_kv_heads, head_dim,
-                                                   max_context_len);
+  const DecodePlan plan = decode_plan(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                      max_context_len, partition_size);
+  const int head_chunks = plan.tc ? 1 : (group + gt - 1) / gt;
+  const int part = plan.partition;
   const long long parts = num_parts_for(max_context_len, part);
   if (num_seqs > 65535 || (long long)num_kv_heads * head_chunks > 65535 || parts > 0x7fffffffLL)
     return PKV_ERR_UNSUPPORTED;
   if ((long long)num_seqs * num_q_heads > 0x7fffffffLL) return PKV_ERR_UNSUPPORTED;
+  if (plan.tc && (long long)num_blocks * num_kv_heads * block_size > 0x7fffffffLL)
+    return PKV_ERR_UNSUPPORTED;
 
   pkv::DecodeParams p{};
   p.out = out;
@@ -257,7 +305,15 @@ pkv_status_t paged_decode_impl(void* out, const void* q, const void* k_new, cons
   }
   cudaError_t err = status_word(&p.status);
   if (err != cudaSuccess) return cuda_fail(err);
-  err = pkv::launch_paged_decode(p, dtype, head_dim, gt, reinterpret_cast<cudaStream_t>(stream));
+  if (plan.tc) {
+    bool unsupported = false;
+    err = pkv::launch_paged_decode_tc(p, dtype, reinterpret_cast<cudaStream_t>(stream),
+                                      &unsupported);
+    if (unsupported) return PKV_ERR_UNSUPPORTED;
+  } else {
+    err = pkv::launch_paged_decode(p, dtype, head_dim, gt,
+                                   reinterpret_cast<cudaStream_t>(stream));
+  }
   if (err != cudaSuccess) return cuda_fail(err);
   return PKV_OK;
 }

@@ -743,6 +743,23 @@ size_t decode_smem_bytes(int head_dim, int gt) {
                  : (gt == 2 ? SmemLayout<__half, 128, 2>::kBytes : SmemLayout<__half, 128, 4>::kBytes);
 }
 
+cudaError_t launch_decode_reduce(const DecodeParams& p, int dtype, int head_dim,
+                                 cudaStream_t stream) {
+  const dim3 grid((p.num_seqs * p.num_q_heads + 3) / 4);
+  if (dtype == PKV_F16) {
+    return head_dim == 64
+               ? launch_overlapped(paged_decode_reduce_kernel<__half, 64>, grid, dim3(128), 0,
+                                   stream, p)
+               : launch_overlapped(paged_decode_reduce_kernel<__half, 128>, grid, dim3(128), 0,
+                                   stream, p);
+  }
+  return head_dim == 64
+             ? launch_overlapped(paged_decode_reduce_kernel<__nv_bfloat16, 64>, grid, dim3(128), 0,
+                                 stream, p)
+             : launch_overlapped(paged_decode_reduce_kernel<__nv_bfloat16, 128>, grid, dim3(128),
+                                 0, stream, p);
+}
+
 cudaError_t launch_paged_decode(const DecodeParams& p, int dtype, int head_dim, int gt,
                                 cudaStream_t stream) {
   return launch_any<true>(p, dtype, head_dim, gt, stream);

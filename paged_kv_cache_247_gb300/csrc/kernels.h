@@ -50,6 +50,22 @@ size_t decode_smem_bytes(int head_dim, int heads_per_cta);
 cudaError_t launch_paged_decode(const DecodeParams& p, int dtype, int head_dim,
                                 int heads_per_cta, cudaStream_t stream);
 
+// Only the split reduction (merging num_parts partials per (sequence, query
+// head)); used after the tensor-core decode kernel.
+cudaError_t launch_decode_reduce(const DecodeParams& p, int dtype, int head_dim,
+                                 cudaStream_t stream);
+
+// Grouped-head decode on the tensor cores: head size 128, groups of
+// kMinTcGroup..kMaxTcGroup query heads, partitions of whole 128-key tiles.
+constexpr int kMinTcGroup = 3;
+constexpr int kMaxTcGroup = 32;
+constexpr int kTcPartitionQuantum = 128;
+bool decode_tc_supported(int head_dim, int group, int partition_size);
+
+// unsupported is set when the tensor maps of the caches cannot be encoded.
+cudaError_t launch_paged_decode_tc(const DecodeParams& p, int dtype, cudaStream_t stream,
+                                   bool* unsupported);
+
 // Same kernels over a contiguous cache [S, Hkv, capacity, D]: block_size is
 // the capacity, block_tables is unused and sequence s reads rows of s.
 cudaError_t launch_contiguous_decode(const DecodeParams& p, int dtype, int head_dim,

@@ -40,8 +40,6 @@
 // tensor core computes the other tile's S or P V, so the two chains
 // S -> softmax -> P V interleave.
 
-#include <cuda.h>
-#include <cudaTypedefs.h>
 #include <math_constants.h>
 
 #include <algorithm>
@@ -49,13 +47,17 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "tcgen05.cuh"
 
 namespace pkv {
 namespace {
 
+using namespace tc;
+
 constexpr int kBM = 128;     // rows of a row tile: MMA M
 constexpr int kRowTiles = 2; // row tiles per CTA, one softmax warpgroup each
 constexpr int kBN = 128;     // keys per K/V tile: N of Q K^T, K of P V
+static_assert(kBN == kTileKeys, "TMA runs are capped at the tile length");
 constexpr int kSoftmaxWarps = 4 * kRowTiles;
 constexpr int kProducerWarp0 = kSoftmaxWarps;      // even K/V tiles
 constexpr int kMmaWarp = kSoftmaxWarps + 1;        // Q K^T; owns the tensor memory
@@ -113,165 +115,10 @@ struct PrefillParams {
   int pairs_per_group;  // (sequence, KV head) pairs whose items are launched together
 };
 
-// ---- tcgen05 helpers ------------------------------------------------------
-
-// Shared-memory matrix descriptor: start, leading/stride byte offsets,
-// descriptor version 1 (bits 46-47), 128-byte swizzle (bits 61-63 = 2).
-__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
-  return (uint64_t)((addr >> 4) & 0x3FFF) | ((uint64_t)((lbo >> 4) & 0x3FFF) << 16) |
-         ((uint64_t)((sbo >> 4) & 0x3FFF) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
-}
-
-// Instruction descriptor of kind::f16: fp32 accumulator, A/B type, majors,
-// N and M.
-__device__ __forceinline__ uint32_t instr_desc(bool bf16, bool b_mn_major, int n, int m) {
-  const uint32_t ab = bf16 ? 1u : 0u;
-  return (1u << 4) | (ab << 7) | (ab << 10) | ((b_mn_major ? 1u : 0u) << 16) |
-         ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
-}
-
-// D (+)= A.B with both operands described by shared-memory descriptors.
-__device__ __forceinline__ void mma_f16_ss(uint32_t d_tmem, uint64_t a, uint64_t b,
-                                           uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
-}
-
-// D (+)= A.B with the A operand read from tensor memory (row r in lane r,
-// element pairs packed low-first, 8 columns per 16 elements of K) and B
-// described by a shared-memory descriptor.
-__device__ __forceinline__ void mma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
-                                           uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate));
-}
-
-__device__ __forceinline__ void mma_commit(uint64_t* bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-          smem_addr(bar))
-      : "memory");
-}
-
-__device__ __forceinline__ void tc_fence_before() {
-  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-
-
-// 32 consecutive 32-bit columns of this thread's TMEM lane, loaded straight
-// into float registers, and a wait that names them, so that no use of the
-// loaded values can be scheduled before the wait.
-__device__ __forceinline__ void tmem_ld32f(uint32_t taddr, float* v) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
-      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-      : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3]), "=f"(v[4]), "=f"(v[5]), "=f"(v[6]),
-        "=f"(v[7]), "=f"(v[8]), "=f"(v[9]), "=f"(v[10]), "=f"(v[11]), "=f"(v[12]), "=f"(v[13]),
-        "=f"(v[14]), "=f"(v[15]), "=f"(v[16]), "=f"(v[17]), "=f"(v[18]), "=f"(v[19]),
-        "=f"(v[20]), "=f"(v[21]), "=f"(v[22]), "=f"(v[23]), "=f"(v[24]), "=f"(v[25]),
-        "=f"(v[26]), "=f"(v[27]), "=f"(v[28]), "=f"(v[29]), "=f"(v[30]), "=f"(v[31])
-      : "r"(taddr));
-}
-
-__device__ __forceinline__ void tmem_wait_ld_bind(float* v) {
-  asm volatile(
-      "tcgen05.wait::ld.sync.aligned;"
-      : "+f"(v[0]), "+f"(v[1]), "+f"(v[2]), "+f"(v[3]), "+f"(v[4]), "+f"(v[5]), "+f"(v[6]),
-        "+f"(v[7]), "+f"(v[8]), "+f"(v[9]), "+f"(v[10]), "+f"(v[11]), "+f"(v[12]), "+f"(v[13]),
-        "+f"(v[14]), "+f"(v[15]), "+f"(v[16]), "+f"(v[17]), "+f"(v[18]), "+f"(v[19]),
-        "+f"(v[20]), "+f"(v[21]), "+f"(v[22]), "+f"(v[23]), "+f"(v[24]), "+f"(v[25]),
-        "+f"(v[26]), "+f"(v[27]), "+f"(v[28]), "+f"(v[29]), "+f"(v[30]), "+f"(v[31])
-      :
-      : "memory");
-}
-
-// 2^x with the hardware approximation (MUFU.EX2, flush-to-zero).
-__device__ __forceinline__ float ex2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
-// max(a, b, c) in one instruction.
-__device__ __forceinline__ float fmax3(float a, float b, float c) {
-  float d;
-  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
-  return d;
-}
-
-// 16 consecutive 32-bit columns of this thread's lane, the wait that binds
-// them, and the store back.
-__device__ __forceinline__ void tmem_ld16f(uint32_t taddr, float* v) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
-      "%14,%15}, [%16];"
-      : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3]), "=f"(v[4]), "=f"(v[5]), "=f"(v[6]),
-        "=f"(v[7]), "=f"(v[8]), "=f"(v[9]), "=f"(v[10]), "=f"(v[11]), "=f"(v[12]), "=f"(v[13]),
-        "=f"(v[14]), "=f"(v[15])
-      : "r"(taddr));
-}
-__device__ __forceinline__ void tmem_wait_ld_bind16(float* v) {
-  asm volatile(
-      "tcgen05.wait::ld.sync.aligned;"
-      : "+f"(v[0]), "+f"(v[1]), "+f"(v[2]), "+f"(v[3]), "+f"(v[4]), "+f"(v[5]), "+f"(v[6]),
-        "+f"(v[7]), "+f"(v[8]), "+f"(v[9]), "+f"(v[10]), "+f"(v[11]), "+f"(v[12]), "+f"(v[13]),
-        "+f"(v[14]), "+f"(v[15])
-      :
-      : "memory");
-}
-__device__ __forceinline__ void tmem_st16f(uint32_t taddr, const float* v) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
-      "%13,%14,%15,%16};" ::"r"(taddr),
-      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
-      "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
-      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
-      "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
-      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
-      "r"(__float_as_uint(v[15]))
-      : "memory");
-}
-
-__device__ __forceinline__ void tmem_wait_st() {
-  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-}
-
-// Copy the box at coordinates (0, 0, 0, g) of a 4-D tensor map.
-__device__ __forceinline__ void tma_load_group(void* dst, const CUtensorMap* map, int g,
-                                               uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %2, %2, %3}], [%4];" ::"r"(smem_addr(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(g), "r"(smem_addr(bar))
-      : "memory");
-}
-
-// 32 consecutive 32-bit columns of packed pairs into this thread's lane.
-__device__ __forceinline__ void tmem_st32u(uint32_t taddr, const uint32_t* w) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
-      "%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(
-          taddr),
-      "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7]),
-      "r"(w[8]), "r"(w[9]), "r"(w[10]), "r"(w[11]), "r"(w[12]), "r"(w[13]), "r"(w[14]),
-      "r"(w[15]), "r"(w[16]), "r"(w[17]), "r"(w[18]), "r"(w[19]), "r"(w[20]), "r"(w[21]),
-      "r"(w[22]), "r"(w[23]), "r"(w[24]), "r"(w[25]), "r"(w[26]), "r"(w[27]), "r"(w[28]),
-      "r"(w[29]), "r"(w[30]), "r"(w[31])
-      : "memory");
-}
-
 // Byte offset of 16-byte chunk c of row r in a tile of the layout above.
 template <int D>
 __device__ __forceinline__ uint32_t tile_chunk_offset(int r, int c) {
-  return (uint32_t)((r >> 3) * PrefillSmem<D>::kGroup + (c >> 3) * 1024 + (r & 7) * 128 +
-                    (((c & 7) ^ (r & 7)) << 4));
+  return chunk_offset<D>(r, c);
 }
 
 // ---- the kernel -----------------------------------------------------------
@@ -429,7 +276,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     // P V; row tile 0 goes first and its softmax overlaps tile 1's MMAs.
     if (lane == 0) {
       constexpr bool bf16 = std::is_same<T, __nv_bfloat16>::value;
-      const uint32_t idesc_s = instr_desc(bf16, false, kBN, kBM);
+      const uint32_t idesc_s = instr_desc(bf16, false, false, kBN, kBM);
       const uint32_t aQ = smem_addr(sQ), aK = smem_addr(sK);
       bool ok = true;
       for (int i = 0; ok && i < n_tiles; ++i) {
@@ -463,7 +310,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
   } else if (warp == kPvWarp) {
     // --------------------------------------------------------- P V issuer
     constexpr bool bf16 = std::is_same<T, __nv_bfloat16>::value;
-    const uint32_t idesc_o = instr_desc(bf16, true, D, kBM);
+    const uint32_t idesc_o = instr_desc(bf16, false, true, D, kBM);
     const uint32_t aV = smem_addr(sV);
     bool ok = true;
     for (int i = 0; ok && i < n_tiles; ++i) {
@@ -689,45 +536,6 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
 }
 
 // ---- host side ------------------------------------------------------------
-
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static bool tried = false;
-  if (!tried) {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-    tried = true;
-  }
-  return fn;
-}
-
-// 4-D view of a cache for TMA: see below; boxes of min(block_size, 128)
-// rows, 128-byte swizzle.
-bool make_cache_map(CUtensorMap* map, const void* base, int dtype, long long rows, int head_dim,
-                    int block_size) {
-  PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
-  if (!fn) return false;
-  // The cache rows [rows, head_dim] seen as (64 columns, 8 rows, head_dim / 64
-  // atoms, rows / 8 groups): a box of whole groups lands as the tile layout
-  // above, every atom of every group in one copy.
-  const int atoms = head_dim / 64;
-  const int run = block_size < kBN ? block_size : kBN;
-  const cuuint64_t dims[4] = {64, 8, (cuuint64_t)atoms, (cuuint64_t)(rows / 8)};
-  const cuuint64_t strides[3] = {(cuuint64_t)head_dim * 2, 128, (cuuint64_t)head_dim * 2 * 8};
-  const cuuint32_t box[4] = {64, 8, (cuuint32_t)atoms, (cuuint32_t)(run / 8)};
-  const cuuint32_t estr[4] = {1, 1, 1, 1};
-  const CUresult r = fn(map,
-                        dtype == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
-                                          : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
-                        4, const_cast<void*>(base), dims, strides, box, estr,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
-}
 
 template <typename T, int D>
 cudaError_t launch_prefill_typed(const PrefillParams& p, const CUtensorMap& km,

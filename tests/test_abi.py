@@ -176,3 +176,26 @@ def test_copy_pair_validation():
                 [[0, 8]], [[-1, 3]]):    # ids outside the pool
         with pytest.raises(ValueError):
             check_copy_pairs(bad, 8)
+
+
+def test_decode_path_switch(lib):
+    """The process-wide decode-path control: values 0-2 only, and the
+    partition it implies (tensor-core partitions are whole 128-key tiles;
+    without a device the library assumes a GB300's 152 SMs)."""
+    assert lib.pkv_get_decode_path() == 0
+    try:
+        for bad in (-1, 3):
+            assert lib.pkv_set_decode_path(bad) == 1
+            assert lib.pkv_get_decode_path() == 0
+        # groups of 8 and more go to the tensor cores by default
+        assert lib.pkv_decode_partition_size(8, 64, 8, 128, 8192) % 128 == 0
+        assert lib.pkv_decode_partition_size(8, 256, 8, 128, 32768) % 128 == 0
+        assert lib.pkv_set_decode_path(2) == 0
+        assert lib.pkv_decode_partition_size(8, 32, 8, 128, 8192) % 128 == 0
+        # head_dim 64 and a group of 2 stay on the CUDA-core kernel
+        for args in ((8, 16, 8, 128, 8192), (8, 64, 8, 64, 8192)):
+            assert lib.pkv_decode_partition_size(*args) % 32 == 0
+        assert lib.pkv_set_decode_path(1) == 0
+        assert lib.pkv_get_decode_path() == 1
+    finally:
+        lib.pkv_set_decode_path(0)
