@@ -141,6 +141,36 @@ int auto_partition(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim
                        kPartitionQuantum);
 }
 
+// Partition of the tensor-core decode kernel.  Its CTAs are persistent (one
+// per SM) and take the work items (sequence, KV head, partition) in turn, so
+// a CTA's share is ceil(items / SMs) items.  The choice minimises that share
+// in 128-key tiles, counting about half a tile per item for the switch
+// between items and two tiles for the split reduction when there is one.
+int tc_partition(int num_seqs, int num_kv_heads, int max_context_len) {
+  const long long units = (long long)num_seqs * num_kv_heads;
+  const long long sms = device_sms();
+  const long long tiles = ((long long)max_context_len + pkv::kTcPartitionQuantum - 1) /
+                          pkv::kTcPartitionQuantum;
+  if (tiles <= 1) return pkv::kTcPartitionQuantum;
+  const int max_tiles = kMaxAutoPartition / pkv::kTcPartitionQuantum;
+  long long best_cost = -1;
+  int best = 1;
+  for (int pt = 1; pt <= max_tiles; ++pt) {
+    const long long parts = (tiles + pt - 1) / pt;
+    const long long per_item = tiles < pt ? tiles : pt;
+    const long long items = units * parts;
+    // costs in half tiles
+    const long long cost =
+        (items + sms - 1) / sms * (2 * per_item + 1) + (parts > 1 ? 4 : 0);
+    if (best_cost < 0 || cost <= best_cost) {  // ties: the longer partition
+      best_cost = cost;
+      best = pt;
+    }
+    if (pt >= tiles) break;
+  }
+  return best * pkv::kTcPartitionQuantum;
+}
+
 // Which decode kernel runs: 0 = chosen per call, 1 = CUDA cores, 2 = tensor
 // cores (where supported).  Process-wide; see pkv_set_decode_path.
 int g_decode_path = 0;
@@ -168,8 +198,7 @@ DecodePlan decode_plan(int num_seqs, int num_q_heads, int num_kv_heads, int head
   if (!tc)
     return {false, auto_partition(num_seqs, num_q_heads, num_kv_heads, head_dim,
                                   max_context_len)};
-  const long long units = (long long)num_seqs * num_kv_heads;
-  return {true, partition_for(units, device_sms(), max_context_len, pkv::kTcPartitionQuantum)};
+  return {true, tc_partition(num_seqs, num_kv_heads, max_context_len)};
 }
 
 long long num_parts_for(int max_context_len, int partition) {
@@ -307,8 +336,8 @@ pkv_status_t paged_decode_impl(void* out, const void* q, const void* k_new, cons
   if (err != cudaSuccess) return cuda_fail(err);
   if (plan.tc) {
     bool unsupported = false;
-    err = pkv::launch_paged_decode_tc(p, dtype, reinterpret_cast<cudaStream_t>(stream),
-                                      &unsupported);
+    err = pkv::launch_paged_decode_tc(p, dtype, device_sms(),
+                                      reinterpret_cast<cudaStream_t>(stream), &unsupported);
     if (unsupported) return PKV_ERR_UNSUPPORTED;
   } else {
     err = pkv::launch_paged_decode(p, dtype, head_dim, gt,

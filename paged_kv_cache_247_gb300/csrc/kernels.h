@@ -62,9 +62,10 @@ constexpr int kMaxTcGroup = 32;
 constexpr int kTcPartitionQuantum = 128;
 bool decode_tc_supported(int head_dim, int group, int partition_size);
 
-// unsupported is set when the tensor maps of the caches cannot be encoded.
-cudaError_t launch_paged_decode_tc(const DecodeParams& p, int dtype, cudaStream_t stream,
-                                   bool* unsupported);
+// Persistent: min(work items, sms) CTAs, one per SM.  unsupported is set when
+// the tensor maps of the caches or of q cannot be encoded.
+cudaError_t launch_paged_decode_tc(const DecodeParams& p, int dtype, int sms,
+                                   cudaStream_t stream, bool* unsupported);
 
 // Same kernels over a contiguous cache [S, Hkv, capacity, D]: block_size is
 // the capacity, block_tables is unused and sequence s reads rows of s.

@@ -166,6 +166,69 @@ __device__ __forceinline__ void tma_load_group(void* dst, const CUtensorMap* map
       : "memory");
 }
 
+// Copy the box at coordinates (0, row, 0) of a 3-D tensor map (make_rows_map).
+__device__ __forceinline__ void tma_load_rows(void* dst, const CUtensorMap* map, int row,
+                                              uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %2}], [%4];" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(row), "r"(smem_addr(bar))
+      : "memory");
+}
+
+// 4, 8 or 16 consecutive 32-bit columns of this thread's lane, loaded and
+// waited for.
+template <int C>
+__device__ __forceinline__ void tmem_load_small(uint32_t taddr, float* v) {
+  static_assert(C == 4 || C == 8 || C == 16, "4, 8 or 16 columns");
+  if constexpr (C == 4) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];"
+                 : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3])
+                 : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+f"(v[0]), "+f"(v[1]), "+f"(v[2]), "+f"(v[3])
+                 :
+                 : "memory");
+  } else if constexpr (C == 8) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3]), "=f"(v[4]), "=f"(v[5]),
+                   "=f"(v[6]), "=f"(v[7])
+                 : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+f"(v[0]), "+f"(v[1]), "+f"(v[2]), "+f"(v[3]), "+f"(v[4]), "+f"(v[5]),
+                   "+f"(v[6]), "+f"(v[7])
+                 :
+                 : "memory");
+  } else {
+    tmem_ld16f(taddr, v);
+    tmem_wait_ld_bind16(v);
+  }
+}
+
+// 4, 8 or 16 consecutive 32-bit columns of this thread's lane stored, and
+// waited for.
+template <int C>
+__device__ __forceinline__ void tmem_store_small(uint32_t taddr, const float* v) {
+  static_assert(C == 4 || C == 8 || C == 16, "4, 8 or 16 columns");
+  if constexpr (C == 4) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1,%2,%3,%4};" ::"r"(taddr),
+                 "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])),
+                 "r"(__float_as_uint(v[2])), "r"(__float_as_uint(v[3]))
+                 : "memory");
+  } else if constexpr (C == 8) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(
+                     taddr),
+                 "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])),
+                 "r"(__float_as_uint(v[2])), "r"(__float_as_uint(v[3])),
+                 "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+                 "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7]))
+                 : "memory");
+  } else {
+    tmem_st16f(taddr, v);
+  }
+  tmem_wait_st();
+}
+
 // 32 consecutive 32-bit columns of packed pairs into this thread's lane.
 __device__ __forceinline__ void tmem_st32u(uint32_t taddr, const uint32_t* w) {
   asm volatile(
@@ -224,6 +287,29 @@ inline bool make_cache_map(CUtensorMap* map, const void* base, int dtype, long l
                         dtype == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                           : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
                         4, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// 3-D view of a row-major [rows, head_dim] array for TMA: (64 columns, rows,
+// head_dim / 64 atoms), 128-byte swizzle.  A box of box_rows rows starting at
+// any row lands as head_dim / 64 atoms of box_rows x 128 bytes each (a
+// K-major operand with 8-row groups 1024 bytes apart and atoms box_rows x 128
+// bytes apart); rows past the end read as zero.
+inline bool make_rows_map(CUtensorMap* map, const void* base, int dtype, long long rows,
+                          int head_dim, int box_rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+  if (!fn) return false;
+  const int atoms = head_dim / 64;
+  const cuuint64_t dims[3] = {64, (cuuint64_t)rows, (cuuint64_t)atoms};
+  const cuuint64_t strides[2] = {(cuuint64_t)head_dim * 2, 128};
+  const cuuint32_t box[3] = {64, (cuuint32_t)box_rows, (cuuint32_t)atoms};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = fn(map,
+                        dtype == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                          : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                        3, const_cast<void*>(base), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
