@@ -1156,20 +1156,38 @@ def run_sweep(args, rank, world, local_rank):
                                  dtype=torch.uint8, device=dev)
                 out = torch.empty_like(case.q)
 
-                def call():
-                    pkv.paged_attn_decode(out, case.q, case.k_cache, case.v_cache,
-                                          case.block_tables, case.context_lens, case.scale,
-                                          case.max_context_len, partition_size=part, workspace=ws)
+                def call(kc=case.k_cache, vc=case.v_cache):
+                    pkv.paged_attn_decode(out, case.q, kc, vc, case.block_tables,
+                                          case.context_lens, case.scale, case.max_context_len,
+                                          partition_size=part, workspace=ws)
                 for _ in range(max(3, args.warmup)):
                     call()
                 iters = max(5, min(args.steps, 30))
                 ms = time_alone(call, flush, stream, iters)
                 nbytes = step_bytes(case)[0]
                 gbs = nbytes / (ms * 1e-3) / 1e9
+                # Back to back, as the layers of a decode step run: calls in a
+                # row over R copies of the cache (R x the K/V bytes > 3 x L2),
+                # so no call finds its data in L2 and none waits behind a flush.
+                reps = max(1, -(-(3 * 129 << 20) // int(nbytes)))
+                copies = [(case.k_cache, case.v_cache)] + [
+                    (case.k_cache.clone(), case.v_cache.clone()) for _ in range(reps - 1)]
+                ctr = [0]
+
+                def call_next():
+                    kc, vc = copies[ctr[0] % reps]
+                    ctr[0] += 1
+                    call(kc, vc)
+                for _ in range(reps + 2):
+                    call_next()
+                n_steady = max(3 * reps, iters)
+                steady_ms = timed_steps(call_next, n_steady, stream, 0.05) / n_steady
+                sgbs = nbytes / (steady_ms * 1e-3) / 1e9
                 rows.append({"block_size": B, "num_seqs": S, "ctx": ctx, "partition": part,
                              "kv_bytes": int(nbytes), "ms": round(ms, 5), "GB/s": round(gbs, 1),
-                             "frac": round(gbs / peak, 4)})
-                del case, ws, out
+                             "frac": round(gbs / peak, 4), "steady_ms": round(steady_ms, 5),
+                             "steady_frac": round(sgbs / peak, 4), "steady_copies": reps})
+                del case, ws, out, copies
                 torch.cuda.empty_cache()
     clock_rec = clocks.stop()
     if pkv.device_status(clear=True) != 0:
@@ -1183,8 +1201,11 @@ def run_sweep(args, rank, world, local_rank):
             "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": "decode sweep: 32q/8kv, D=128, bf16; value at B=16, 64 seqs, "
-                                   "ctx 8192", "l2": "flushed (256 MiB read) before every call",
-                       "launch": "queued behind a device-side wait, outside the timed region"},
+                                   "ctx 8192", "l2": "ms: flushed (256 MiB read) before every "
+                                   "call; steady_ms: calls back to back over copies of the cache "
+                                   "that together exceed 3 x L2",
+                       "launch": "ms: queued behind a device-side wait, outside the timed "
+                                 "region; steady_ms: back to back, as the layers of a step"},
             "roofline": {"bound": "hbm", "achieved": ref["GB/s"], "peak": peak, "unit": "GB/s",
                          "frac": ref["frac"], "peak_kind": peak_kind, "traffic": None},
             "sweep": rows, "clocks": clock_rec}), flush=True)

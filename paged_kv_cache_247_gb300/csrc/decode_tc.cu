@@ -100,13 +100,17 @@ struct Item {
   int s, kvh, part, ctx, t_begin, t_end, n_tiles, nparts_seq;
 };
 
-__device__ __forceinline__ Item item_at(const DecodeParams& p, int j) {
+__device__ __forceinline__ int item_seq(const DecodeParams& p, int j) {
+  return j / p.num_parts / p.num_kv_heads;
+}
+
+// The item's fields from its sequence's raw context length.
+__device__ __forceinline__ Item item_from(const DecodeParams& p, int j, int ctx) {
   Item it;
   it.part = j % p.num_parts;
   const int r = j / p.num_parts;
   it.kvh = r % p.num_kv_heads;
   it.s = r / p.num_kv_heads;
-  int ctx = __ldg(p.context_lens + it.s);
   const long long cap = min((long long)p.max_context_len,
                             (long long)p.max_blocks_per_seq * p.block_size);
   if (ctx < 0) ctx = 0;
@@ -117,6 +121,10 @@ __device__ __forceinline__ Item item_at(const DecodeParams& p, int j) {
   it.n_tiles = it.t_begin < it.t_end ? (it.t_end - it.t_begin + kKeys - 1) / kKeys : 0;
   it.nparts_seq = (ctx + p.partition_size - 1) / p.partition_size;
   return it;
+}
+
+__device__ __forceinline__ Item item_at(const DecodeParams& p, int j) {
+  return item_from(p, j, __ldg(p.context_lens + item_seq(p, j)));
 }
 
 // Reduction of a predicate over one key warpgroup (named barrier 1 + kg):
@@ -215,18 +223,28 @@ __global__ void __launch_bounds__(TcShape<NH>::kThreads, 1)
     const void* new_rows = is_k ? p.k_new : p.v_new;
     T* cache = const_cast<T*>(static_cast<const T*>(is_k ? p.k_cache : p.v_cache));
     const int B = p.block_size;
+    prefetch_tensormap(map);
+    if (is_k) prefetch_tensormap(&qmap);
     int kt = 0, k_item = 0, issued = 0, q_issued = 0;
     bool ok = true;
     for (int j = blockIdx.x; ok && j < num_items; j += gridDim.x) {
-      const Item it = item_at(p, j);
+      // The context length and the block ids of the item's first tile are
+      // loaded together (the ids speculatively, within the table row), so
+      // the item costs one memory latency before its first copy.
+      const int sj = item_seq(p, j);
+      const int32_t* trow = p.block_tables + (size_t)sj * p.max_blocks_per_seq;
+      const int lb0 = ((j % p.num_parts) * p.partition_size) / B + lane;
+      const bool in_row = lane * B < kKeys && lb0 < p.max_blocks_per_seq;
+      const int ctx_raw = __ldg(p.context_lens + sj);
+      const int first_id = in_row ? __ldg(trow + lb0) : 0;
+      const Item it = item_from(p, j, ctx_raw);
       if (it.n_tiles == 0) continue;
-      const int32_t* trow = p.block_tables + (size_t)it.s * p.max_blocks_per_seq;
       auto table_entry = [&](int i) -> int {
         const int key = it.t_begin + i * kKeys + lane * B;
         return (lane * B < kKeys && i < it.n_tiles && key < it.t_end) ? __ldg(trow + key / B)
                                                                       : 0;
       };
-      int phys_next = table_entry(0);
+      int phys_next = (it.t_begin + lane * B < it.t_end && lane * B < kKeys) ? first_id : 0;
       if (is_k) {
         const int qb = k_item & 1;
         if (k_item >= 2 && !mbar_wait_warp(&q_empty[qb], ((k_item - 2) >> 1) & 1, p.status)) {

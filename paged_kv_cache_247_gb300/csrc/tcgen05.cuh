@@ -166,6 +166,12 @@ __device__ __forceinline__ void tma_load_group(void* dst, const CUtensorMap* map
       : "memory");
 }
 
+// Fetch a tensor map (a __grid_constant__ kernel parameter) into the
+// descriptor cache ahead of its first copy.
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
 // Copy the box at coordinates (0, row, 0) of a 3-D tensor map (make_rows_map).
 __device__ __forceinline__ void tma_load_rows(void* dst, const CUtensorMap* map, int row,
                                               uint64_t* bar) {
