@@ -85,7 +85,12 @@ def source_hash(*names):
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(kernel_key, workload, sources=("decode.cu", "common.cuh", "overlap.cuh")):
+DECODE_SOURCES = ("decode.cu", "common.cuh", "overlap.cuh")
+DECODE_TC_SOURCES = ("decode_tc.cu", "decode.cu", "common.cuh", "overlap.cuh", "tcgen05.cuh")
+PREFILL_SOURCES = ("prefill.cu", "common.cuh", "tcgen05.cuh")
+
+
+def ncu_traffic(kernel_key, workload, sources=DECODE_SOURCES):
     """DRAM bytes per launch from a committed ncu summary, if it was taken on
     the current kernel source (else None)."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
@@ -650,12 +655,18 @@ def decode_record(pkv, args, workload, dev, stream, world, K, extras, rank):
                                   case.context_lens, case.scale, case.max_context_len,
                                   partition_size=args.partition, workspace=workspace)
     kernel_name += " + split reduction)" if split else ")"
+    kernel_name += ("; tensor-core kernel paged_decode_tc_kernel" if pkv.decode_uses_tensor_cores(
+        S, Hq, Hkv, D, case.max_context_len, args.partition) else "; CUDA-core kernel "
+        "paged_decode_kernel")
     # Cross-check: the same call timed alone, launch queued behind a device
     # wait so that it is outside the event pair (K/V larger than L2: no flush).
     alone_ms = time_alone(call_alone, None, stream, max(10, min(K, 50)))
     peak, peak_kind = peak_hbm()
     achieved = kernel_b / (avg_launch_ms * 1e-3) / 1e9
-    traffic = ncu_traffic(f"paged_decode_kernel:{args.path}", workload)
+    tc = pkv.decode_uses_tensor_cores(S, Hq, Hkv, D, case.max_context_len, args.partition)
+    kname = "paged_decode_tc_kernel" if tc else "paged_decode_kernel"
+    traffic = ncu_traffic(f"{kname}:{args.path}", workload,
+                          DECODE_TC_SOURCES if tc else DECODE_SOURCES)
     roofline = {"kernel": kernel_name, "bound": "hbm", "achieved": round(achieved, 2),
                 "peak": peak, "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
                 if peak_kind == "measured" else "fallback",
@@ -910,7 +921,7 @@ def run_prefill(args, rank, world, local_rank):
                      "unit": "TFLOP/s", "frac": round(tflops / peak, 4),
                      "frac_issued": round(issued / (ms * 1e-3) / 1e12 / peak, 4),
                      "traffic": ncu_traffic("paged_prefill_kernel", "prefill",
-                                            ("prefill.cu", "common.cuh")) if S == w["num_seqs"] else None},
+                                            PREFILL_SOURCES) if S == w["num_seqs"] else None},
         "e2e": {"value": round(flops / (e2e_ms * 1e-3) / 1e12 * world, 2), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": q_host.numel() * 2,
                 "d2h_bytes_per_step": out_host[0].numel() * 2, "ms_per_step": round(e2e_ms, 5),
@@ -1253,7 +1264,10 @@ def run_groups(args, rank, world, local_rank):
         gbs = nbytes / (ms * 1e-3) / 1e9
         rows.append({"group": G, "num_q_heads": Hq, "partition": part, "kv_bytes": int(nbytes),
                      "ms": round(ms, 5), "GB/s": round(gbs, 1), "frac": round(gbs / peak, 4),
-                     "traffic": ncu_traffic(f"paged_decode_kernel:g{G}", "groups")})
+                     "kernel": "paged_decode_tc_kernel" if pkv.decode_uses_tensor_cores(
+                         Sq, Hq, 8, D, case.max_context_len, part) else "paged_decode_kernel",
+                     "traffic": ncu_traffic(f"paged_decode_tc_kernel:g{G}", "groups",
+                                            DECODE_TC_SOURCES)})
         del case, ws, out
         torch.cuda.empty_cache()
     clock_rec = clocks.stop()

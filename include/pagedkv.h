@@ -103,7 +103,7 @@ int pkv_version(void);
  * h reads KV head h / G) and K_s[t] = k_cache[block_tables[s][t / B]][.][t % B].
  * Logits, softmax and the weighted sum are fp32; out is rounded to dtype
  * (round to nearest even).  On the tensor-core path (head_dim 128 and a group
- * G of 8 to 32 query heads by default, see pkv_set_decode_path) the softmax
+ * G of 2 to 32 query heads by default, see pkv_set_decode_path) the softmax
  * weights are rounded to dtype before the weighted sum, which the tensor
  * core accumulates in fp32 ([P3] "Calculate bytes per token before choosing
  * a batch": groups of query heads share one KV head, and a group of G heads
@@ -217,11 +217,12 @@ int pkv_decode_partition_size(int num_seqs, int num_q_heads, int num_kv_heads,
 
 /* Which decode kernel the decode calls use, process-wide (a tuning and test
  * control; the default suits every shape measured):
- *   0  chosen per call (default): the tensor-core kernel for head_dim 128
- *      and groups of 8 to 32 query heads, the CUDA-core kernel otherwise;
+ *   0  chosen per call (default): the tensor-core kernel where it applies
+ *      (head_dim 128, groups of 2 to 32 query heads, partition_size 0 or a
+ *      multiple of 128), the CUDA-core kernel otherwise (MHA, head_dim 64);
  *   1  always the CUDA-core kernel;
- *   2  the tensor-core kernel wherever it applies (head_dim 128, groups of 3
- *      to 32, partition_size 0 or a multiple of 128), else the CUDA-core one.
+ *   2  the tensor-core kernel wherever it applies, else the CUDA-core one
+ *      (today the same choice as 0).
  * Both compute the same attention within the stated tolerance.  It changes
  * the partition pkv_decode_partition_size and pkv_decode_workspace_size
  * report, so set it before sizing a workspace, and not while another host
@@ -229,6 +230,12 @@ int pkv_decode_partition_size(int num_seqs, int num_q_heads, int num_kv_heads,
  * values. */
 pkv_status_t pkv_set_decode_path(int path);
 int pkv_get_decode_path(void);
+
+/* 1 if a decode call with these sizes (partition_size as in
+ * pkv_paged_attn_decode) runs the tensor-core kernel under the current
+ * setting, 0 if the CUDA-core kernel, -1 for invalid arguments. */
+int pkv_decode_uses_tensor_cores(int num_seqs, int num_q_heads, int num_kv_heads,
+                                 int head_dim, int max_context_len, int partition_size);
 
 /* Workspace bytes pkv_paged_attn_decode needs for these sizes (0 when the
  * call will not split).  partition_size as in pkv_paged_attn_decode.

@@ -3,7 +3,9 @@
 Device calls (hand-written CUDA behind the C ABI of ``libpagedkv.so``):
 
 * :func:`paged_attn_decode` — single-query decode attention walking each
-  sequence's block table, with split-context partitions and GQA grouping;
+  sequence's block table, with split-context partitions and GQA grouping
+  (grouped heads of 128 on the tcgen05 tensor cores, single-head groups on
+  the CUDA cores);
 * :func:`kv_append` — scatter of each step's new K/V into its slot;
 * :func:`paged_attn_decode_append` — both in one launch (the new token is
   written to its slot and used directly);
@@ -29,5 +31,7 @@ from .ops import (  # noqa: F401
     debug_wait_timeout,
     decode_workspace_size,
     decode_partition_size,
+    decode_uses_tensor_cores,
+    set_decode_path,
 )
 from .allocator import BlockAllocator, OutOfBlocks  # noqa: F401

@@ -145,7 +145,9 @@ int auto_partition(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim
 // per SM) and take the work items (sequence, KV head, partition) in turn, so
 // a CTA's share is ceil(items / SMs) items.  The choice minimises that share
 // in 128-key tiles, counting about half a tile per item for the switch
-// between items and two tiles for the split reduction when there is one.
+// between items and four tiles for the split reduction when there is one
+// (its launch and one round trip through the workspace: about 2 us on
+// GB300, against about 0.6 us per tile for a CTA streaming alone).
 int tc_partition(int num_seqs, int num_kv_heads, int max_context_len) {
   const long long units = (long long)num_seqs * num_kv_heads;
   const long long sms = device_sms();
@@ -161,7 +163,7 @@ int tc_partition(int num_seqs, int num_kv_heads, int max_context_len) {
     const long long items = units * parts;
     // costs in half tiles
     const long long cost =
-        (items + sms - 1) / sms * (2 * per_item + 1) + (parts > 1 ? 4 : 0);
+        (items + sms - 1) / sms * (2 * per_item + 1) + (parts > 1 ? 8 : 0);
     if (best_cost < 0 || cost <= best_cost) {  // ties: the longer partition
       best_cost = cost;
       best = pt;
@@ -177,9 +179,13 @@ int g_decode_path = 0;
 
 // The decode kernel and partition size of one call.  The CUDA-core kernel
 // streams K/V through its FMA pipes; from a group of 8 query heads on, the
-// group's 2 G flops per byte exceed what those deliver at the HBM rate, and
-// the tensor-core kernel (one CTA per SM, every head of the group per CTA)
-// takes the call.
+// group's 2 G flops per byte exceed what those deliver at the HBM rate.  The
+// tensor-core kernel (persistent, one CTA per SM, every head of the group
+// per work item) leaves the threads a few instructions per key and measured
+// faster than the CUDA-core one on every grouped shape of GB300 (groups of 2
+// to 32, 8 to 256 sequences, 1k to 32k tokens, blocks of 8 to 128), so it
+// takes every grouped call it supports; single-head groups (MHA) stay on
+// the CUDA-core kernel, which reaches the HBM roofline there.
 struct DecodePlan {
   bool tc;
   int partition;
@@ -189,7 +195,7 @@ DecodePlan decode_plan(int num_seqs, int num_q_heads, int num_kv_heads, int head
                        int max_context_len, int partition_size) {
   const int group = num_q_heads / num_kv_heads;
   const int path = __atomic_load_n(&g_decode_path, __ATOMIC_RELAXED);
-  bool tc = path == 2 || (path == 0 && group >= 8);
+  bool tc = path == 2 || (path == 0 && group >= 2);
   if (tc && !pkv::decode_tc_supported(head_dim, group,
                                       partition_size ? partition_size
                                                      : pkv::kTcPartitionQuantum))
@@ -234,6 +240,15 @@ int pkv_decode_partition_size(int num_seqs, int num_q_heads, int num_kv_heads, i
   if (!decode_shape_ok(num_seqs, num_q_heads, num_kv_heads, max_context_len)) return -1;
   if (head_dim != 64 && head_dim != 128) return -1;
   return decode_plan(num_seqs, num_q_heads, num_kv_heads, head_dim, max_context_len, 0).partition;
+}
+
+int pkv_decode_uses_tensor_cores(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                 int max_context_len, int partition_size) {
+  if (!decode_shape_ok(num_seqs, num_q_heads, num_kv_heads, max_context_len)) return -1;
+  if (head_dim != 64 && head_dim != 128) return -1;
+  if (partition_size < 0 || partition_size % kPartitionQuantum) return -1;
+  return decode_plan(num_seqs, num_q_heads, num_kv_heads, head_dim, max_context_len,
+                     partition_size).tc ? 1 : 0;
 }
 
 pkv_status_t pkv_set_decode_path(int path) {

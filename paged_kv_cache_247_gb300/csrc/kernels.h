@@ -57,7 +57,7 @@ cudaError_t launch_decode_reduce(const DecodeParams& p, int dtype, int head_dim,
 
 // Grouped-head decode on the tensor cores: head size 128, groups of
 // kMinTcGroup..kMaxTcGroup query heads, partitions of whole 128-key tiles.
-constexpr int kMinTcGroup = 3;
+constexpr int kMinTcGroup = 2;
 constexpr int kMaxTcGroup = 32;
 constexpr int kTcPartitionQuantum = 128;
 bool decode_tc_supported(int head_dim, int group, int partition_size);

@@ -37,6 +37,22 @@ def decode_partition_size(num_seqs, num_q_heads, num_kv_heads, head_dim, max_con
                                                  max_context_len)
 
 
+def decode_uses_tensor_cores(num_seqs, num_q_heads, num_kv_heads, head_dim, max_context_len,
+                             partition_size=0):
+    """Whether a decode call of these sizes runs the tensor-core kernel."""
+    r = _lib.load().pkv_decode_uses_tensor_cores(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                                 max_context_len, partition_size)
+    if r < 0:
+        raise ValueError("invalid decode sizes")
+    return bool(r)
+
+
+def set_decode_path(path):
+    """Process-wide decode kernel choice: 0 = library's choice, 1 = CUDA cores,
+    2 = tensor cores where supported."""
+    _lib.check(_lib.load().pkv_set_decode_path(int(path)), "pkv_set_decode_path")
+
+
 def decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim, max_context_len,
                           partition_size=0):
     """Bytes of scratch :func:`paged_attn_decode` needs (0 when it does not split)."""

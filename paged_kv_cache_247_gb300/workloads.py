@@ -190,7 +190,8 @@ def gqa_4k_decode(device="cpu", poison=False, num_seqs=None):
     w = GQA_4K
     n = w["num_seqs"] if num_seqs is None else num_seqs
     lens = np.full(n, w["ctx"], dtype=np.int64)
-    pool = max(w["pool_blocks"], n * w["ctx"] // w["block_size"])
+    # the workload's pool, in proportion when fewer sequences are asked for
+    pool = max(w["pool_blocks"] * n // w["num_seqs"], n * w["ctx"] // w["block_size"])
     return make_decode_case(w["seed"], n, w["num_q_heads"], w["num_kv_heads"],
                             w["head_dim"], w["block_size"], w["dtype"], lens,
                             pool_blocks=pool, poison=poison, device=device)

@@ -83,26 +83,55 @@ def test_workspace_size_arithmetic(lib):
 
 
 def test_auto_partition_policy(lib):
-    """Library choice (assumes a GB300: 152 SMs, 3 CTAs each, without a device)."""
+    """The CUDA-core kernel's choice (assumes a GB300 without a device: 152
+    SMs, 3 CTAs each)."""
     part = lib.pkv_decode_partition_size
-    assert part(8, 32, 8, 128, 100) == 128          # short context: one partition
     assert part(64, 40, 40, 128, 2048) == 2048      # 2560 units: enough CTAs unsplit
-    assert part(256, 32, 8, 128, 4096) == 2048      # long contexts: 2048-token partitions
-    # 64 or 128 units: the fewest whole waves of CTAs (within 5 % below k x 456)
-    assert part(8, 32, 8, 128, 8192) == 1184        # 7 parts: 448 CTAs, one wave
-    assert part(16, 32, 8, 128, 8192) == 1184       # 7 parts: 896 CTAs, two waves
-    assert part(8, 32, 8, 128, 32768) == 1568       # 21 parts: 1344 CTAs, three waves
-    assert part(16, 32, 8, 128, 16384) == 1184      # 14 parts: 1792 CTAs, four waves
-    assert part(32, 32, 8, 128, 4096) == 1024       # no whole-wave split: ~four waves
-    assert part(128, 32, 8, 128, 2048) == 1024      # 1024 units: two partitions
-    assert part(8, 32, 8, 128, 1024) == 256         # 64 units: split finer to fill the GPU
-    assert part(64, 32, 8, 128, 1024) == 1024       # 512 units: not worth splitting 1k
+    assert lib.pkv_set_decode_path(1) == 0
+    try:
+        assert part(8, 32, 8, 128, 100) == 128          # short context: one partition
+        assert part(256, 32, 8, 128, 4096) == 2048      # long contexts: 2048-token partitions
+        # 64 or 128 units: the fewest whole waves of CTAs (within 5 % below k x 456)
+        assert part(8, 32, 8, 128, 8192) == 1184        # 7 parts: 448 CTAs, one wave
+        assert part(16, 32, 8, 128, 8192) == 1184       # 7 parts: 896 CTAs, two waves
+        assert part(8, 32, 8, 128, 32768) == 1568       # 21 parts: 1344 CTAs, three waves
+        assert part(16, 32, 8, 128, 16384) == 1184      # 14 parts: 1792 CTAs, four waves
+        assert part(32, 32, 8, 128, 4096) == 1024       # no whole-wave split: ~four waves
+        assert part(128, 32, 8, 128, 2048) == 1024      # 1024 units: two partitions
+        assert part(8, 32, 8, 128, 1024) == 256         # 64 units: split finer to fill the GPU
+        assert part(64, 32, 8, 128, 1024) == 1024       # 512 units: not worth splitting 1k
+    finally:
+        lib.pkv_set_decode_path(0)
     for args in [(1, 1, 1, 64, 5), (3, 12, 4, 64, 100000), (200, 64, 8, 128, 777)]:
         p = part(*args)
         assert p > 0 and p % 32 == 0
         ws = lib.pkv_decode_workspace_size(*args, 0)
         parts = -(-args[4] // p)
         assert ws == (0 if parts <= 1 else args[0] * args[1] * parts * (args[3] + 2) * 4)
+
+
+def test_tensor_core_partition_policy(lib):
+    """The tensor-core kernel's choice (grouped heads, head_dim 128): whole
+    128-key tiles, minimising a CTA's share of the work items in half tiles
+    (2 per tile, 1 per item, 8 for a split reduction), 152 SMs assumed."""
+    part = lib.pkv_decode_partition_size
+
+    def share(S, hkv, ctx, pt):
+        tiles = -(-ctx // 128)
+        parts = -(-tiles // pt)
+        items = S * hkv * parts
+        return -(-items // 152) * (2 * min(tiles, pt) + 1) + (8 if parts > 1 else 0)
+
+    for S, ctx, want in [(8, 100, 128), (8, 1024, 1024), (64, 1024, 1024), (8, 8192, 1280),
+                         (64, 8192, 1664), (8, 32768, 2048), (256, 4096, 2048)]:
+        p = part(S, 32, 8, 128, ctx)
+        assert p == want, (S, ctx, p)
+        tiles = -(-ctx // 128)
+        costs = [share(S, 8, ctx, pt) for pt in range(1, min(16, tiles) + 1)]
+        assert share(S, 8, ctx, p // 128) == min(costs)
+    # groups of 2 to 32 share the policy; single-head groups do not
+    assert part(8, 16, 8, 128, 8192) == part(8, 256, 8, 128, 8192) == 1280
+    assert part(8, 8, 8, 128, 8192) % 128 != 0
 
 
 def test_auto_partition_properties(lib):
@@ -192,8 +221,8 @@ def test_decode_path_switch(lib):
         assert lib.pkv_decode_partition_size(8, 256, 8, 128, 32768) % 128 == 0
         assert lib.pkv_set_decode_path(2) == 0
         assert lib.pkv_decode_partition_size(8, 32, 8, 128, 8192) % 128 == 0
-        # head_dim 64 and a group of 2 stay on the CUDA-core kernel
-        for args in ((8, 16, 8, 128, 8192), (8, 64, 8, 64, 8192)):
+        # head_dim 64 and single-head groups stay on the CUDA-core kernel
+        for args in ((8, 8, 8, 128, 8192), (8, 64, 8, 64, 8192)):
             assert lib.pkv_decode_partition_size(*args) % 32 == 0
         assert lib.pkv_set_decode_path(1) == 0
         assert lib.pkv_get_decode_path() == 1

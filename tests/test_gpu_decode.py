@@ -3,7 +3,9 @@
 Every case runs the CUDA kernels through the C ABI and compares with the
 oracle on the same seeded inputs: element by element on small cases (several
 32-token stages, ragged tails, NaN-poisoned unused slots and blocks) and on
-sampled (sequence, head) outputs at the full workload sizes."""
+sampled (sequence, head) outputs at the full workload sizes.  Each case runs
+with the library's default kernel choice and with the CUDA-core kernel
+forced, so both decode kernels are checked on every shape."""
 
 import numpy as np
 import pytest
@@ -16,10 +18,14 @@ from _gpu_util import TOL, assert_within_tol, oracle_decode
 pytestmark = pytest.mark.gpu
 
 
-@pytest.fixture(autouse=True)
-def _clean_status(lib, cuda_device):
+@pytest.fixture(autouse=True, params=[0, 1], ids=["default-path", "cuda-cores"])
+def _clean_status(request, lib, cuda_device):
+    """Every case runs twice: with the library's choice of kernel (grouped
+    heads of 128 on the tensor cores) and with the CUDA-core kernel forced."""
+    assert lib.pkv_set_decode_path(request.param) == 0
     pkv.device_status(clear=True)
     yield
+    lib.pkv_set_decode_path(0)
     assert pkv.device_status(clear=True) == 0, "kernel raised a device status flag"
 
 

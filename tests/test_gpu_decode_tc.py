@@ -45,8 +45,8 @@ LENS = [1, 2, 15, 16, 17, 127, 128, 129, 255, 256, 257, 700, 1500]
 
 
 @pytest.mark.parametrize("dtype", ["fp16", "bf16"])
-@pytest.mark.parametrize("hq,hkv", [(12, 4), (16, 4), (24, 4), (16, 2), (48, 4), (32, 2),
-                                    (40, 2), (64, 2), (32, 1)])
+@pytest.mark.parametrize("hq,hkv", [(16, 8), (12, 4), (16, 4), (24, 4), (16, 2), (48, 4),
+                                    (32, 2), (40, 2), (64, 2), (32, 1)])
 def test_groups_ragged(cuda_device, dtype, hq, hkv):
     case = W.make_decode_case(hq * 13 + hkv, len(LENS), hq, hkv, 128, 16, dtype, LENS,
                               pool_factor=1.4, poison=True, device=cuda_device)
@@ -152,16 +152,16 @@ def test_long_contexts_sampled(cuda_device, group):
     torch.cuda.empty_cache()
 
 
-def test_default_path_takes_groups_of_eight(lib, cuda_device):
-    """By default groups of 8 or more go to the tensor-core kernel (its
-    partitions are whole 128-key tiles) and smaller groups to the CUDA-core
-    kernel; both agree with the oracle."""
+def test_default_path_takes_grouped_heads(lib, cuda_device):
+    """By default grouped heads go to the tensor-core kernel (its partitions
+    are whole 128-key tiles) and single-head groups to the CUDA-core kernel;
+    both agree with the oracle."""
     lib.pkv_set_decode_path(0)
     assert lib.pkv_get_decode_path() == 0
     for hq, hkv in ((64, 8), (32, 8), (8, 8)):
         part = pkv.decode_partition_size(8, hq, hkv, 128, 8192)
         assert part > 0 and part % 32 == 0
-        if hq // hkv >= 8:
+        if hq // hkv >= 2:
             assert part % 128 == 0
         lens = [8192, 100, 5000, 7777, 1, 4096, 3000, 8000]
         case = W.make_decode_case(hq + 1, 8, hq, hkv, 128, 16, "bf16", lens, pool_factor=1.1,
