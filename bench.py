@@ -206,6 +206,9 @@ def step_bytes(case):
 
 
 def contiguous_baseline(pkv, case, out, part, dev, stream, iters):
+    """Paged vs contiguous decode on the same tokens, both on the CUDA-core
+    kernel (the contiguous layout has only that one), at the same partition:
+    the ratio of the two times is the cost of the indirection."""
     S, Hq, D = case.q.shape
     Hkv, B = case.k_cache.shape[1], case.block_size
     cap = case.max_context_len
@@ -225,9 +228,14 @@ def contiguous_baseline(pkv, case, out, part, dev, stream, iters):
             fn()
         return timed_steps(fn, iters, stream, 0.05) / iters
 
-    t_paged = timed(lambda: pkv.paged_attn_decode(
-        out, case.q, case.k_cache, case.v_cache, case.block_tables, case.context_lens,
-        case.scale, cap, partition_size=part, workspace=ws))
+    path = pkv.load_library().pkv_get_decode_path()
+    pkv.set_decode_path(1)
+    try:
+        t_paged = timed(lambda: pkv.paged_attn_decode(
+            out, case.q, case.k_cache, case.v_cache, case.block_tables, case.context_lens,
+            case.scale, cap, partition_size=part, workspace=ws))
+    finally:
+        pkv.set_decode_path(path)
     t_contig = timed(lambda: pkv.contiguous_attn_decode(
         out, case.q, kc, vc, case.context_lens, case.scale, partition_size=part, workspace=ws))
     reserved = kc.numel() * kc.element_size() * 2
@@ -237,7 +245,7 @@ def contiguous_baseline(pkv, case, out, part, dev, stream, iters):
     return {"paged_decode_ms": round(t_paged, 5), "contiguous_decode_ms": round(t_contig, 5),
             "indirection_overhead_pct": round(100.0 * (t_paged / t_contig - 1.0), 2),
             "contiguous_reserved_bytes": reserved, "paged_held_bytes": held,
-            "partition_size": part, "iters": iters}
+            "partition_size": part, "iters": iters, "kernel": "CUDA-core decode kernel, both"}
 
 
 def time_alone(fn, flush, stream, iters):

@@ -261,8 +261,11 @@ size_t pkv_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads
  *                 sequence s holds its positions t < context_lens[s] at
  *                 [s][h][t][:]; capacity is the reservation per sequence
  *   context_lens  int32 [num_seqs], each in [0, capacity]
- * Other arguments, results, workspace and errors as pkv_paged_attn_decode
- * (with max_context_len = capacity).
+ * It runs the CUDA-core decode kernel (and its partition choice) whatever
+ * pkv_set_decode_path says, so it is the contiguous twin of
+ * pkv_paged_attn_decode under setting 1; the workspace it needs is
+ * pkv_contiguous_workspace_size.  Other arguments, results and errors as
+ * pkv_paged_attn_decode (with max_context_len = capacity).
  * ---------------------------------------------------------------------- */
 pkv_status_t pkv_contiguous_attn_decode(
     void* out, const void* q, const void* k_cache, const void* v_cache,
@@ -270,6 +273,11 @@ pkv_status_t pkv_contiguous_attn_decode(
     int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
     float scale, pkv_dtype_t dtype, int partition_size,
     void* workspace, size_t workspace_bytes, pkv_stream_t stream);
+
+/* Workspace bytes pkv_contiguous_attn_decode needs (0 when it will not
+ * split); (size_t)-1 for invalid arguments. */
+size_t pkv_contiguous_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads,
+                                     int head_dim, int capacity, int partition_size);
 
 /* ------------------------------------------------------------------------
  * Multi-query (chunked prompt) attention over the paged cache.

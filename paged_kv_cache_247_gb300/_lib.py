@@ -59,6 +59,7 @@ SIGNATURES = {
     "pkv_get_decode_path": (c_int, []),
     "pkv_decode_uses_tensor_cores": (c_int, [c_int, c_int, c_int, c_int, c_int, c_int]),
     "pkv_decode_workspace_size": (c_size_t, [c_int, c_int, c_int, c_int, c_int, c_int]),
+    "pkv_contiguous_workspace_size": (c_size_t, [c_int, c_int, c_int, c_int, c_int, c_int]),
     "pkv_kv_append": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int,
                               c_int, c_int, c_int, c_int, c_void_p]),
     "pkv_block_copy": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_int, c_size_t, c_void_p]),

@@ -242,6 +242,19 @@ int pkv_decode_partition_size(int num_seqs, int num_q_heads, int num_kv_heads, i
   return decode_plan(num_seqs, num_q_heads, num_kv_heads, head_dim, max_context_len, 0).partition;
 }
 
+size_t pkv_contiguous_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads,
+                                     int head_dim, int capacity, int partition_size) {
+  if (!decode_shape_ok(num_seqs, num_q_heads, num_kv_heads, capacity)) return (size_t)-1;
+  if (head_dim != 64 && head_dim != 128) return (size_t)-1;
+  if (partition_size < 0 || partition_size % kPartitionQuantum) return (size_t)-1;
+  const int part = partition_size ? partition_size
+                                  : auto_partition(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                                   capacity);
+  const long long parts = num_parts_for(capacity, part);
+  if (parts <= 1) return 0;
+  return (size_t)num_seqs * num_q_heads * parts * (head_dim + 2) * sizeof(float);
+}
+
 int pkv_decode_uses_tensor_cores(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
                                  int max_context_len, int partition_size) {
   if (!decode_shape_ok(num_seqs, num_q_heads, num_kv_heads, max_context_len)) return -1;

@@ -177,7 +177,8 @@ def paged_attn_prefill(out, q, query_start, k_cache, v_cache, block_tables, cont
 def contiguous_attn_decode(out, q, k_cache, v_cache, context_lens, scale, partition_size=0,
                            workspace=None):
     """Decode over a contiguous cache ``[S, Hkv, capacity, D]`` (no block
-    table): the baseline the paged layout is compared with."""
+    table): the baseline the paged layout is compared with.  It runs the
+    CUDA-core decode kernel, whatever the decode-path setting."""
     _cuda(q, "q", ndim=3)
     dtype = q.dtype
     if dtype not in _DTYPE_CODE:
@@ -191,7 +192,9 @@ def contiguous_attn_decode(out, q, k_cache, v_cache, context_lens, scale, partit
     if v_cache.shape != k_cache.shape or D2 != D or S2 != S or out.shape != q.shape:
         raise ValueError("shape mismatch between q, out and the caches")
     lib = _lib.load()
-    ws_bytes = decode_workspace_size(S, Hq, Hkv, D, cap, partition_size)
+    ws_bytes = lib.pkv_contiguous_workspace_size(S, Hq, Hkv, D, cap, partition_size)
+    if ws_bytes == _SIZE_T_MAX:
+        raise ValueError("invalid decode sizes")
     ws_ptr, ws_len = None, 0
     if ws_bytes:
         if workspace is None:

@@ -39,8 +39,12 @@ def contiguous_from_paged(case, capacity):
 
 @pytest.fixture(autouse=True)
 def _clean_status(lib, cuda_device):
+    """The contiguous call runs the CUDA-core kernel; the paged calls it is
+    compared with bit for bit run the same kernel (setting 1)."""
     pkv.device_status(clear=True)
+    assert lib.pkv_set_decode_path(1) == 0
     yield
+    lib.pkv_set_decode_path(0)
     assert pkv.device_status(clear=True) == 0
 
 
