@@ -818,6 +818,23 @@ def run_ours(args, rank, world, local_rank):
         # The grouped-query workload is the second shape the target names; it
         # is measured the same way and reported beside the headline.
         line["gqa4k"] = decode_record(pkv, args, "gqa4k", dev, stream, world, K, False, rank)
+        # The other configurations, each in its own (shorter) form, so that
+        # one default run measures every one of them: the decode sweep at
+        # blocks of 16 (batches 8 and 64, contexts 1k, 8k, 32k), the
+        # shared-prompt serving step, and chunked prefill on the tensor cores.
+        sw = sweep_line(args, rank, world, local_rank, block_sizes=(16,))
+        line["sweep_b16"] = {"rows": sw["sweep"], "l2": sw["config"]["l2"],
+                             "clocks": sw["clocks"]}
+        sh = shared_line(args, rank, world, local_rank)
+        line["shared_prefix"] = {k: sh[k] for k in (
+            "value", "unit", "ms_per_step", "steps_per_s", "steps", "device_ms_per_step",
+            "kernel_ms_last_step", "logical_gbs_kernel", "allocator_us_per_step", "first_step",
+            "held_kv_bytes", "logical_kv_bytes_per_step", "config", "clocks")}
+        pf = prefill_line(args, rank, world, local_rank, with_cpu=False)
+        line["prefill"] = {k: pf[k] for k in (
+            "metric", "value", "unit", "ms_per_step", "config", "roofline", "e2e", "clocks")}
+        line["gpu_launches_note"] = ("gpu_launches counts the headline step's timed region; "
+                                     "each sub-record times its own")
     if rank == 0:
         print(json.dumps(line), flush=True)
 
@@ -833,6 +850,13 @@ def prefill_flops(lens, chunks, num_q_heads, head_dim):
 
 
 def run_prefill(args, rank, world, local_rank):
+    line = prefill_line(args, rank, world, local_rank)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def prefill_line(args, rank, world, local_rank, with_cpu=True):
+    """The chunked-prefill record (TFLOP/s of the causal attention)."""
     import paged_kv_cache_247_gb300 as pkv
     from paged_kv_cache_247_gb300 import build as _build
     from paged_kv_cache_247_gb300 import workloads as W
@@ -939,7 +963,7 @@ def run_prefill(args, rank, world, local_rank):
                 "serial_value": round(flops / (e2e_serial_ms * 1e-3) / 1e12 * world, 2)},
         "gpu_launches": K, "clocks": clock_rec,
     }
-    if rank == 0 and world == 1:
+    if with_cpu and rank == 0 and world == 1:
         import oracle
         n_q = 8
         tables = case.block_tables.cpu().numpy()
@@ -956,11 +980,18 @@ def run_prefill(args, rank, world, local_rank):
         line["cpu_baseline"] = {"value": round(f_sample / secs / 1e12, 6), "unit": "TFLOP/s",
                                 "cores": cores_used(), "kind": "oracle",
                                 "sample": f"the last {n_q} queries of one sequence, {secs:.2f} s"}
+    del case, q, qs, out, q_host, out_host, q_dev, outs
+    torch.cuda.empty_cache()
+    return line
+
+
+def run_shared(args, rank, world, local_rank):
+    line = shared_line(args, rank, world, local_rank)
     if rank == 0:
         print(json.dumps(line), flush=True)
 
 
-def run_shared(args, rank, world, local_rank):
+def shared_line(args, rank, world, local_rank):
     """Parallel sampling with shared prompts (16 prompts x 8 samples): each
     timed step is the whole serving step - the native allocator's next slots
     and copy-on-write pairs and the block tables on the host, one staged copy
@@ -1109,8 +1140,7 @@ def run_shared(args, rank, world, local_rank):
     st = alloc.stats()
     held = st["used_blocks"] * B * 2 * H * D * e
     logical_gbs = stats["logical_bytes"] / elapsed / 1e9
-    if rank == 0:
-        print(json.dumps({
+    line = {
             "metric": "parallel-sampling serving step: logical K/V GB/s attended (whole step, "
                       "allocator on the host included)",
             "value": round(logical_gbs * world, 1), "unit": "GB/s", "n_gpus": world, "steps": K,
@@ -1135,11 +1165,20 @@ def run_shared(args, rank, world, local_rank):
             "pool": {k: st[k] for k in st},
             "held_kv_bytes": held,
             "logical_kv_bytes_per_step": int(stats["logical_bytes"] / K),
-            "clocks": clock_rec}), flush=True)
+            "clocks": clock_rec}
     alloc.close()
+    del kc, vc, ws, out, stage_d
+    torch.cuda.empty_cache()
+    return line
 
 
 def run_sweep(args, rank, world, local_rank):
+    line = sweep_line(args, rank, world, local_rank)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def sweep_line(args, rank, world, local_rank, block_sizes=None):
     """Decode over the block-size / batch / context grid: each call timed
     alone with CUDA events after reading 256 MiB (small cases fit in L2),
     algorithmic bytes / time against the HBM peak."""
@@ -1161,7 +1200,7 @@ def run_sweep(args, rank, world, local_rank):
     clocks = ClockSampler(dev.index if dev.index is not None else 0)
     clocks.start()
     only = tuple(int(x) for x in args.only.split(",")) if args.only else None
-    for B in sw["block_sizes"]:
+    for B in (block_sizes or sw["block_sizes"]):
         for S in sw["batches"]:
             for ctx in sw["ctxs"]:
                 if only is not None and (B, S, ctx) != only:
@@ -1213,8 +1252,7 @@ def run_sweep(args, rank, world, local_rank):
         raise RuntimeError("device status flags during the sweep")
     ref = next((r for r in rows if r["block_size"] == 16 and r["num_seqs"] == 64
                 and r["ctx"] == 8192), rows[-1])
-    if rank == 0:
-        print(json.dumps({
+    return {
             "metric": "paged decode attention HBM GB/s across block sizes, batches and contexts",
             "value": ref["GB/s"], "unit": "GB/s", "n_gpus": world, "steps": iters,
             "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
@@ -1227,7 +1265,7 @@ def run_sweep(args, rank, world, local_rank):
                                  "region; steady_ms: back to back, as the layers of a step"},
             "roofline": {"bound": "hbm", "achieved": ref["GB/s"], "peak": peak, "unit": "GB/s",
                          "frac": ref["frac"], "peak_kind": peak_kind, "traffic": None},
-            "sweep": rows, "clocks": clock_rec}), flush=True)
+            "sweep": rows, "clocks": clock_rec}
 
 
 def run_groups(args, rank, world, local_rank):
