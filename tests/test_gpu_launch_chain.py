@@ -28,10 +28,14 @@ from _gpu_util import assert_within_tol, to_f64
 pytestmark = pytest.mark.gpu
 
 
-@pytest.fixture(autouse=True)
-def _clean_status(lib, cuda_device):
+@pytest.fixture(autouse=True, params=[0, 1], ids=["default-path", "cuda-cores"])
+def _clean_status(request, lib, cuda_device):
+    """Both decode kernels: the library's choice (grouped heads of 128 on the
+    tensor cores) and the CUDA-core one."""
+    assert lib.pkv_set_decode_path(request.param) == 0
     pkv.device_status(clear=True)
     yield
+    lib.pkv_set_decode_path(0)
     assert pkv.device_status(clear=True) == 0
 
 
