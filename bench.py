@@ -55,6 +55,8 @@ def parse_args():
     ap.add_argument("--only", default=None,
                     help="--workload sweep: one case as block_size,batch,ctx (for profiler "
                          "captures)")
+    ap.add_argument("--head-dim", type=int, default=128, choices=[64, 128],
+                    help="--workload groups: head size")
     ap.add_argument("--group", type=int, default=0,
                     help="one query-head group size for --workload groups (0 = all)")
     ap.add_argument("--partition", type=int, default=0, help="tokens per partition (0 = library)")
@@ -1291,7 +1293,8 @@ def run_groups(args, rank, world, local_rank):
     clocks = ClockSampler(dev.index if dev.index is not None else 0)
     clocks.start()
     for G in groups:
-        case = W.make_decode_case(6, S, 8 * G, 8, 128, 16, "bf16", [4096] * S, device=dev)
+        case = W.make_decode_case(6, S, 8 * G, 8, args.head_dim, 16, "bf16", [4096] * S,
+                                  device=dev)
         Sq, Hq, D = case.q.shape
         part = args.partition or pkv.decode_partition_size(Sq, Hq, 8, D, case.max_context_len)
         ws = torch.empty(max(16, pkv.decode_workspace_size(Sq, Hq, 8, D, case.max_context_len,
@@ -1325,7 +1328,7 @@ def run_groups(args, rank, world, local_rank):
             "value": rows[-1]["GB/s"], "unit": "GB/s", "n_gpus": world, "steps": iters,
             "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": f"decode, {S} seqs x 4096 tokens, 8 KV heads of 128, bf16, "
+            "config": {"workload": f"decode, {S} seqs x 4096 tokens, 8 KV heads of {args.head_dim}, bf16, "
                                    f"B=16, query heads 8 x group", "l2": "flushed (256 MiB read) "
                                    "before every call",
                        "launch": "queued behind a device-side wait, outside the timed region"},

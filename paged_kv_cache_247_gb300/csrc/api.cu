@@ -364,7 +364,7 @@ pkv_status_t paged_decode_impl(void* out, const void* q, const void* k_new, cons
   if (err != cudaSuccess) return cuda_fail(err);
   if (plan.tc) {
     bool unsupported = false;
-    err = pkv::launch_paged_decode_tc(p, dtype, device_sms(),
+    err = pkv::launch_paged_decode_tc(p, dtype, head_dim, device_sms(),
                                       reinterpret_cast<cudaStream_t>(stream), &unsupported);
     if (unsupported) return PKV_ERR_UNSUPPORTED;
   } else {

@@ -59,18 +59,24 @@ namespace {
 
 using namespace tc;
 
-constexpr int kD = 128;                 // head size of this path
-constexpr int kKeys = kTileKeys;        // keys per tile: M of S^T, K of O^T
-constexpr int kGroupKV = (kD / 64) * 1024;   // bytes between 8-row groups of a K/V tile
-constexpr int kKvTile = (kKeys / 8) * kGroupKV;
+constexpr int kKeys = kTileKeys;        // keys per tile: M of S^T, K of the P.V product
 constexpr int kGroupP = (kKeys / 64) * 1024; // bytes between 8-head groups of P^T
 constexpr int kBarSlots = 32;
 constexpr int kStages = 3;              // K ring and V ring depth
 
-// NH: the group rounded up to a power of two (4 .. 32).
-template <int NH>
+constexpr int pow2_at_least(int x, int p = 32) { return p >= x ? p : pow2_at_least(x, 2 * p); }
+
+// NH: the group rounded up to a power of two (4 .. 32); D: head size (64 or
+// 128).  For D = 128 the P.V product is O^T [D x N] = V^T P^T (M = D); for
+// D = 64, where an M of 64 would be needed, it is O [128 x D] = P V with the
+// heads on M (rows past the group unused) and P^T read as the K-major A
+// operand.
+template <int NH, int D>
 struct TcShape {
-  static constexpr int N = NH < 16 ? 16 : NH;  // MMA N
+  static constexpr bool kTrans = D == 128;     // O^T (M = D) or O (M = 128 heads)
+  static constexpr int kGroupKV = (D / 64) * 1024;  // bytes between 8-row groups of a K/V tile
+  static constexpr int kKvTile = (kKeys / 8) * kGroupKV;
+  static constexpr int N = NH < 16 ? 16 : NH;  // MMA N of S^T
   static constexpr int KG = NH > 16 ? 2 : 1;   // key warpgroups
   static constexpr int NHW = NH / KG;          // heads per key warpgroup
   static constexpr int kKeyThreads = 128 * KG;
@@ -79,8 +85,10 @@ struct TcShape {
   static constexpr int kSWarp = kKWarp + 2;    // S^T issuer, owns tensor memory
   static constexpr int kOWarp = kKWarp + 3;    // O^T issuer
   static constexpr int kThreads = kKeyThreads + 4 * 32;
-  static constexpr int kQBytes = N * 256;      // two 64-column atoms of N rows
-  static constexpr int kPBuf = (N / 8) * kGroupP;
+  static constexpr int kQBytes = N * D * 2;    // D / 64 atoms of N rows x 128 bytes
+  static constexpr int kPRows = kTrans ? N : 128;
+  static constexpr int kPBuf = (kPRows / 8) * kGroupP;
+  static constexpr int kOCols = kTrans ? N : D;  // tensor-memory columns of one O buffer
   static constexpr int kQ = 2 * kStages * kKvTile;  // after the K and V rings
   static constexpr int kP = kQ + 2 * kQBytes;
   static constexpr int kRed = kP + 2 * kPBuf;       // [KG][4 warps][NHW] floats
@@ -90,8 +98,8 @@ struct TcShape {
   static constexpr int kBytes = kTmemSlot + 16 + 1024;  // + alignment slack
   static_assert(kBytes <= 227 * 1024, "shared memory overflow");
   static constexpr int kColO = 2 * N;                   // S^T buffers first
-  static constexpr int kTmemCols = 4 * N <= 64 ? 64 : 128;
-  static_assert(4 * N <= kTmemCols, "tensor memory overflow");
+  static constexpr int kTmemCols = pow2_at_least(2 * N + 2 * kOCols);
+  static_assert(kTmemCols <= 512, "tensor memory overflow");
 };
 
 // One work item: sequence s, KV head, partition [t_begin, t_end) of the
@@ -142,15 +150,17 @@ __device__ __forceinline__ bool group_any(int kg, bool v) {
 
 __device__ __forceinline__ void group_sync(int kg) { named_barrier_sync(1 + kg, 128); }
 
-template <typename T, int NH>
-__global__ void __launch_bounds__(TcShape<NH>::kThreads, 1)
+template <typename T, int NH, int D>
+__global__ void __launch_bounds__(TcShape<NH, D>::kThreads, 1)
     paged_decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap kmap,
                            const __grid_constant__ CUtensorMap vmap,
                            const __grid_constant__ CUtensorMap qmap, int num_items) {
-  using L = TcShape<NH>;
+  using L = TcShape<NH, D>;
   constexpr int N = L::N;
   constexpr int S = kStages;
   constexpr int NHW = L::NHW;
+  constexpr int kGroupKV = L::kGroupKV;
+  constexpr int kKvTile = L::kKvTile;
   grid_dep_wait();
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
@@ -260,14 +270,15 @@ __global__ void __launch_bounds__(TcShape<NH>::kThreads, 1)
         q_issued = k_item + 1;
       }
       // Fused append: the step's new token is position ctx - 1 of the last
-      // partition; its row (16 chunks of 16 bytes, lanes 0-15) is written to
-      // its cache slot before the copy of the tile that holds it.
+      // partition; its row (D / 8 chunks of 16 bytes, one per lane) is written
+      // to its cache slot before the copy of the tile that holds it.
+      constexpr int kRowChunks = D / 8;
       const bool fused_here = new_rows != nullptr && it.t_end == it.ctx;
       uint4 new_chunk = make_uint4(0, 0, 0, 0);
-      if (fused_here && lane < 16)
+      if (fused_here && lane < kRowChunks)
         new_chunk = reinterpret_cast<const uint4*>(
             static_cast<const T*>(new_rows) +
-            ((size_t)it.s * p.num_kv_heads + it.kvh) * kD)[lane];
+            ((size_t)it.s * p.num_kv_heads + it.kvh) * D)[lane];
       for (int i = 0; i < it.n_tiles; ++i, ++kt) {
         const int st = kt % S;
         const int key0 = it.t_begin + i * kKeys;
@@ -282,9 +293,9 @@ __global__ void __launch_bounds__(TcShape<NH>::kThreads, 1)
         if (fused_here && key0 + nvalid == it.ctx) {
           const int pos = it.ctx - 1;
           const int phys_new = __shfl_sync(0xffffffffu, phys, (pos - key0) / B);
-          if (lane < 16) {
+          if (lane < kRowChunks) {
             const size_t dst =
-                (((size_t)phys_new * p.num_kv_heads + it.kvh) * B + (pos % B)) * kD;
+                (((size_t)phys_new * p.num_kv_heads + it.kvh) * B + (pos % B)) * D;
             reinterpret_cast<uint4*>(cache + dst)[lane] = new_chunk;
           }
           // the row must be visible to the copy engine's read below
@@ -295,7 +306,7 @@ __global__ void __launch_bounds__(TcShape<NH>::kThreads, 1)
           ok = false;
           break;
         }
-        if (lane == 0) mbar_arrive_expect_tx(&full[st], (uint32_t)nseg * B * kD * sizeof(T));
+        if (lane == 0) mbar_arrive_expect_tx(&full[st], (uint32_t)nseg * B * D * sizeof(T));
         __syncwarp();
         if (lane < nseg)
           tma_load_group(ring + st * kKvTile + lane * (B / 8) * kGroupKV, map,
@@ -318,7 +329,8 @@ __global__ void __launch_bounds__(TcShape<NH>::kThreads, 1)
       constexpr bool bf16 = std::is_same<T, __nv_bfloat16>::value;
       const bool is_s = warp == L::kSWarp;
       const uint32_t idesc = is_s ? instr_desc(bf16, false, false, N, kKeys)
-                                  : instr_desc(bf16, true, false, N, kD);
+                                  : (L::kTrans ? instr_desc(bf16, true, false, N, D)
+                                               : instr_desc(bf16, false, true, D, kKeys));
       const uint32_t aK = smem_addr(sK), aV = smem_addr(sV), aQ = smem_addr(sQ),
                      aP = smem_addr(sP);
       int kt = 0, k_item = 0;
@@ -340,7 +352,7 @@ __global__ void __launch_bounds__(TcShape<NH>::kThreads, 1)
             // S^T = K . Q^T: 16 dimensions per MMA; a 32-byte step inside the
             // 128-byte rows, then the next 64-column atom.
 #pragma unroll
-            for (int ks = 0; ks < kD / 16; ++ks)
+            for (int ks = 0; ks < D / 16; ++ks)
               mma_f16_ss(tmem + (kt & 1) * N,
                          smem_desc(aK + st * kKvTile + (ks / 4) * 1024 + (ks % 4) * 32, 16,
                                    kGroupKV),
@@ -361,15 +373,22 @@ __global__ void __launch_bounds__(TcShape<NH>::kThreads, 1)
               break;
             }
             tc_fence_after();
-            // O^T += V^T P^T: 16 keys per MMA, two 8-key groups of V and a
-            // 32-byte step inside P^T's 128-byte rows.
+            // O^T += V^T P^T (D = 128) or O += P V (D = 64): 16 keys per
+            // MMA, two 8-key groups of V and a 32-byte step inside P^T's
+            // 128-byte rows.
 #pragma unroll
-            for (int ks = 0; ks < kKeys / 16; ++ks)
-              mma_f16_ss(tmem + L::kColO + b * N,
-                         smem_desc(aV + st * kKvTile + ks * 2 * kGroupKV, 1024, kGroupKV),
-                         smem_desc(aP + (kt & 1) * L::kPBuf + (ks / 4) * 1024 + (ks % 4) * 32,
-                                   16, kGroupP),
-                         idesc, (i > 0 || ks > 0) ? 1u : 0u);
+            for (int ks = 0; ks < kKeys / 16; ++ks) {
+              const uint64_t dv =
+                  smem_desc(aV + st * kKvTile + ks * 2 * kGroupKV, 1024, kGroupKV);
+              const uint64_t dp = smem_desc(
+                  aP + (kt & 1) * L::kPBuf + (ks / 4) * 1024 + (ks % 4) * 32, 16, kGroupP);
+              if constexpr (L::kTrans)
+                mma_f16_ss(tmem + L::kColO + b * L::kOCols, dv, dp, idesc,
+                           (i > 0 || ks > 0) ? 1u : 0u);
+              else
+                mma_f16_ss(tmem + L::kColO + b * L::kOCols, dp, dv, idesc,
+                           (i > 0 || ks > 0) ? 1u : 0u);
+            }
             mma_commit(&p_free[kt & 1]);
             mma_commit(&v_empty[st]);
           }
@@ -390,6 +409,13 @@ __global__ void __launch_bounds__(TcShape<NH>::kThreads, 1)
     float* red = reinterpret_cast<float*>(smem + L::kRed) + kg * 4 * NHW;
     float* mref_s = reinterpret_cast<float*>(smem + L::kMref) + kg * NHW;
     const float qs = p.qscale;
+    if constexpr (!L::kTrans) {
+      // P's rows past the group are read by the P V product but never
+      // written: clear them once (the first release's proxy fence orders
+      // these stores before the tensor core reads them).
+      for (int i = threadIdx.x; i < 2 * L::kPBuf / 16; i += L::kKeyThreads)
+        reinterpret_cast<uint4*>(sP)[i] = make_uint4(0, 0, 0, 0);
+    }
     int kt = 0, k_item = 0;
     bool ok = true;
     for (int j = blockIdx.x; j < num_items; j += gridDim.x) {
@@ -401,8 +427,8 @@ __global__ void __launch_bounds__(TcShape<NH>::kThreads, 1)
       }
       if (it.n_tiles == 0) {
         if (it.ctx == 0 && it.part == 0) {  // empty context: the output is zero
-          T* o = static_cast<T*>(p.out) + ((size_t)it.s * p.num_q_heads + h0 + hb) * kD;
-          const int n = min(NHW, G - hb) * kD;
+          T* o = static_cast<T*>(p.out) + ((size_t)it.s * p.num_q_heads + h0 + hb) * D;
+          const int n = min(NHW, G - hb) * D;
           for (int i = t; i < n; i += 128) o[i] = static_cast<T>(0.f);
         }
         continue;
@@ -462,18 +488,36 @@ __global__ void __launch_bounds__(TcShape<NH>::kThreads, 1)
             for (int g = 0; g < NHW; ++g) mref_s[g] = mref[g];
           }
           if (i > 0 && moved) {
-            // O^T holds this item's tiles so far: once their MMAs are done
-            // (P^T buffer of the previous tile released), thread d rescales
-            // this warpgroup's columns of its lane.
+            // O holds this item's tiles so far: once their MMAs are done
+            // (P^T buffer of the previous tile released), rescale it.
             if (ok && !mbar_wait_warp(&p_free[(kt - 1) & 1], ((kt - 1) >> 1) & 1, p.status))
               ok = false;
             tc_fence_after();
-            const uint32_t oaddr = tmem + L::kColO + ob * N + hb + lane_base;
-            float o[NHW];
-            tmem_load_small<NHW>(oaddr, o);
+            if constexpr (L::kTrans) {
+              // O^T: thread d rescales this warpgroup's columns of its lane
+              const uint32_t oaddr = tmem + L::kColO + ob * L::kOCols + hb + lane_base;
+              float o[NHW];
+              tmem_load_small<NHW>(oaddr, o);
 #pragma unroll
-            for (int g = 0; g < NHW; ++g) o[g] *= alpha[g];
-            tmem_store_small<NHW>(oaddr, o);
+              for (int g = 0; g < NHW; ++g) o[g] *= alpha[g];
+              tmem_store_small<NHW>(oaddr, o);
+            } else {
+              // O: lane h is head h; the warpgroup that owns head h scales
+              // its D columns (the other lanes store what they read)
+              float a = 1.f;
+#pragma unroll
+              for (int g = 0; g < NHW; ++g)
+                if (t == hb + g) a = alpha[g];
+              const uint32_t oaddr = tmem + L::kColO + ob * L::kOCols + lane_base;
+#pragma unroll
+              for (int c = 0; c < D / 16; ++c) {
+                float o[16];
+                tmem_load_small<16>(oaddr + c * 16, o);
+#pragma unroll
+                for (int k = 0; k < 16; ++k) o[k] *= a;
+                tmem_store_small<16>(oaddr + c * 16, o);
+              }
+            }
             tc_fence_before();
           }
         }
@@ -500,8 +544,8 @@ __global__ void __launch_bounds__(TcShape<NH>::kThreads, 1)
           if (ok && !mbar_wait_warp(&v_full[st], (kt / S) & 1, p.status)) ok = false;
           if (!valid) {
 #pragma unroll
-            for (int c = 0; c < kD / 8; ++c)
-              *reinterpret_cast<uint4*>(sV + st * kKvTile + chunk_offset<kD>(t, c)) =
+            for (int c = 0; c < D / 8; ++c)
+              *reinterpret_cast<uint4*>(sV + st * kKvTile + chunk_offset<D>(t, c)) =
                   make_uint4(0, 0, 0, 0);
           }
         }
@@ -521,28 +565,79 @@ __global__ void __launch_bounds__(TcShape<NH>::kThreads, 1)
       const int last = kt - 1;
       if (ok && !mbar_wait_warp(&p_free[last & 1], (last >> 1) & 1, p.status)) ok = false;
       tc_fence_after();
-      float o[NHW];
-      tmem_load_small<NHW>(tmem + L::kColO + ob * N + hb + lane_base, o);
-      tc_fence_before();
-      mbar_arrive(&o_free[ob]);
-      if (ok) {
-        const int d = t;
+      if constexpr (L::kTrans) {
+        // O^T: thread d writes dimension d of this warpgroup's heads.
+        float o[NHW];
+        tmem_load_small<NHW>(tmem + L::kColO + ob * L::kOCols + hb + lane_base, o);
+        tc_fence_before();
+        mbar_arrive(&o_free[ob]);
+        if (ok) {
+          const int d = t;
 #pragma unroll
-        for (int g = 0; g < NHW; ++g) {
-          if (hb + g >= G) continue;
-          const float l = (red[g] + red[NHW + g]) + (red[2 * NHW + g] + red[3 * NHW + g]);
-          const float val = o[g] / l;
-          const size_t row = (size_t)it.s * p.num_q_heads + h0 + hb + g;
-          if (it.nparts_seq == 1) {
-            static_cast<T*>(p.out)[row * kD + d] = static_cast<T>(val);
-          } else {
-            const size_t r = row * p.num_parts + it.part;
-            p.ws_o[r * kD + d] = val;
-            if (d == 0) {
-              p.ws_m[r] = mref[g];
-              p.ws_l[r] = l;
+          for (int g = 0; g < NHW; ++g) {
+            if (hb + g >= G) continue;
+            const float l = (red[g] + red[NHW + g]) + (red[2 * NHW + g] + red[3 * NHW + g]);
+            const float val = o[g] / l;
+            const size_t row = (size_t)it.s * p.num_q_heads + h0 + hb + g;
+            if (it.nparts_seq == 1) {
+              static_cast<T*>(p.out)[row * D + d] = static_cast<T>(val);
+            } else {
+              const size_t r = row * p.num_parts + it.part;
+              p.ws_o[r * D + d] = val;
+              if (d == 0) {
+                p.ws_m[r] = mref[g];
+                p.ws_l[r] = l;
+              }
             }
           }
+        }
+      } else {
+        // O: thread h (lane h) writes the D outputs of head h if this
+        // warpgroup owns it.
+        const int g = t - hb;
+        const bool mine = g >= 0 && g < NHW && t < G;
+        float l = 1.f, m = 0.f;
+#pragma unroll
+        for (int k = 0; k < NHW; ++k)
+          if (k == g) {
+            l = (red[k] + red[NHW + k]) + (red[2 * NHW + k] + red[3 * NHW + k]);
+            m = mref[k];
+          }
+        const float inv = 1.f / l;
+        const size_t row = (size_t)it.s * p.num_q_heads + h0 + (mine ? t : 0);
+        const size_t r = row * p.num_parts + it.part;
+#pragma unroll
+        for (int c = 0; c < D / 16; ++c) {
+          float o[16];
+          tmem_load_small<16>(tmem + L::kColO + ob * L::kOCols + lane_base + c * 16, o);
+          if (ok && mine) {
+            if (it.nparts_seq == 1) {
+              uint4 v0, v1;
+              v0.x = Cvt<T>::from_float2(o[0] * inv, o[1] * inv);
+              v0.y = Cvt<T>::from_float2(o[2] * inv, o[3] * inv);
+              v0.z = Cvt<T>::from_float2(o[4] * inv, o[5] * inv);
+              v0.w = Cvt<T>::from_float2(o[6] * inv, o[7] * inv);
+              v1.x = Cvt<T>::from_float2(o[8] * inv, o[9] * inv);
+              v1.y = Cvt<T>::from_float2(o[10] * inv, o[11] * inv);
+              v1.z = Cvt<T>::from_float2(o[12] * inv, o[13] * inv);
+              v1.w = Cvt<T>::from_float2(o[14] * inv, o[15] * inv);
+              uint4* dst = reinterpret_cast<uint4*>(static_cast<T*>(p.out) + row * D + c * 16);
+              dst[0] = v0;
+              dst[1] = v1;
+            } else {
+              float4* dst = reinterpret_cast<float4*>(p.ws_o + r * D + c * 16);
+#pragma unroll
+              for (int k = 0; k < 4; ++k)
+                dst[k] = make_float4(o[4 * k] * inv, o[4 * k + 1] * inv, o[4 * k + 2] * inv,
+                                     o[4 * k + 3] * inv);
+            }
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(&o_free[ob]);
+        if (ok && mine && it.nparts_seq > 1) {
+          p.ws_m[r] = m;
+          p.ws_l[r] = l;
         }
       }
       ++k_item;
@@ -559,48 +654,48 @@ __global__ void __launch_bounds__(TcShape<NH>::kThreads, 1)
   }
 }
 
-template <typename T, int NH>
+template <typename T, int NH, int D>
 cudaError_t launch_tc_typed(const DecodeParams& p, const CUtensorMap& km, const CUtensorMap& vm,
                             const CUtensorMap& qm, int sms, cudaStream_t stream) {
-  using L = TcShape<NH>;
+  using L = TcShape<NH, D>;
   static unsigned long long configured = 0;  // bit per device ordinal (< 64)
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
   if (dev >= 64 || !(__atomic_load_n(&configured, __ATOMIC_ACQUIRE) & (1ull << dev))) {
-    err = cudaFuncSetAttribute(paged_decode_tc_kernel<T, NH>,
+    err = cudaFuncSetAttribute(paged_decode_tc_kernel<T, NH, D>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
     if (err != cudaSuccess) return err;
     if (dev < 64) __atomic_fetch_or(&configured, 1ull << dev, __ATOMIC_RELEASE);
   }
   const long long items = (long long)p.num_parts * p.num_kv_heads * p.num_seqs;
   const int grid = (int)(items < sms ? items : sms);
-  err = launch_overlapped(paged_decode_tc_kernel<T, NH>, dim3(grid), dim3(L::kThreads),
+  err = launch_overlapped(paged_decode_tc_kernel<T, NH, D>, dim3(grid), dim3(L::kThreads),
                           L::kBytes, stream, p, km, vm, qm, (int)items);
   if (err != cudaSuccess || p.num_parts <= 1) return err;
-  return launch_decode_reduce(p, std::is_same<T, __nv_bfloat16>::value ? PKV_BF16 : PKV_F16, kD,
+  return launch_decode_reduce(p, std::is_same<T, __nv_bfloat16>::value ? PKV_BF16 : PKV_F16, D,
                               stream);
 }
 
-template <typename T>
+template <typename T, int D>
 cudaError_t launch_tc_group(const DecodeParams& p, const CUtensorMap& km, const CUtensorMap& vm,
                             const CUtensorMap& qm, int sms, cudaStream_t stream) {
   static_assert(kMaxTcGroup == 32, "instantiations cover groups up to 32");
-  if (p.group <= 4) return launch_tc_typed<T, 4>(p, km, vm, qm, sms, stream);
-  if (p.group <= 8) return launch_tc_typed<T, 8>(p, km, vm, qm, sms, stream);
-  if (p.group <= 16) return launch_tc_typed<T, 16>(p, km, vm, qm, sms, stream);
-  return launch_tc_typed<T, 32>(p, km, vm, qm, sms, stream);
+  if (p.group <= 4) return launch_tc_typed<T, 4, D>(p, km, vm, qm, sms, stream);
+  if (p.group <= 8) return launch_tc_typed<T, 8, D>(p, km, vm, qm, sms, stream);
+  if (p.group <= 16) return launch_tc_typed<T, 16, D>(p, km, vm, qm, sms, stream);
+  return launch_tc_typed<T, 32, D>(p, km, vm, qm, sms, stream);
 }
 
 }  // namespace
 
 bool decode_tc_supported(int head_dim, int group, int partition_size) {
   static_assert(kTcPartitionQuantum == kKeys, "partitions are whole tiles");
-  return head_dim == kD && group >= kMinTcGroup && group <= kMaxTcGroup &&
-         partition_size % kKeys == 0;
+  return (head_dim == 64 || head_dim == 128) && group >= kMinTcGroup &&
+         group <= kMaxTcGroup && partition_size % kKeys == 0;
 }
 
-cudaError_t launch_paged_decode_tc(const DecodeParams& p, int dtype, int sms,
+cudaError_t launch_paged_decode_tc(const DecodeParams& p, int dtype, int head_dim, int sms,
                                    cudaStream_t stream, bool* unsupported) {
   *unsupported = false;
   CUtensorMap km, vm, qm;
@@ -608,14 +703,18 @@ cudaError_t launch_paged_decode_tc(const DecodeParams& p, int dtype, int sms,
   // Q rows of an item: a box of N rows from the item's first head (rows past
   // the group are other heads' or zero, and only feed unused columns).
   const int box_rows = p.group <= 16 ? 16 : 32;
-  if (!make_cache_map(&km, p.k_cache, dtype, rows, kD, p.block_size) ||
-      !make_cache_map(&vm, p.v_cache, dtype, rows, kD, p.block_size) ||
-      !make_rows_map(&qm, p.q, dtype, (long long)p.num_seqs * p.num_q_heads, kD, box_rows)) {
+  const int d = head_dim;
+  if (!make_cache_map(&km, p.k_cache, dtype, rows, d, p.block_size) ||
+      !make_cache_map(&vm, p.v_cache, dtype, rows, d, p.block_size) ||
+      !make_rows_map(&qm, p.q, dtype, (long long)p.num_seqs * p.num_q_heads, d, box_rows)) {
     *unsupported = true;
     return cudaErrorInvalidValue;
   }
-  return dtype == PKV_F16 ? launch_tc_group<__half>(p, km, vm, qm, sms, stream)
-                          : launch_tc_group<__nv_bfloat16>(p, km, vm, qm, sms, stream);
+  if (dtype == PKV_F16)
+    return d == 64 ? launch_tc_group<__half, 64>(p, km, vm, qm, sms, stream)
+                   : launch_tc_group<__half, 128>(p, km, vm, qm, sms, stream);
+  return d == 64 ? launch_tc_group<__nv_bfloat16, 64>(p, km, vm, qm, sms, stream)
+                 : launch_tc_group<__nv_bfloat16, 128>(p, km, vm, qm, sms, stream);
 }
 
 }  // namespace pkv

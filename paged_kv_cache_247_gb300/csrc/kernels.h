@@ -55,7 +55,7 @@ cudaError_t launch_paged_decode(const DecodeParams& p, int dtype, int head_dim,
 cudaError_t launch_decode_reduce(const DecodeParams& p, int dtype, int head_dim,
                                  cudaStream_t stream);
 
-// Grouped-head decode on the tensor cores: head size 128, groups of
+// Grouped-head decode on the tensor cores: head size 64 or 128, groups of
 // kMinTcGroup..kMaxTcGroup query heads, partitions of whole 128-key tiles.
 constexpr int kMinTcGroup = 2;
 constexpr int kMaxTcGroup = 32;
@@ -64,7 +64,7 @@ bool decode_tc_supported(int head_dim, int group, int partition_size);
 
 // Persistent: min(work items, sms) CTAs, one per SM.  unsupported is set when
 // the tensor maps of the caches or of q cannot be encoded.
-cudaError_t launch_paged_decode_tc(const DecodeParams& p, int dtype, int sms,
+cudaError_t launch_paged_decode_tc(const DecodeParams& p, int dtype, int head_dim, int sms,
                                    cudaStream_t stream, bool* unsupported);
 
 // Same kernels over a contiguous cache [S, Hkv, capacity, D]: block_size is

@@ -2,7 +2,8 @@
 oracle.
 
 The kernel puts 128 keys of a tile on the MMA's M dimension and the group's
-query heads on N (padded to 16 or 32), so the cases cover groups that fill
+query heads on N (padded to 16 or 32); for head size 64 the P.V product puts
+the heads on M instead.  Both head sizes run every case, covering groups that fill
 N exactly and groups that leave padding (3, 6, 12, 20), contexts that end
 inside, at and just past a 128-key tile and a block, every block size,
 NaN-poisoned tails and unused blocks, split and unsplit partitions, the
@@ -44,30 +45,36 @@ def run(case, partition_size=0):
 LENS = [1, 2, 15, 16, 17, 127, 128, 129, 255, 256, 257, 700, 1500]
 
 
+@pytest.mark.parametrize("head_dim", [128, 64])
 @pytest.mark.parametrize("dtype", ["fp16", "bf16"])
 @pytest.mark.parametrize("hq,hkv", [(16, 8), (12, 4), (16, 4), (24, 4), (16, 2), (48, 4),
                                     (32, 2), (40, 2), (64, 2), (32, 1)])
-def test_groups_ragged(cuda_device, dtype, hq, hkv):
-    case = W.make_decode_case(hq * 13 + hkv, len(LENS), hq, hkv, 128, 16, dtype, LENS,
-                              pool_factor=1.4, poison=True, device=cuda_device)
+def test_groups_ragged(cuda_device, dtype, hq, hkv, head_dim):
+    case = W.make_decode_case(hq * 13 + hkv + head_dim, len(LENS), hq, hkv, head_dim, 16, dtype,
+                              LENS, pool_factor=1.4, poison=True, device=cuda_device)
+    assert pkv.decode_uses_tensor_cores(len(LENS), hq, hkv, head_dim, case.max_context_len)
     ref = oracle_decode(case)
     for part in (0, 128, 256, 1024):
-        assert_within_tol(run(case, part), ref, W.DTYPES[dtype], f"G={hq // hkv} part={part}")
+        assert_within_tol(run(case, part), ref, W.DTYPES[dtype],
+                          f"G={hq // hkv} D={head_dim} part={part}")
 
 
+@pytest.mark.parametrize("head_dim", [128, 64])
 @pytest.mark.parametrize("block_size", [8, 16, 32, 64, 128])
-def test_block_sizes(cuda_device, block_size):
+def test_block_sizes(cuda_device, block_size, head_dim):
     lens = [1, block_size - 1, block_size, block_size + 1, 3 * block_size + 7, 600, 1025]
-    case = W.make_decode_case(block_size + 3, len(lens), 64, 8, 128, block_size, "bf16", lens,
-                              pool_factor=1.2, poison=True, device=cuda_device)
+    case = W.make_decode_case(block_size + 3, len(lens), 64, 8, head_dim, block_size, "bf16",
+                              lens, pool_factor=1.2, poison=True, device=cuda_device)
     ref = oracle_decode(case)
     for part in (0, 128, 384):
-        assert_within_tol(run(case, part), ref, torch.bfloat16, f"B={block_size} part={part}")
+        assert_within_tol(run(case, part), ref, torch.bfloat16,
+                          f"B={block_size} D={head_dim} part={part}")
 
 
-def test_empty_and_single_token_contexts(cuda_device):
+@pytest.mark.parametrize("head_dim", [128, 64])
+def test_empty_and_single_token_contexts(cuda_device, head_dim):
     lens = [0, 1, 0, 5, 1]
-    case = W.make_decode_case(78, len(lens), 64, 8, 128, 16, "fp16", lens, pool_blocks=20,
+    case = W.make_decode_case(78, len(lens), 64, 8, head_dim, 16, "fp16", lens, pool_blocks=20,
                               max_blocks_per_seq=4, poison=True, device=cuda_device)
     case.max_context_len = 40  # a loose host bound is allowed
     out = run(case)
@@ -80,12 +87,13 @@ def test_empty_and_single_token_contexts(cuda_device):
         assert torch.equal(out[s], v_row.repeat_interleave(8, dim=0))
 
 
-def test_running_max_moves_late(cuda_device):
+@pytest.mark.parametrize("head_dim", [128, 64])
+def test_running_max_moves_late(cuda_device, head_dim):
     """A key late in the context dominates (its logit is far above the first
     tile's maximum), and logits with a large scale keep moving the maximum:
     the accumulated output must be rescaled, not overflow or go stale."""
     lens = [300, 1000, 2000, 129]
-    case = W.make_decode_case(91, len(lens), 32, 4, 128, 16, "bf16", lens, pool_factor=1.1,
+    case = W.make_decode_case(91, len(lens), 32, 4, head_dim, 16, "bf16", lens, pool_factor=1.1,
                               device=cuda_device)
     tbl = case.block_tables.cpu()
     for s, pos in ((0, 290), (1, 700), (2, 1999), (3, 128)):
@@ -102,13 +110,14 @@ def test_running_max_moves_late(cuda_device):
         assert_within_tol(run(case, part), ref, torch.bfloat16, f"scale 1 part={part}")
 
 
-@pytest.mark.parametrize("dtype,hq,hkv,B", [("bf16", 32, 8, 16), ("fp16", 64, 8, 8),
-                                             ("bf16", 24, 4, 128)])
-def test_fused_append_equals_separate_and_oracle(cuda_device, dtype, hq, hkv, B):
+@pytest.mark.parametrize("dtype,hq,hkv,B,D", [("bf16", 32, 8, 16, 128), ("fp16", 64, 8, 8, 128),
+                                               ("bf16", 24, 4, 128, 128), ("fp16", 32, 8, 16, 64),
+                                               ("bf16", 64, 4, 32, 64)])
+def test_fused_append_equals_separate_and_oracle(cuda_device, dtype, hq, hkv, B, D):
     lens = [1, 0, B - 1, B, B + 1, 127, 128, 129, 600, 1500]
-    case = W.make_decode_case(hq * 5 + B, len(lens), hq, hkv, 128, B, dtype, lens,
+    case = W.make_decode_case(hq * 5 + B + D, len(lens), hq, hkv, D, B, dtype, lens,
                               pool_factor=1.3, poison=True, device=cuda_device)
-    k_new, v_new = W.new_tokens(B + hq + 1, len(lens), hkv, 128, dtype, device=cuda_device)
+    k_new, v_new = W.new_tokens(B + hq + 1, len(lens), hkv, D, dtype, device=cuda_device)
     k0, v0 = to_f64(case.k_cache), to_f64(case.v_cache)
     slots = W.last_position_slots(case)
     k1, v1 = oracle.kv_append(to_f64(k_new), to_f64(v_new), k0, v0, slots.numpy())
@@ -131,15 +140,15 @@ def test_fused_append_equals_separate_and_oracle(cuda_device, dtype, hq, hkv, B)
         assert_within_tol(out_b, ref, W.DTYPES[dtype], f"fused partition {part}")
 
 
-@pytest.mark.parametrize("group", [4, 8, 32])
-def test_long_contexts_sampled(cuda_device, group):
+@pytest.mark.parametrize("group,head_dim", [(4, 128), (8, 128), (32, 128), (8, 64), (32, 64)])
+def test_long_contexts_sampled(cuda_device, group, head_dim):
     """32 sequences x 4096 tokens over 8 KV heads (the query-head group sweep
     of the bench) plus 8 x 32k, sampled sequences, every head."""
-    case = W.make_decode_case(6, 32, 8 * group, 8, 128, 16, "bf16", [4096] * 32,
+    case = W.make_decode_case(6, 32, 8 * group, 8, head_dim, 16, "bf16", [4096] * 32,
                               device=cuda_device)
     out = run(case)
     assert_within_tol(out[[0, 31]], oracle_decode(case, [0, 31]), torch.bfloat16,
-                      f"G={group} 32x4k")
+                      f"G={group} D={head_dim} 32x4k")
     del case, out
     case = W.sweep_decode(16, 8, 32768, device=cuda_device)
     out = run(case)
