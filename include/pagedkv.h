@@ -102,8 +102,8 @@ int pkv_version(void);
  * over t < context_lens[s], where G = num_q_heads / num_kv_heads (query head
  * h reads KV head h / G) and K_s[t] = k_cache[block_tables[s][t / B]][.][t % B].
  * Logits, softmax and the weighted sum are fp32; out is rounded to dtype
- * (round to nearest even).  On the tensor-core path (head_dim 128 and a group
- * G of 2 to 32 query heads by default, see pkv_set_decode_path) the softmax
+ * (round to nearest even).  On the tensor-core path (groups G of 2 to 32
+ * query heads by default, see pkv_set_decode_path) the softmax
  * weights are rounded to dtype before the weighted sum, which the tensor
  * core accumulates in fp32 ([P3] "Calculate bytes per token before choosing
  * a batch": groups of query heads share one KV head, and a group of G heads
@@ -217,12 +217,13 @@ int pkv_decode_partition_size(int num_seqs, int num_q_heads, int num_kv_heads,
 
 /* Which decode kernel the decode calls use, process-wide (a tuning and test
  * control; the default suits every shape measured):
- *   0  chosen per call (default): the tensor-core kernel where it applies
- *      (head_dim 128, groups of 2 to 32 query heads, partition_size 0 or a
- *      multiple of 128), the CUDA-core kernel otherwise (MHA, head_dim 64);
+ *   0  chosen per call (default): the tensor-core kernel for grouped heads
+ *      (groups of 2 to 32 query heads, head_dim 64 or 128, partition_size 0
+ *      or a multiple of 128), the CUDA-core kernel otherwise (MHA);
  *   1  always the CUDA-core kernel;
- *   2  the tensor-core kernel wherever it applies, else the CUDA-core one
- *      (today the same choice as 0).
+ *   2  the tensor-core kernel wherever it can run (groups of 1 to 32, head_dim
+ *      64 or 128, partition_size 0 or a multiple of 128), else the CUDA-core
+ *      one.
  * Both compute the same attention within the stated tolerance.  It changes
  * the partition pkv_decode_partition_size and pkv_decode_workspace_size
  * report, so set it before sizing a workspace, and not while another host

@@ -55,9 +55,10 @@ cudaError_t launch_paged_decode(const DecodeParams& p, int dtype, int head_dim,
 cudaError_t launch_decode_reduce(const DecodeParams& p, int dtype, int head_dim,
                                  cudaStream_t stream);
 
-// Grouped-head decode on the tensor cores: head size 64 or 128, groups of
-// kMinTcGroup..kMaxTcGroup query heads, partitions of whole 128-key tiles.
-constexpr int kMinTcGroup = 2;
+// Decode on the tensor cores: head size 64 or 128, groups of
+// kMinTcGroup..kMaxTcGroup query heads (grouped heads by default, single
+// heads when forced), partitions of whole 128-key tiles.
+constexpr int kMinTcGroup = 1;
 constexpr int kMaxTcGroup = 32;
 constexpr int kTcPartitionQuantum = 128;
 bool decode_tc_supported(int head_dim, int group, int partition_size);

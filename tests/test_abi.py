@@ -129,9 +129,11 @@ def test_tensor_core_partition_policy(lib):
         tiles = -(-ctx // 128)
         costs = [share(S, 8, ctx, pt) for pt in range(1, min(16, tiles) + 1)]
         assert share(S, 8, ctx, p // 128) == min(costs)
-    # groups of 2 to 32 share the policy; single-head groups do not
+    # groups of 2 to 32 share the policy; single-head groups do not (by default)
     assert part(8, 16, 8, 128, 8192) == part(8, 256, 8, 128, 8192) == 1280
     assert part(8, 8, 8, 128, 8192) % 128 != 0
+    assert lib.pkv_decode_uses_tensor_cores(8, 8, 8, 128, 8192, 0) == 0
+    assert lib.pkv_decode_uses_tensor_cores(8, 16, 8, 64, 8192, 0) == 1
 
 
 def test_auto_partition_properties(lib):
@@ -221,8 +223,8 @@ def test_decode_path_switch(lib):
         assert lib.pkv_decode_partition_size(8, 256, 8, 128, 32768) % 128 == 0
         assert lib.pkv_set_decode_path(2) == 0
         assert lib.pkv_decode_partition_size(8, 32, 8, 128, 8192) % 128 == 0
-        # single-head groups stay on the CUDA-core kernel; head size 64 has both
-        assert lib.pkv_decode_uses_tensor_cores(8, 8, 8, 128, 8192, 0) == 0
+        # forced, single-head groups run on the tensor cores too; head size 64 has both
+        assert lib.pkv_decode_uses_tensor_cores(8, 8, 8, 128, 8192, 0) == 1
         assert lib.pkv_decode_uses_tensor_cores(8, 64, 8, 64, 8192, 0) == 1
         assert lib.pkv_decode_uses_tensor_cores(8, 64, 8, 64, 8192, 96) == 0  # not whole tiles
         for args in ((8, 8, 8, 128, 8192), (8, 64, 8, 64, 8192)):

@@ -47,7 +47,7 @@ LENS = [1, 2, 15, 16, 17, 127, 128, 129, 255, 256, 257, 700, 1500]
 
 @pytest.mark.parametrize("head_dim", [128, 64])
 @pytest.mark.parametrize("dtype", ["fp16", "bf16"])
-@pytest.mark.parametrize("hq,hkv", [(16, 8), (12, 4), (16, 4), (24, 4), (16, 2), (48, 4),
+@pytest.mark.parametrize("hq,hkv", [(8, 8), (16, 8), (12, 4), (16, 4), (24, 4), (16, 2), (48, 4),
                                     (32, 2), (40, 2), (64, 2), (32, 1)])
 def test_groups_ragged(cuda_device, dtype, hq, hkv, head_dim):
     case = W.make_decode_case(hq * 13 + hkv + head_dim, len(LENS), hq, hkv, head_dim, 16, dtype,
