@@ -1,4 +1,5 @@
-// Grouped-head paged decode on the 5th-generation tensor cores (tcgen05).
+// Grouped-head paged decode on the 5th-generation tensor cores (tcgen05),
+// head sizes 64 and 128.
 //
 // What it computes is what paged_decode_kernel computes ("Only 20.4% of your
 // KV cache held actual tokens", section "The page table, relocated into
@@ -19,6 +20,11 @@
 //   O^T [D x N]        += V_tile^T . P^T              A = V tile (MN-major),
 //                                                     B = P^T (K-major)
 //
+// for head size 128.  For head size 64 (an M of 64 would need another
+// accumulator layout) the second product is O [128 x D] += P . V with the
+// heads on M: P^T [heads x keys] is the K-major A operand, V the MN-major B
+// operand, rows past the group unused.
+//
 // N is the group rounded up to 16 or 32.  A work item is (sequence, KV head,
 // partition of the context) with every head of the group, so each K/V tile is
 // read from HBM once per group.  The kernel is persistent: one CTA per SM
@@ -33,15 +39,16 @@
 //              (base 2; the warpgroup then agrees on the new maxima and
 //              rescales its partial sums and O^T); partial row sums stay per
 //              thread.  At the end of an item thread d normalises and writes
-//              dimension d of its heads.
+//              dimension d of its heads (head size 128), or thread h the D
+//              outputs of head h (head size 64).
 //   K producer the item's Q rows (one TMA copy), and one 4-D TMA copy per
 //              (block, head) run of K into a ring of tiles.
 //   V producer the same for V.
 //   S issuer   S^T of each tile (8 MMAs); owns the tensor memory.
-//   O issuer   O^T += V^T P^T of each tile (8 MMAs).
+//   O issuer   the P.V product of each tile (8 MMAs).
 //
-// Tensor memory: S^T in two buffers of N columns, O^T in two (items
-// alternate, so an item's output is read while the next one accumulates).
+// Tensor memory: S^T in two buffers of N columns, O in two (items alternate,
+// so an item's output is read while the next one accumulates).
 // The split-context partials (o, m, l in base 2) have the layout and meaning
 // of paged_decode_kernel's, so the same reduction kernel merges them.
 
