@@ -68,7 +68,7 @@ using namespace tc;
 
 constexpr int kKeys = kTileKeys;        // keys per tile: M of S^T, K of the P.V product
 constexpr int kGroupP = (kKeys / 64) * 1024; // bytes between 8-head groups of P^T
-constexpr int kBarSlots = 32;
+constexpr int kBarSlots = 40;
 constexpr int kStages = 3;              // K ring and V ring depth
 
 constexpr int pow2_at_least(int x, int p = 32) { return p >= x ? p : pow2_at_least(x, 2 * p); }
@@ -95,17 +95,20 @@ struct TcShape {
   static constexpr int kQBytes = N * D * 2;    // D / 64 atoms of N rows x 128 bytes
   static constexpr int kPRows = kTrans ? N : 128;
   static constexpr int kPBuf = (kPRows / 8) * kGroupP;
+  // S^T buffers and P^T buffers: three where shared memory allows, else two
+  static constexpr int kSB =
+      2 * kStages * kKvTile + 2 * kQBytes + 3 * kPBuf + 4096 <= 227 * 1024 ? 3 : 2;
   static constexpr int kOCols = kTrans ? N : D;  // tensor-memory columns of one O buffer
   static constexpr int kQ = 2 * kStages * kKvTile;  // after the K and V rings
   static constexpr int kP = kQ + 2 * kQBytes;
-  static constexpr int kRed = kP + 2 * kPBuf;       // [KG][4 warps][NHW] floats
+  static constexpr int kRed = kP + kSB * kPBuf;     // [KG][4 warps][NHW] floats
   static constexpr int kMref = kRed + KG * 4 * NHW * 4;
   static constexpr int kBar = kMref + KG * NHW * 4;
   static constexpr int kTmemSlot = kBar + kBarSlots * 8;
   static constexpr int kBytes = kTmemSlot + 16 + 1024;  // + alignment slack
   static_assert(kBytes <= 227 * 1024, "shared memory overflow");
-  static constexpr int kColO = 2 * N;                   // S^T buffers first
-  static constexpr int kTmemCols = pow2_at_least(2 * N + 2 * kOCols);
+  static constexpr int kColO = kSB * N;                 // S^T buffers first
+  static constexpr int kTmemCols = pow2_at_least(kSB * N + 2 * kOCols);
   static_assert(kTmemCols <= 512, "tensor memory overflow");
 };
 
@@ -181,15 +184,16 @@ __global__ void __launch_bounds__(TcShape<NH, D>::kThreads, 1)
   uint64_t* k_empty = k_full + S;      // [S] S^T MMAs done reading it (commit)
   uint64_t* v_full = k_empty + S;      // [S] V tile landed
   uint64_t* v_empty = v_full + S;      // [S] O^T MMAs done reading it (commit)
-  uint64_t* s_full = v_empty + S;      // [2] S^T buffer computed (commit)
-  uint64_t* s_free = s_full + 2;       // [2] S^T buffer read by the key warpgroups
-  uint64_t* p_full = s_free + 2;       // [2] P^T buffer written (key warpgroups)
-  uint64_t* p_free = p_full + 2;       // [2] O^T MMAs done with P^T buffer (commit)
-  uint64_t* q_full = p_free + 2;       // [2] Q rows of an item landed (TMA bytes)
+  constexpr int SB = L::kSB;
+  uint64_t* s_full = v_empty + S;      // [SB] S^T buffer computed (commit)
+  uint64_t* s_free = s_full + SB;      // [SB] S^T buffer read by the key warpgroups
+  uint64_t* p_full = s_free + SB;      // [SB] P^T buffer written (key warpgroups)
+  uint64_t* p_free = p_full + SB;      // [SB] P.V MMAs done with P^T buffer (commit)
+  uint64_t* q_full = p_free + SB;      // [2] Q rows of an item landed (TMA bytes)
   uint64_t* q_empty = q_full + 2;      // [2] S^T MMAs of that item done (commit)
   uint64_t* o_free = q_empty + 2;      // [2] O^T buffer read by the key warpgroups
   uint64_t* drain = o_free + 2;        // [2] each issuer's last MMAs finished
-  static_assert(4 * S + 16 <= kBarSlots, "barrier area too small");
+  static_assert(4 * S + 4 * SB + 8 <= kBarSlots, "barrier area too small");
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kTmemSlot);
 
   const int warp = threadIdx.x >> 5;
@@ -203,11 +207,13 @@ __global__ void __launch_bounds__(TcShape<NH, D>::kThreads, 1)
       mbar_init(&v_full[i], 1);
       mbar_init(&v_empty[i], 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < SB; ++b) {
       mbar_init(&s_full[b], 1);
       mbar_init(&s_free[b], L::kKeyThreads);
       mbar_init(&p_full[b], L::kKeyThreads);
       mbar_init(&p_free[b], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
       mbar_init(&q_full[b], 1);
       mbar_init(&q_empty[b], 1);
       mbar_init(&o_free[b], L::kKeyThreads);
@@ -351,7 +357,7 @@ __global__ void __launch_bounds__(TcShape<NH, D>::kThreads, 1)
           for (int i = 0; i < it.n_tiles; ++i, ++kt) {
             const int st = kt % S;
             if (!mbar_wait(&k_full[st], (kt / S) & 1, p.status) ||
-                (kt >= 2 && !mbar_wait(&s_free[kt & 1], ((kt - 2) >> 1) & 1, p.status))) {
+                (kt >= SB && !mbar_wait(&s_free[kt % SB], ((kt / SB) - 1) & 1, p.status))) {
               ok = false;
               break;
             }
@@ -360,13 +366,13 @@ __global__ void __launch_bounds__(TcShape<NH, D>::kThreads, 1)
             // 128-byte rows, then the next 64-column atom.
 #pragma unroll
             for (int ks = 0; ks < D / 16; ++ks)
-              mma_f16_ss(tmem + (kt & 1) * N,
+              mma_f16_ss(tmem + (kt % SB) * N,
                          smem_desc(aK + st * kKvTile + (ks / 4) * 1024 + (ks % 4) * 32, 16,
                                    kGroupKV),
                          smem_desc(aQ + b * L::kQBytes + (ks / 4) * (N * 128) + (ks % 4) * 32,
                                    16, 1024),
                          idesc, ks > 0 ? 1u : 0u);
-            mma_commit(&s_full[kt & 1]);
+            mma_commit(&s_full[kt % SB]);
             mma_commit(&k_empty[st]);
           }
           if (ok) mma_commit(&q_empty[b]);
@@ -375,7 +381,7 @@ __global__ void __launch_bounds__(TcShape<NH, D>::kThreads, 1)
           for (int i = 0; i < it.n_tiles; ++i, ++kt) {
             const int st = kt % S;
             if (!mbar_wait(&v_full[st], (kt / S) & 1, p.status) ||
-                !mbar_wait(&p_full[kt & 1], (kt >> 1) & 1, p.status)) {
+                !mbar_wait(&p_full[kt % SB], (kt / SB) & 1, p.status)) {
               ok = false;
               break;
             }
@@ -388,7 +394,7 @@ __global__ void __launch_bounds__(TcShape<NH, D>::kThreads, 1)
               const uint64_t dv =
                   smem_desc(aV + st * kKvTile + ks * 2 * kGroupKV, 1024, kGroupKV);
               const uint64_t dp = smem_desc(
-                  aP + (kt & 1) * L::kPBuf + (ks / 4) * 1024 + (ks % 4) * 32, 16, kGroupP);
+                  aP + (kt % SB) * L::kPBuf + (ks / 4) * 1024 + (ks % 4) * 32, 16, kGroupP);
               if constexpr (L::kTrans)
                 mma_f16_ss(tmem + L::kColO + b * L::kOCols, dv, dp, idesc,
                            (i > 0 || ks > 0) ? 1u : 0u);
@@ -396,7 +402,7 @@ __global__ void __launch_bounds__(TcShape<NH, D>::kThreads, 1)
                 mma_f16_ss(tmem + L::kColO + b * L::kOCols, dp, dv, idesc,
                            (i > 0 || ks > 0) ? 1u : 0u);
             }
-            mma_commit(&p_free[kt & 1]);
+            mma_commit(&p_free[kt % SB]);
             mma_commit(&v_empty[st]);
           }
         }
@@ -420,7 +426,7 @@ __global__ void __launch_bounds__(TcShape<NH, D>::kThreads, 1)
       // P's rows past the group are read by the P V product but never
       // written: clear them once (the first release's proxy fence orders
       // these stores before the tensor core reads them).
-      for (int i = threadIdx.x; i < 2 * L::kPBuf / 16; i += L::kKeyThreads)
+      for (int i = threadIdx.x; i < SB * L::kPBuf / 16; i += L::kKeyThreads)
         reinterpret_cast<uint4*>(sP)[i] = make_uint4(0, 0, 0, 0);
     }
     int kt = 0, k_item = 0;
@@ -451,12 +457,12 @@ __global__ void __launch_bounds__(TcShape<NH, D>::kThreads, 1)
         // A wait that gives up (never expected) leaves ok false; the loop
         // runs on without waiting, so that every named barrier stays matched,
         // and nothing it computes is stored.
-        if (ok && !mbar_wait_warp(&s_full[kt & 1], (kt >> 1) & 1, p.status)) ok = false;
+        if (ok && !mbar_wait_warp(&s_full[kt % SB], (kt / SB) & 1, p.status)) ok = false;
         tc_fence_after();
         float x[NHW];
-        tmem_load_small<NHW>(tmem + (kt & 1) * N + hb + lane_base, x);
+        tmem_load_small<NHW>(tmem + (kt % SB) * N + hb + lane_base, x);
         tc_fence_before();
-        mbar_arrive(&s_free[kt & 1]);
+        mbar_arrive(&s_free[kt % SB]);
         group_sync(kg);  // mref_s: reset for the item or last moved
 #pragma unroll
         for (int g = 0; g < NHW; ++g) mref[g] = mref_s[g];
@@ -497,7 +503,7 @@ __global__ void __launch_bounds__(TcShape<NH, D>::kThreads, 1)
           if (i > 0 && moved) {
             // O holds this item's tiles so far: once their MMAs are done
             // (P^T buffer of the previous tile released), rescale it.
-            if (ok && !mbar_wait_warp(&p_free[(kt - 1) & 1], ((kt - 1) >> 1) & 1, p.status))
+            if (ok && !mbar_wait_warp(&p_free[(kt - 1) % SB], ((kt - 1) / SB) & 1, p.status))
               ok = false;
             tc_fence_after();
             if constexpr (L::kTrans) {
@@ -536,10 +542,10 @@ __global__ void __launch_bounds__(TcShape<NH, D>::kThreads, 1)
           l_part[g] += e;
           pt[g] = static_cast<T>(e);
         }
-        // The buffer was last read by the MMAs of tile kt - 2.
-        if (kt >= 2 && ok && !mbar_wait_warp(&p_free[kt & 1], ((kt - 2) >> 1) & 1, p.status))
+        // The buffer was last read by the MMAs of tile kt - SB.
+        if (kt >= SB && ok && !mbar_wait_warp(&p_free[kt % SB], ((kt / SB) - 1) & 1, p.status))
           ok = false;
-        unsigned char* pb = sP + (kt & 1) * L::kPBuf;
+        unsigned char* pb = sP + (kt % SB) * L::kPBuf;
 #pragma unroll
         for (int g = 0; g < NHW; ++g)
           if (hb + g < G)
@@ -557,7 +563,7 @@ __global__ void __launch_bounds__(TcShape<NH, D>::kThreads, 1)
           }
         }
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        mbar_arrive(&p_full[kt & 1]);
+        mbar_arrive(&p_full[kt % SB]);
       }
 
       // Row sums per head over the 128 keys' partial sums.
@@ -570,7 +576,7 @@ __global__ void __launch_bounds__(TcShape<NH, D>::kThreads, 1)
       }
       group_sync(kg);
       const int last = kt - 1;
-      if (ok && !mbar_wait_warp(&p_free[last & 1], (last >> 1) & 1, p.status)) ok = false;
+      if (ok && !mbar_wait_warp(&p_free[last % SB], (last / SB) & 1, p.status)) ok = false;
       tc_fence_after();
       if constexpr (L::kTrans) {
         // O^T: thread d writes dimension d of this warpgroup's heads.
