@@ -57,6 +57,8 @@ def parse_args():
                          "captures)")
     ap.add_argument("--head-dim", type=int, default=128, choices=[64, 128],
                     help="--workload groups: head size")
+    ap.add_argument("--block-size", type=int, default=16, choices=[8, 16, 32, 64, 128],
+                    help="--workload groups: tokens per block")
     ap.add_argument("--group", type=int, default=0,
                     help="one query-head group size for --workload groups (0 = all)")
     ap.add_argument("--partition", type=int, default=0, help="tokens per partition (0 = library)")
@@ -1293,8 +1295,8 @@ def run_groups(args, rank, world, local_rank):
     clocks = ClockSampler(dev.index if dev.index is not None else 0)
     clocks.start()
     for G in groups:
-        case = W.make_decode_case(6, S, 8 * G, 8, args.head_dim, 16, "bf16", [4096] * S,
-                                  device=dev)
+        case = W.make_decode_case(6, S, 8 * G, 8, args.head_dim, args.block_size, "bf16",
+                                  [4096] * S, device=dev)
         Sq, Hq, D = case.q.shape
         part = args.partition or pkv.decode_partition_size(Sq, Hq, 8, D, case.max_context_len)
         ws = torch.empty(max(16, pkv.decode_workspace_size(Sq, Hq, 8, D, case.max_context_len,
@@ -1329,7 +1331,7 @@ def run_groups(args, rank, world, local_rank):
             "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": f"decode, {S} seqs x 4096 tokens, 8 KV heads of {args.head_dim}, bf16, "
-                                   f"B=16, query heads 8 x group", "l2": "flushed (256 MiB read) "
+                                   f"B={args.block_size}, query heads 8 x group", "l2": "flushed (256 MiB read) "
                                    "before every call",
                        "launch": "queued behind a device-side wait, outside the timed region"},
             "groups": rows, "clocks": clock_rec}), flush=True)

@@ -69,7 +69,6 @@ using namespace tc;
 constexpr int kKeys = kTileKeys;        // keys per tile: M of S^T, K of the P.V product
 constexpr int kGroupP = (kKeys / 64) * 1024; // bytes between 8-head groups of P^T
 constexpr int kBarSlots = 40;
-constexpr int kStages = 3;              // K ring and V ring depth
 
 constexpr int pow2_at_least(int x, int p = 32) { return p >= x ? p : pow2_at_least(x, 2 * p); }
 
@@ -95,9 +94,17 @@ struct TcShape {
   static constexpr int kQBytes = N * D * 2;    // D / 64 atoms of N rows x 128 bytes
   static constexpr int kPRows = kTrans ? N : 128;
   static constexpr int kPBuf = (kPRows / 8) * kGroupP;
+  // K and V ring depth: the bytes in flight per SM set the bandwidth an SM
+  // draws (about 2-3 us of latency under load), so the rings hold about 96
+  // KiB per operand: 3 tiles at D = 128, as many as fit beside two P^T
+  // buffers (4) at D = 64.
+  static constexpr int kFixed = 2 * kQBytes + 4096;
+  static constexpr int kStages =
+      D == 128 ? 3 : (227 * 1024 - kFixed - 2 * kPBuf) / (2 * kKvTile) < 6
+                         ? (227 * 1024 - kFixed - 2 * kPBuf) / (2 * kKvTile)
+                         : 6;
   // S^T buffers and P^T buffers: three where shared memory allows, else two
-  static constexpr int kSB =
-      2 * kStages * kKvTile + 2 * kQBytes + 3 * kPBuf + 4096 <= 227 * 1024 ? 3 : 2;
+  static constexpr int kSB = 2 * kStages * kKvTile + kFixed + 3 * kPBuf <= 227 * 1024 ? 3 : 2;
   static constexpr int kOCols = kTrans ? N : D;  // tensor-memory columns of one O buffer
   static constexpr int kQ = 2 * kStages * kKvTile;  // after the K and V rings
   static constexpr int kP = kQ + 2 * kQBytes;
@@ -167,7 +174,7 @@ __global__ void __launch_bounds__(TcShape<NH, D>::kThreads, 1)
                            const __grid_constant__ CUtensorMap qmap, int num_items) {
   using L = TcShape<NH, D>;
   constexpr int N = L::N;
-  constexpr int S = kStages;
+  constexpr int S = L::kStages;
   constexpr int NHW = L::NHW;
   constexpr int kGroupKV = L::kGroupKV;
   constexpr int kKvTile = L::kKvTile;
