@@ -68,7 +68,7 @@ using namespace tc;
 
 constexpr int kKeys = kTileKeys;        // keys per tile: M of S^T, K of the P.V product
 constexpr int kGroupP = (kKeys / 64) * 1024; // bytes between 8-head groups of P^T
-constexpr int kBarSlots = 40;
+constexpr int kBarSlots = 48;
 
 constexpr int pow2_at_least(int x, int p = 32) { return p >= x ? p : pow2_at_least(x, 2 * p); }
 
@@ -92,7 +92,12 @@ struct TcShape {
   static constexpr int kOWarp = kKWarp + 3;    // O^T issuer
   static constexpr int kThreads = kKeyThreads + 4 * 32;
   static constexpr int kQBytes = N * D * 2;    // D / 64 atoms of N rows x 128 bytes
-  static constexpr int kPRows = kTrans ? N : 128;
+  // P^T rows: the padded group for O^T; for O the MMA's 128 rows, except that
+  // a group of at most 8 heads keeps only one 8-row group, which the A
+  // operand's descriptor repeats down all 128 rows (group stride 0: rows
+  // 8..127 of O repeat rows 0..7 and are never read).
+  static constexpr int kPRows = kTrans ? N : (NH <= 8 ? 8 : 128);
+  static constexpr int kPGroupStride = kPRows == 8 ? 0 : kGroupP;
   static constexpr int kPBuf = (kPRows / 8) * kGroupP;
   // K and V ring depth: the bytes in flight per SM set the bandwidth an SM
   // draws (about 2-3 us of latency under load), so the rings hold about 96
@@ -400,8 +405,9 @@ __global__ void __launch_bounds__(TcShape<NH, D>::kThreads, 1)
             for (int ks = 0; ks < kKeys / 16; ++ks) {
               const uint64_t dv =
                   smem_desc(aV + st * kKvTile + ks * 2 * kGroupKV, 1024, kGroupKV);
-              const uint64_t dp = smem_desc(
-                  aP + (kt % SB) * L::kPBuf + (ks / 4) * 1024 + (ks % 4) * 32, 16, kGroupP);
+              const uint64_t dp =
+                  smem_desc(aP + (kt % SB) * L::kPBuf + (ks / 4) * 1024 + (ks % 4) * 32, 16,
+                            L::kTrans ? kGroupP : L::kPGroupStride);
               if constexpr (L::kTrans)
                 mma_f16_ss(tmem + L::kColO + b * L::kOCols, dv, dp, idesc,
                            (i > 0 || ks > 0) ? 1u : 0u);
