@@ -65,6 +65,9 @@ def parse_args():
     ap.add_argument("--path", default="fused", choices=["fused", "separate"],
                     help="one fused append+decode launch, or kv_append then decode")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--e2e-buffers", type=int, default=2,
+                    help="staging buffers of the end-to-end loop (inputs copied that many - 1 "
+                         "steps ahead)")
     ap.add_argument("--num-seqs", type=int, default=None,
                     help="fewer sequences than the workload's (for profiler captures)")
     return ap.parse_args()
@@ -272,46 +275,49 @@ def time_alone(fn, flush, stream, iters):
     return total / iters
 
 
-def pipelined_steps(stream, n_steps, copy_in, compute, copy_out, hold_ms=5.0):
-    """Mean ms per step of a double-buffered serving loop, on the device
+def pipelined_steps(stream, n_steps, copy_in, compute, copy_out, hold_ms=5.0, nbuf=2):
+    """Mean ms per step of a multi-buffered serving loop, on the device
     clock.  copy_in(b) fills input buffer b on a copy stream, compute(b)
     reads input b and writes output b on `stream`, copy_out(b) reads output
-    b back on a second copy stream.  Step i+1's inputs go in, and step i's
-    output comes out, while the compute stream moves on; each buffer is
-    reused only after the step that last touched it is done with it."""
+    b back on a second copy stream.  Step i + nbuf - 1's inputs go in, and
+    step i's output comes out, while the compute stream moves on; each buffer
+    is reused only after the step that last touched it is done with it."""
     dev = stream.device
     s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-    in_ready = [torch.cuda.Event() for _ in range(2)]
-    done = [torch.cuda.Event() for _ in range(2)]
-    out_done = [torch.cuda.Event() for _ in range(2)]
+    in_ready = [torch.cuda.Event() for _ in range(nbuf)]
+    done = [torch.cuda.Event() for _ in range(nbuf)]
+    out_done = [torch.cuda.Event() for _ in range(nbuf)]
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     with torch.cuda.stream(stream):
         hold_stream(hold_ms)  # the host queues the first steps before t0 fires
     t0.record(stream)
     s_in.wait_event(t0)
-    with torch.cuda.stream(s_in):
-        copy_in(0)
-    in_ready[0].record(s_in)
+    for k in range(min(nbuf - 1, n_steps)):
+        with torch.cuda.stream(s_in):
+            copy_in(k)
+        in_ready[k].record(s_in)
     for i in range(n_steps):
-        b = i & 1
+        b = i % nbuf
         stream.wait_event(in_ready[b])
-        if i >= 2:
-            stream.wait_event(out_done[b])  # step i-2's output has been read back
+        if i >= nbuf:
+            stream.wait_event(out_done[b])  # step i-nbuf's output has been read back
         with torch.cuda.stream(stream):
             compute(b)
         done[b].record(stream)
-        if i + 1 < n_steps:
-            if i >= 1:
-                s_in.wait_event(done[1 - b])  # step i-1 has read that input buffer
+        nxt = i + nbuf - 1
+        if nxt < n_steps:
+            bn = nxt % nbuf
+            if nxt >= nbuf:
+                s_in.wait_event(done[bn])  # step nxt-nbuf has read that input buffer
             with torch.cuda.stream(s_in):
-                copy_in(1 - b)
-            in_ready[1 - b].record(s_in)
+                copy_in(bn)
+            in_ready[bn].record(s_in)
         s_out.wait_event(done[b])
         with torch.cuda.stream(s_out):
             copy_out(b)
         out_done[b].record(s_out)
-    stream.wait_event(out_done[(n_steps - 1) & 1])
+    stream.wait_event(out_done[(n_steps - 1) % nbuf])
     t1.record(stream)
     torch.cuda.synchronize()
     return t0.elapsed_time(t1) / n_steps
@@ -712,16 +718,17 @@ def decode_record(pkv, args, workload, dev, stream, world, K, extras, rank):
     for n, x in srcs:
         offs[n] = total
         total += -(-x.numel() * x.element_size() // 256) * 256
-    stage_host = [torch.zeros(total, dtype=torch.uint8).pin_memory() for _ in range(2)]
-    stage_dev = [torch.empty(total, dtype=torch.uint8, device=dev) for _ in range(2)]
-    dev_in = [{}, {}]
-    for bb in range(2):
+    NBUF = max(2, args.e2e_buffers)
+    stage_host = [torch.zeros(total, dtype=torch.uint8).pin_memory() for _ in range(NBUF)]
+    stage_dev = [torch.empty(total, dtype=torch.uint8, device=dev) for _ in range(NBUF)]
+    dev_in = [{} for _ in range(NBUF)]
+    for bb in range(NBUF):
         for n, x in srcs:
             nb = x.numel() * x.element_size()
             stage_host[bb][offs[n]:offs[n] + nb].copy_(x.cpu().contiguous().view(-1).view(torch.uint8))
             dev_in[bb][n] = stage_dev[bb][offs[n]:offs[n] + nb].view(x.dtype).view(x.shape)
-    outs = [out, torch.empty_like(out)]
-    out_host = [torch.empty(out.shape, dtype=out.dtype).pin_memory() for _ in range(2)]
+    outs = [out] + [torch.empty_like(out) for _ in range(NBUF - 1)]
+    out_host = [torch.empty(out.shape, dtype=out.dtype).pin_memory() for _ in range(NBUF)]
     h2d = sum(x.numel() * x.element_size() for _, x in srcs)
     d2h = out_host[0].numel() * out_host[0].element_size()
     K_e2e = max(10, K // 4)
@@ -737,14 +744,14 @@ def decode_record(pkv, args, workload, dev, stream, world, K, extras, rank):
             lambda bb: stage_dev[bb].copy_(stage_host[bb], non_blocking=True),
             lambda bb: enqueue(args.path, *[dev_in[bb][n] for n in names], o=outs[bb]),
             lambda bb: out_host[bb].copy_(outs[bb], non_blocking=True),
-            hold_ms=queue_ahead_ms(4 * host_ms, n_steps))
+            hold_ms=queue_ahead_ms(4 * host_ms, n_steps), nbuf=NBUF)
 
     for _ in range(3):
         e2e_serial_step()
     e2e_serial_ms = timed_steps(e2e_serial_step, K_e2e, stream, 4 * host_ms) / K_e2e
     e2e_pipelined(4)
     e2e_ms = e2e_pipelined(K_e2e)
-    if not torch.equal(out_host[(K_e2e - 1) & 1], out.cpu()):
+    if not torch.equal(out_host[(K_e2e - 1) % NBUF], out.cpu()):
         raise RuntimeError("pipelined end-to-end output differs from the device output")
     del stage_host, stage_dev, dev_in, outs, out_host
 
