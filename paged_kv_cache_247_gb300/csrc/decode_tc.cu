@@ -350,81 +350,79 @@ __global__ void __launch_bounds__(TcShape<NH, D>::kThreads, 1)
     __syncwarp();
   } else if (warp == L::kSWarp || warp == L::kOWarp) {
     // ------------------------------------------------------------ issuers
-    if (lane == 0) {
-      constexpr bool bf16 = std::is_same<T, __nv_bfloat16>::value;
-      const bool is_s = warp == L::kSWarp;
-      const uint32_t idesc = is_s ? instr_desc(bf16, false, false, N, kKeys)
-                                  : (L::kTrans ? instr_desc(bf16, true, false, N, D)
-                                               : instr_desc(bf16, false, true, D, kKeys));
-      const uint32_t aK = smem_addr(sK), aV = smem_addr(sV), aQ = smem_addr(sQ),
-                     aP = smem_addr(sP);
-      int kt = 0, k_item = 0;
-      bool ok = true;
-      for (int j = blockIdx.x; ok && j < num_items; j += gridDim.x) {
-        const Item it = item_at(p, j);
-        if (it.n_tiles == 0) continue;
-        const int b = k_item & 1;
-        if (is_s) {
-          if (!mbar_wait(&q_full[b], (k_item >> 1) & 1, p.status)) break;
-          for (int i = 0; i < it.n_tiles; ++i, ++kt) {
-            const int st = kt % S;
-            if (!mbar_wait(&k_full[st], (kt / S) & 1, p.status) ||
-                (kt >= SB && !mbar_wait(&s_free[kt % SB], ((kt / SB) - 1) & 1, p.status))) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            // S^T = K . Q^T: 16 dimensions per MMA; a 32-byte step inside the
-            // 128-byte rows, then the next 64-column atom.
-#pragma unroll
-            for (int ks = 0; ks < D / 16; ++ks)
-              mma_f16_ss(tmem + (kt % SB) * N,
-                         smem_desc(aK + st * kKvTile + (ks / 4) * 1024 + (ks % 4) * 32, 16,
-                                   kGroupKV),
-                         smem_desc(aQ + b * L::kQBytes + (ks / 4) * (N * 128) + (ks % 4) * 32,
-                                   16, 1024),
-                         idesc, ks > 0 ? 1u : 0u);
-            mma_commit(&s_full[kt % SB]);
-            mma_commit(&k_empty[st]);
+    // The whole warp runs the loop and one elected lane issues.
+    constexpr bool bf16 = std::is_same<T, __nv_bfloat16>::value;
+    const bool is_s = warp == L::kSWarp;
+    const uint32_t idesc = is_s ? instr_desc(bf16, false, false, N, kKeys)
+                                : (L::kTrans ? instr_desc(bf16, true, false, N, D)
+                                             : instr_desc(bf16, false, true, D, kKeys));
+    const uint32_t aK = smem_addr(sK), aV = smem_addr(sV), aQ = smem_addr(sQ),
+                   aP = smem_addr(sP);
+    int kt = 0, k_item = 0;
+    bool ok = true;
+    for (int j = blockIdx.x; ok && j < num_items; j += gridDim.x) {
+      const Item it = item_at(p, j);
+      if (it.n_tiles == 0) continue;
+      const int b = k_item & 1;
+      if (is_s) {
+        if (!mbar_wait_warp(&q_full[b], (k_item >> 1) & 1, p.status)) break;
+        for (int i = 0; i < it.n_tiles; ++i, ++kt) {
+          const int st = kt % S;
+          if (!mbar_wait_warp(&k_full[st], (kt / S) & 1, p.status) ||
+              (kt >= SB && !mbar_wait_warp(&s_free[kt % SB], ((kt / SB) - 1) & 1, p.status))) {
+            ok = false;
+            break;
           }
-          if (ok) mma_commit(&q_empty[b]);
-        } else {
-          if (k_item >= 2 && !mbar_wait(&o_free[b], ((k_item - 2) >> 1) & 1, p.status)) break;
-          for (int i = 0; i < it.n_tiles; ++i, ++kt) {
-            const int st = kt % S;
-            if (!mbar_wait(&v_full[st], (kt / S) & 1, p.status) ||
-                !mbar_wait(&p_full[kt % SB], (kt / SB) & 1, p.status)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            // O^T += V^T P^T (D = 128) or O += P V (D = 64): 16 keys per
-            // MMA, two 8-key groups of V and a 32-byte step inside P^T's
-            // 128-byte rows.
+          tc_fence_after();
+          // S^T = K . Q^T: 16 dimensions per MMA; a 32-byte step inside the
+          // 128-byte rows, then the next 64-column atom.
 #pragma unroll
-            for (int ks = 0; ks < kKeys / 16; ++ks) {
-              const uint64_t dv =
-                  smem_desc(aV + st * kKvTile + ks * 2 * kGroupKV, 1024, kGroupKV);
-              const uint64_t dp =
-                  smem_desc(aP + (kt % SB) * L::kPBuf + (ks / 4) * 1024 + (ks % 4) * 32, 16,
-                            L::kTrans ? kGroupP : L::kPGroupStride);
-              if constexpr (L::kTrans)
-                mma_f16_ss(tmem + L::kColO + b * L::kOCols, dv, dp, idesc,
-                           (i > 0 || ks > 0) ? 1u : 0u);
-              else
-                mma_f16_ss(tmem + L::kColO + b * L::kOCols, dp, dv, idesc,
-                           (i > 0 || ks > 0) ? 1u : 0u);
-            }
-            mma_commit(&p_free[kt % SB]);
-            mma_commit(&v_empty[st]);
-          }
+          for (int ks = 0; ks < D / 16; ++ks)
+            mma_f16_ss_warp(tmem + (kt % SB) * N,
+                            smem_desc(aK + st * kKvTile + (ks / 4) * 1024 + (ks % 4) * 32, 16,
+                                      kGroupKV),
+                            smem_desc(aQ + b * L::kQBytes + (ks / 4) * (N * 128) + (ks % 4) * 32,
+                                      16, 1024),
+                            idesc, ks > 0 ? 1u : 0u);
+          mma_commit_warp(&s_full[kt % SB]);
+          mma_commit_warp(&k_empty[st]);
         }
-        ++k_item;
+        if (ok) mma_commit_warp(&q_empty[b]);
+      } else {
+        if (k_item >= 2 && !mbar_wait_warp(&o_free[b], ((k_item - 2) >> 1) & 1, p.status)) break;
+        for (int i = 0; i < it.n_tiles; ++i, ++kt) {
+          const int st = kt % S;
+          if (!mbar_wait_warp(&v_full[st], (kt / S) & 1, p.status) ||
+              !mbar_wait_warp(&p_full[kt % SB], (kt / SB) & 1, p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          // O^T += V^T P^T (D = 128) or O += P V (D = 64): 16 keys per
+          // MMA, two 8-key groups of V and a 32-byte step inside P^T's
+          // 128-byte rows.
+#pragma unroll
+          for (int ks = 0; ks < kKeys / 16; ++ks) {
+            const uint64_t dv = smem_desc(aV + st * kKvTile + ks * 2 * kGroupKV, 1024, kGroupKV);
+            const uint64_t dp =
+                smem_desc(aP + (kt % SB) * L::kPBuf + (ks / 4) * 1024 + (ks % 4) * 32, 16,
+                          L::kTrans ? kGroupP : L::kPGroupStride);
+            if constexpr (L::kTrans)
+              mma_f16_ss_warp(tmem + L::kColO + b * L::kOCols, dv, dp, idesc,
+                              (i > 0 || ks > 0) ? 1u : 0u);
+            else
+              mma_f16_ss_warp(tmem + L::kColO + b * L::kOCols, dp, dv, idesc,
+                              (i > 0 || ks > 0) ? 1u : 0u);
+          }
+          mma_commit_warp(&p_free[kt % SB]);
+          mma_commit_warp(&v_empty[st]);
+        }
       }
-      uint64_t* d = &drain[is_s ? 0 : 1];
-      mma_commit(d);
-      mbar_drain(d, 0);
+      ++k_item;
     }
+    uint64_t* d = &drain[is_s ? 0 : 1];
+    mma_commit_warp(d);
+    mbar_drain(d, 0);
     __syncwarp();
   } else {
     // ----------------------------------------------------- key warpgroups

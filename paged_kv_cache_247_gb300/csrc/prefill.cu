@@ -274,38 +274,37 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     // ------------------------------------------------------ Q K^T issuer
     // S_t of key tile i overwrites P_t of tile i - 1, so it waits for that
     // P V; row tile 0 goes first and its softmax overlaps tile 1's MMAs.
-    if (lane == 0) {
-      constexpr bool bf16 = std::is_same<T, __nv_bfloat16>::value;
-      const uint32_t idesc_s = instr_desc(bf16, false, false, kBN, kBM);
-      const uint32_t aQ = smem_addr(sQ), aK = smem_addr(sK);
-      bool ok = true;
-      for (int i = 0; ok && i < n_tiles; ++i) {
-        const int st = i % kStages;
-        if (!mbar_wait(&k_full[st], (i / kStages) & 1, p.status)) break;
+    // The whole warp runs the loop and one elected lane issues.
+    constexpr bool bf16 = std::is_same<T, __nv_bfloat16>::value;
+    const uint32_t idesc_s = instr_desc(bf16, false, false, kBN, kBM);
+    const uint32_t aQ = smem_addr(sQ), aK = smem_addr(sK);
+    bool ok = true;
+    for (int i = 0; ok && i < n_tiles; ++i) {
+      const int st = i % kStages;
+      if (!mbar_wait_warp(&k_full[st], (i / kStages) & 1, p.status)) break;
 #pragma unroll
-        for (int t = 0; t < kRowTiles; ++t) {
-          if (i >= n_t[t]) continue;
-          const bool ready = i == 0 ? mbar_wait(&q_full[t], 0, p.status)
-                                    : mbar_wait(&pv_done[t], (i - 1) & 1, p.status);
-          if (!ready) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-#pragma unroll
-          for (int ks = 0; ks < D / 16; ++ks) {
-            const uint32_t koff = (ks / 4) * 1024 + (ks % 4) * 32;
-            mma_f16_ss(tmem + t * kBN,
-                       smem_desc(aQ + t * L::kQTile + koff, 16, L::kGroup),
-                       smem_desc(aK + st * L::kKvTile + koff, 16, L::kGroup), idesc_s, ks > 0);
-          }
-          mma_commit(&s_full[t]);
+      for (int t = 0; t < kRowTiles; ++t) {
+        if (i >= n_t[t]) continue;
+        const bool ready = i == 0 ? mbar_wait_warp(&q_full[t], 0, p.status)
+                                  : mbar_wait_warp(&pv_done[t], (i - 1) & 1, p.status);
+        if (!ready) {
+          ok = false;
+          break;
         }
-        if (ok) mma_commit(&k_empty[st]);
+        tc_fence_after();
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t koff = (ks / 4) * 1024 + (ks % 4) * 32;
+          mma_f16_ss_warp(tmem + t * kBN, smem_desc(aQ + t * L::kQTile + koff, 16, L::kGroup),
+                          smem_desc(aK + st * L::kKvTile + koff, 16, L::kGroup), idesc_s,
+                          ks > 0);
+        }
+        mma_commit_warp(&s_full[t]);
       }
-      mma_commit(&drain[0]);
-      mbar_drain(&drain[0], 0);
+      if (ok) mma_commit_warp(&k_empty[st]);
     }
+    mma_commit_warp(&drain[0]);
+    mbar_drain(&drain[0], 0);
     __syncwarp();
   } else if (warp == kPvWarp) {
     // --------------------------------------------------------- P V issuer
@@ -339,28 +338,22 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
             ok = false;
             break;
           }
-          if (lane == 0) {
-            tc_fence_after();
-            // V as an MN-major operand: 8-key groups kGroup bytes apart,
-            // 64-column atoms 1024 bytes apart.
+          tc_fence_after();
+          // V as an MN-major operand: 8-key groups kGroup bytes apart,
+          // 64-column atoms 1024 bytes apart.
 #pragma unroll
-            for (int ks = h * kBN / 32; ks < (h + 1) * kBN / 32; ++ks)
-              mma_f16_ta(tmem + L::kColO + t * D, tmem + t * kBN + ks * 8,
-                         smem_desc(aV + st * L::kKvTile + ks * 2 * L::kGroup, 1024, L::kGroup),
-                         idesc_o, (i > 0 || ks > 0) ? 1u : 0u);
-          }
-          __syncwarp();
+          for (int ks = h * kBN / 32; ks < (h + 1) * kBN / 32; ++ks)
+            mma_f16_ta_warp(tmem + L::kColO + t * D, tmem + t * kBN + ks * 8,
+                            smem_desc(aV + st * L::kKvTile + ks * 2 * L::kGroup, 1024, L::kGroup),
+                            idesc_o, (i > 0 || ks > 0) ? 1u : 0u);
         }
         if (!ok) break;
-        if (lane == 0) mma_commit(&pv_done[t]);
-        __syncwarp();
+        mma_commit_warp(&pv_done[t]);
       }
-      if (ok && lane == 0) mma_commit(&v_empty[st]);
+      if (ok) mma_commit_warp(&v_empty[st]);
     }
-    if (lane == 0) {
-      mma_commit(&drain[1]);
-      mbar_drain(&drain[1], 0);
-    }
+    mma_commit_warp(&drain[1]);
+    mbar_drain(&drain[1], 0);
     __syncwarp();
   } else if (warp < kSoftmaxWarps) {
     // ------------------------------------------- softmax / epilogue (rows)

@@ -43,29 +43,39 @@ __device__ __forceinline__ uint32_t instr_desc(bool bf16, bool a_mn_major, bool 
          ((uint32_t)(m >> 4) << 24);
 }
 
+// The MMA and commit helpers are warp-collective: every lane of a converged
+// warp calls them with the same arguments and one lane, chosen by
+// elect.sync, issues the instruction.  Issuing from a converged warp keeps
+// the descriptors in the warp's uniform registers: on GB300 one warp then
+// issues an MMA about every 40 cycles, against about 64 when a branch taken
+// by a single lane issues it.
+
 // D (+)= A.B with both operands described by shared-memory descriptors.
-__device__ __forceinline__ void mma_f16_ss(uint32_t d_tmem, uint64_t a, uint64_t b,
-                                           uint32_t idesc, uint32_t accumulate) {
+__device__ __forceinline__ void mma_f16_ss_warp(uint32_t d_tmem, uint64_t a, uint64_t b,
+                                                uint32_t idesc, uint32_t accumulate) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "{\n\t.reg .pred p, e;\n\telect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
 }
 
 // D (+)= A.B with the A operand read from tensor memory (row r in lane r,
 // element pairs packed low-first, 8 columns per 16 elements of K) and B
 // described by a shared-memory descriptor.
-__device__ __forceinline__ void mma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
-                                           uint32_t idesc, uint32_t accumulate) {
+__device__ __forceinline__ void mma_f16_ta_warp(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
+                                                uint32_t idesc, uint32_t accumulate) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "{\n\t.reg .pred p, e;\n\telect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
       "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate));
 }
 
-__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+// The barrier completes once every MMA issued before by the elected lane
+// (elect.sync picks the same lane of a converged warp every time) has.
+__device__ __forceinline__ void mma_commit_warp(uint64_t* bar) {
   asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
           smem_addr(bar))
       : "memory");
 }
