@@ -297,8 +297,9 @@ size_t pkv_contiguous_workspace_size(int num_seqs, int num_q_heads, int num_kv_h
  * Q.K and P.V run on the tensor cores (fp32 accumulation); the softmax
  * weights P are rounded to dtype before P.V, as the operand type requires.
  *
- *   q, out        [total_queries, num_q_heads, head_dim] dtype, total =
- *                 query_start[num_seqs]
+ *   q, out        [total_queries, num_q_heads, head_dim] dtype, with
+ *                 total_queries >= query_start[num_seqs] (rows of either past
+ *                 total_queries are neither read nor written)
  *   query_start   int32 [num_seqs + 1], non-decreasing, starting at 0
  *   max_query_len host-side bound on L_s (sizes the grid)
  *   context_lens  int32 [num_seqs] with L_s <= context_lens[s] <= max_context_len
@@ -309,7 +310,7 @@ size_t pkv_contiguous_workspace_size(int num_seqs, int num_q_heads, int num_kv_h
  * exceeds 2^31 - 1), PKV_ERR_CUDA.
  * ---------------------------------------------------------------------- */
 pkv_status_t pkv_paged_attn_prefill(
-    void* out, const void* q, const int32_t* query_start, int max_query_len,
+    void* out, const void* q, int total_queries, const int32_t* query_start, int max_query_len,
     const void* k_cache, const void* v_cache,
     const int32_t* block_tables, int max_blocks_per_seq,
     const int32_t* context_lens, int max_context_len,

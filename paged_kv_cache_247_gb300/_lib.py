@@ -52,8 +52,8 @@ SIGNATURES = {
         c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int,
         c_float, c_int, c_int, c_void_p, c_size_t, c_void_p]),
     "pkv_paged_attn_prefill": (c_int, [
-        c_void_p, c_void_p, c_void_p, c_int, c_void_p, c_void_p, c_void_p, c_int, c_void_p,
-        c_int, c_int, c_int, c_int, c_int, c_int, c_int, c_float, c_int, c_void_p]),
+        c_void_p, c_void_p, c_int, c_void_p, c_int, c_void_p, c_void_p, c_void_p, c_int,
+        c_void_p, c_int, c_int, c_int, c_int, c_int, c_int, c_int, c_float, c_int, c_void_p]),
     "pkv_decode_partition_size": (c_int, [c_int, c_int, c_int, c_int, c_int]),
     "pkv_set_decode_path": (c_int, [c_int]),
     "pkv_get_decode_path": (c_int, []),

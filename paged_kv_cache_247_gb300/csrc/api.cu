@@ -478,8 +478,9 @@ pkv_status_t pkv_contiguous_attn_decode(void* out, const void* q, const void* k_
   return PKV_OK;
 }
 
-pkv_status_t pkv_paged_attn_prefill(void* out, const void* q, const int32_t* query_start,
-                                    int max_query_len, const void* k_cache, const void* v_cache,
+pkv_status_t pkv_paged_attn_prefill(void* out, const void* q, int total_queries,
+                                    const int32_t* query_start, int max_query_len,
+                                    const void* k_cache, const void* v_cache,
                                     const int32_t* block_tables, int max_blocks_per_seq,
                                     const int32_t* context_lens, int max_context_len,
                                     int num_seqs, int num_q_heads, int num_kv_heads,
@@ -488,11 +489,11 @@ pkv_status_t pkv_paged_attn_prefill(void* out, const void* q, const int32_t* que
   if (!decode_shape_ok(num_seqs, num_q_heads, num_kv_heads, max_context_len))
     return PKV_ERR_INVALID_ARG;
   if (dtype != PKV_F16 && dtype != PKV_BF16) return PKV_ERR_INVALID_ARG;
-  if (!isfinite(scale) || max_query_len < 0) return PKV_ERR_INVALID_ARG;
+  if (!isfinite(scale) || max_query_len < 0 || total_queries < 0) return PKV_ERR_INVALID_ARG;
   if (head_dim != 64 && head_dim != 128) return PKV_ERR_UNSUPPORTED;
   if (!supported_block_size(block_size)) return PKV_ERR_UNSUPPORTED;
   if (num_q_heads / num_kv_heads > 128) return PKV_ERR_UNSUPPORTED;
-  if (num_seqs == 0 || max_query_len == 0) return PKV_OK;
+  if (num_seqs == 0 || max_query_len == 0 || total_queries == 0) return PKV_OK;
   if (!out || !q || !query_start || !k_cache || !v_cache || !block_tables || !context_lens)
     return PKV_ERR_INVALID_ARG;
   if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
@@ -508,6 +509,7 @@ pkv_status_t pkv_paged_attn_prefill(void* out, const void* q, const int32_t* que
   pkv::PrefillArgs a{};
   a.out = out;
   a.q = q;
+  a.total_queries = total_queries;
   a.query_start = query_start;
   a.max_query_len = max_query_len;
   a.k_cache = k_cache;

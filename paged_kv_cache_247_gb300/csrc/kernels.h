@@ -77,6 +77,7 @@ cudaError_t launch_contiguous_decode(const DecodeParams& p, int dtype, int head_
 struct PrefillArgs {
   void* out;
   const void* q;
+  int total_queries;  // rows of q and out
   const int32_t* query_start;
   int max_query_len;
   const void* k_cache;
@@ -97,8 +98,8 @@ struct PrefillArgs {
   int sm_count;  // SMs of the device (sizes the launch order's groups)
 };
 
-// unsupported is set when the tensor maps of the caches cannot be encoded or
-// the work needs more CTAs than a 1-D grid holds.
+// unsupported is set when the tensor maps of q or of the caches cannot be
+// encoded, or the work needs more CTAs than a 1-D grid holds.
 cudaError_t launch_paged_prefill(const PrefillArgs& a, cudaStream_t stream, bool* unsupported);
 
 // kv_append indexes (token, 16-byte chunk) pairs with 32 bits: a call may move

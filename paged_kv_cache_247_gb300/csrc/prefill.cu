@@ -16,19 +16,22 @@
 //
 //   warps 8, 10  producers, alternate 128-key tiles: read the tile's block
 //            ids, then load every (block, head) run of K and of V with one
-//            4-D TMA copy each (cp.async.bulk.tensor, 128-byte swizzle).
+//            4-D TMA copy each (cp.async.bulk.tensor, 128-byte swizzle);
+//            warp 8 first loads the Q rows of both row tiles, one 4-D TMA
+//            copy per 8-row group.
 //   warp 9   issues S_t = Q_t K^T for both row tiles t (Q from shared
 //            memory); allocates and frees the tensor memory.
 //   warp 11  issues O_t += P_t V (P from tensor memory, V as an MN-major
 //            operand); clears V rows past the context first.
 //   warps 0-3, 4-7  softmax, one warpgroup per row tile and one thread per
-//            row: each writes its Q rows into shared memory, then per key
-//            tile reads its S row (tcgen05.ld) for the row max (diagonal
-//            masked), keeps the running max and sum in base 2 (lazy
+//            row: per key tile it reads its S row for the row max (off the
+//            diagonal with tcgen05.ld.red, which returns each 32-column
+//            chunk's maximum with the values; on the diagonal with a masked
+//            pass), keeps the running max and sum in base 2 (lazy
 //            rescaling, O rescaled in place when the max moved), then
-//            re-reads S half a row at a time for the exponentials and writes
-//            each half of P over S in tensor memory, releasing it to P V at
-//            once; at the end it normalises and stores its O row.
+//            computes the exponentials half a row at a time and writes each
+//            half of P over S in tensor memory, releasing it to P V at once;
+//            at the end it normalises and stores its O row.
 //
 // Work items (one per CTA) are (query tile, KV head, sequence).  The (sequence,
 // KV head) pairs go in groups of about one wave of items, and within a group
@@ -113,6 +116,7 @@ struct PrefillParams {
   int num_seqs;
   int q_tiles;          // CTAs per (sequence, KV head)
   int pairs_per_group;  // (sequence, KV head) pairs whose items are launched together
+  int total_queries;    // rows of q and out
 };
 
 // Byte offset of 16-byte chunk c of row r in a tile of the layout above.
@@ -125,7 +129,8 @@ __device__ __forceinline__ uint32_t tile_chunk_offset(int r, int c) {
 
 template <typename T, int D>
 __global__ void __launch_bounds__(kPrefillThreads, 1)
-    paged_prefill_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap kmap,
+    paged_prefill_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap qmap,
+                         const __grid_constant__ CUtensorMap kmap,
                          const __grid_constant__ CUtensorMap vmap) {
   using L = PrefillSmem<D>;
   extern __shared__ unsigned char smem_raw[];
@@ -139,7 +144,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
   uint64_t* k_empty = k_full + kStages;       // K slot consumed by both Q K^T (MMA commit)
   uint64_t* v_full = k_empty + kStages;       // V slot landed
   uint64_t* v_empty = v_full + kStages;       // V slot consumed by both P V
-  uint64_t* q_full = v_empty + kStages;       // [t] Q rows of tile t in shared memory
+  uint64_t* q_full = v_empty + kStages;       // [t] Q rows of tile t landed (TMA bytes)
   uint64_t* s_full = q_full + kRowTiles;      // [t] S_t computed (MMA commit)
   uint64_t* p_full = s_full + kRowTiles;      // [t][h] keys of half h of P_t written
                                               // (after O_t was rescaled; softmax)
@@ -198,7 +203,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       mbar_init(&v_empty[i], 1);
     }
     for (int t = 0; t < kRowTiles; ++t) {
-      mbar_init(&q_full[t], kBM);
+      mbar_init(&q_full[t], 1);
       mbar_init(&s_full[t], 1);
       mbar_init(&p_full[2 * t], kBM);
       mbar_init(&p_full[2 * t + 1], kBM);
@@ -238,6 +243,24 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     };
     int phys_next = table_entry(first);
     int last_k = -1, last_v = -1;  // last tiles whose copies this warp issued
+    // Warp 8 first loads the Q rows of both row tiles: one copy per 8-row
+    // group, lane = group, box_heads heads x box_tokens queries.  Heads past
+    // the group and queries past the sequence are copied too (their rows are
+    // masked out and never written); rows past the end of q read as zero.
+    if (first == 0) {
+      const int hg = Gp > 8 ? Gp / 8 : 1;   // groups per query
+      const int tpg = Gp > 8 ? 1 : 8 / Gp;  // queries per group
+#pragma unroll
+      for (int t = 0; t < kRowTiles; ++t) {
+        if (n_t[t] == 0) continue;
+        if (lane == 0) mbar_arrive_expect_tx(&q_full[t], L::kQTile);
+        __syncwarp();
+        if (lane < kBM / 8)
+          tma_load_token_heads(sQ + t * L::kQTile + lane * L::kGroup, &qmap,
+                               kvh * G + (lane % hg) * 8, q0 + j0 + t * qpt + (lane / hg) * tpg,
+                               &q_full[t]);
+      }
+    }
     for (int i = first; i < n_tiles; i += 2) {
       const int st = i % kStages;
       const uint32_t ph = ((i / kStages) - 1) & 1;
@@ -269,6 +292,11 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     // CTA leaves: wait, bounded, for the last slots this warp filled.
     if (last_k >= 0) mbar_drain(&k_full[last_k % kStages], (last_k / kStages) & 1);
     if (last_v >= 0) mbar_drain(&v_full[last_v % kStages], (last_v / kStages) & 1);
+    if (first == 0) {
+#pragma unroll
+      for (int t = 0; t < kRowTiles; ++t)
+        if (n_t[t] > 0) mbar_drain(&q_full[t], 0);
+    }
     __syncwarp();
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------ Q K^T issuer
@@ -362,29 +390,13 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     const int nt = n_t[t];
     const int jq = j0 + t * qpt + r / Gp;
     const int g = r % Gp;
-    const bool row_valid = (r / Gp) < qpt && jq < nq && g < G;
+    const bool row_valid = jq < nq && g < G && q0 + jq < p.total_queries;
     const int pos = row_valid ? ctx - nq + jq : -1;
     const size_t row_elem =
         ((size_t)(q0 + (row_valid ? jq : 0)) * p.num_q_heads + kvh * G + (row_valid ? g : 0)) * D;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t tmem_s = tmem + t * kBN + lane_base;
     const uint32_t tmem_o = tmem + L::kColO + t * D + lane_base;
-
-    // This row of Q into shared memory, in the K-major operand layout: all
-    // of the row's loads are issued before the first store, so the row costs
-    // one memory latency, not one per 16 bytes.
-    {
-      const uint4* src = reinterpret_cast<const uint4*>(static_cast<const T*>(p.q) + row_elem);
-      unsigned char* dst = sQ + t * L::kQTile;
-      uint4 v[D / 8];
-#pragma unroll
-      for (int c = 0; c < D / 8; ++c) v[c] = row_valid ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
-#pragma unroll
-      for (int c = 0; c < D / 8; ++c)
-        *reinterpret_cast<uint4*>(dst + tile_chunk_offset<D>(r, c)) = v[c];
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      mbar_arrive(&q_full[t]);
-    }
 
     float m_run = -CUDART_INF_F, l_run = 0.f;
     bool ok = true;
@@ -397,35 +409,46 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       // its position (the diagonal); elsewhere every key is visible.
       const int key0 = i * kBN;
       const bool diag = __any_sync(0xffffffffu, key0 + kBN - 1 > pos);
-      // First pass over the S row: its maximum.  The exponentials re-read
-      // S from tensor memory half a row at a time, which keeps the live
-      // registers to half a row.
+      // The row maximum.  Off the diagonal, tcgen05.ld.red returns each
+      // 32-column chunk's maximum with its values: the row is read half at a
+      // time for the maxima alone (the values are read again below), and no
+      // comparisons are needed.  On the diagonal (masked keys must not
+      // count) the whole row is read and masked.
       float mt;
-      {
+      if (!diag) {
+        float c[4];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          float sv[kBN / 2];
+          tmem_ld32f_max(tmem_s + h * (kBN / 2), sv, &c[2 * h]);
+          tmem_ld32f_max(tmem_s + h * (kBN / 2) + 32, sv + 32, &c[2 * h + 1]);
+          tmem_wait_ld_bind_max(sv, &c[2 * h]);
+          tmem_wait_ld_bind_max(sv + 32, &c[2 * h + 1]);
+        }
+        mt = fmaxf(fmax3(c[0], c[1], c[2]), c[3]) * p.qscale;
+      } else {
         float sv[kBN];
 #pragma unroll
         for (int c = 0; c < kBN / 32; ++c) tmem_ld32f(tmem_s + c * 32, sv + c * 32);
 #pragma unroll
         for (int c = 0; c < kBN / 32; ++c) tmem_wait_ld_bind(sv + c * 32);
-        if (diag) {
 #pragma unroll
-          for (int c = 0; c < kBN; ++c)
-            if (key0 + c > pos) sv[c] = -CUDART_INF_F;
-        }
-      // Row max with 8 independent chains (scaling by qscale > 0 commutes
-      // with the max).
-      float mx[8];
+        for (int c = 0; c < kBN; ++c)
+          if (key0 + c > pos) sv[c] = -CUDART_INF_F;
+        // Row max with 8 independent chains (scaling by qscale > 0 commutes
+        // with the max).
+        float mx[8];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) mx[k] = sv[k];
-      constexpr int kTriples = (kBN - 8) / 16;  // columns 8 .. 8 + 16 kTriples - 1, in threes
+        for (int k = 0; k < 8; ++k) mx[k] = sv[k];
+        constexpr int kTriples = (kBN - 8) / 16;  // columns 8 .. 8 + 16 kTriples - 1, in threes
 #pragma unroll
-      for (int c = 0; c < kTriples; ++c)
+        for (int c = 0; c < kTriples; ++c)
 #pragma unroll
-        for (int k = 0; k < 8; ++k) mx[k] = fmax3(mx[k], sv[8 + 16 * c + k], sv[16 + 16 * c + k]);
+          for (int k = 0; k < 8; ++k) mx[k] = fmax3(mx[k], sv[8 + 16 * c + k], sv[16 + 16 * c + k]);
 #pragma unroll
-      for (int c = 8 + 16 * kTriples; c < kBN; c += 8)
+        for (int c = 8 + 16 * kTriples; c < kBN; c += 8)
 #pragma unroll
-        for (int k = 0; k < 8; ++k) mx[k] = fmaxf(mx[k], sv[c + k]);
+          for (int k = 0; k < 8; ++k) mx[k] = fmaxf(mx[k], sv[c + k]);
         mt = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])) *
              p.qscale;
       }
@@ -531,9 +554,9 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
 // ---- host side ------------------------------------------------------------
 
 template <typename T, int D>
-cudaError_t launch_prefill_typed(const PrefillParams& p, const CUtensorMap& km,
-                                 const CUtensorMap& vm, int q_tiles, int num_seqs,
-                                 cudaStream_t stream) {
+cudaError_t launch_prefill_typed(const PrefillParams& p, const CUtensorMap& qm,
+                                 const CUtensorMap& km, const CUtensorMap& vm, int q_tiles,
+                                 int num_seqs, cudaStream_t stream) {
   using L = PrefillSmem<D>;
   static unsigned long long configured = 0;
   int dev = 0;
@@ -546,7 +569,7 @@ cudaError_t launch_prefill_typed(const PrefillParams& p, const CUtensorMap& km,
     if (dev < 64) __atomic_fetch_or(&configured, 1ull << dev, __ATOMIC_RELEASE);
   }
   const dim3 grid((unsigned)((long long)q_tiles * p.num_kv_heads * num_seqs));
-  paged_prefill_kernel<T, D><<<grid, kPrefillThreads, L::kBytes, stream>>>(p, km, vm);
+  paged_prefill_kernel<T, D><<<grid, kPrefillThreads, L::kBytes, stream>>>(p, qm, km, vm);
   return cudaGetLastError();
 }
 
@@ -563,6 +586,13 @@ cudaError_t launch_paged_prefill(const PrefillArgs& a, cudaStream_t stream, bool
   }
   int gp = 1;
   while (gp < a.num_q_heads / a.num_kv_heads) gp <<= 1;
+  // Q rows: 8-row groups of box_heads heads x box_tokens queries.
+  CUtensorMap qm;
+  if (!make_token_head_map(&qm, a.q, a.dtype, a.total_queries, a.num_q_heads, a.head_dim,
+                           gp < 8 ? gp : 8, gp < 8 ? 8 / gp : 1)) {
+    *unsupported = true;
+    return cudaErrorInvalidValue;
+  }
   PrefillParams p{};
   p.out = a.out;
   p.q = a.q;
@@ -587,18 +617,19 @@ cudaError_t launch_paged_prefill(const PrefillArgs& a, cudaStream_t stream, bool
   }
   p.num_seqs = a.num_seqs;
   p.q_tiles = q_tiles;
+  p.total_queries = a.total_queries;
   // About one wave of CTAs (one per SM) per group; the count only shapes
   // the order, not the result.
   const int pairs = a.num_kv_heads * a.num_seqs;
   p.pairs_per_group = std::max(1, std::min(pairs, a.sm_count / std::max(1, q_tiles)));
   if (a.dtype == PKV_F16) {
     return a.head_dim == 64
-               ? launch_prefill_typed<__half, 64>(p, km, vm, q_tiles, a.num_seqs, stream)
-               : launch_prefill_typed<__half, 128>(p, km, vm, q_tiles, a.num_seqs, stream);
+               ? launch_prefill_typed<__half, 64>(p, qm, km, vm, q_tiles, a.num_seqs, stream)
+               : launch_prefill_typed<__half, 128>(p, qm, km, vm, q_tiles, a.num_seqs, stream);
   }
   return a.head_dim == 64
-             ? launch_prefill_typed<__nv_bfloat16, 64>(p, km, vm, q_tiles, a.num_seqs, stream)
-             : launch_prefill_typed<__nv_bfloat16, 128>(p, km, vm, q_tiles, a.num_seqs, stream);
+             ? launch_prefill_typed<__nv_bfloat16, 64>(p, qm, km, vm, q_tiles, a.num_seqs, stream)
+             : launch_prefill_typed<__nv_bfloat16, 128>(p, qm, km, vm, q_tiles, a.num_seqs, stream);
 }
 
 }  // namespace pkv

@@ -103,6 +103,25 @@ __device__ __forceinline__ void tmem_ld32f(uint32_t taddr, float* v) {
       : "r"(taddr));
 }
 
+// The same load, which also returns the maximum of the 32 loaded values of
+// this thread's lane (tcgen05.ld.red with .max; on GB300 the loaded values
+// are returned unchanged and the maximum matches fmaxf over them).
+__device__ __forceinline__ void tmem_ld32f_max(uint32_t taddr, float* v, float* mx) {
+  asm volatile(
+      "tcgen05.ld.red.sync.aligned.32x32b.x32.max.f32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,"
+      "%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, %32, "
+      "[%33];"
+      : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3]), "=f"(v[4]), "=f"(v[5]), "=f"(v[6]),
+        "=f"(v[7]), "=f"(v[8]), "=f"(v[9]), "=f"(v[10]), "=f"(v[11]), "=f"(v[12]), "=f"(v[13]),
+        "=f"(v[14]), "=f"(v[15]), "=f"(v[16]), "=f"(v[17]), "=f"(v[18]), "=f"(v[19]),
+        "=f"(v[20]), "=f"(v[21]), "=f"(v[22]), "=f"(v[23]), "=f"(v[24]), "=f"(v[25]),
+        "=f"(v[26]), "=f"(v[27]), "=f"(v[28]), "=f"(v[29]), "=f"(v[30]), "=f"(v[31]), "=f"(*mx)
+      : "r"(taddr));
+}
+
+// Wait for this thread's outstanding tensor-memory loads, naming the loaded
+// registers (and, below, a reduction result) so that no use is scheduled
+// before the wait.
 __device__ __forceinline__ void tmem_wait_ld_bind(float* v) {
   asm volatile(
       "tcgen05.wait::ld.sync.aligned;"
@@ -111,6 +130,18 @@ __device__ __forceinline__ void tmem_wait_ld_bind(float* v) {
         "+f"(v[14]), "+f"(v[15]), "+f"(v[16]), "+f"(v[17]), "+f"(v[18]), "+f"(v[19]),
         "+f"(v[20]), "+f"(v[21]), "+f"(v[22]), "+f"(v[23]), "+f"(v[24]), "+f"(v[25]),
         "+f"(v[26]), "+f"(v[27]), "+f"(v[28]), "+f"(v[29]), "+f"(v[30]), "+f"(v[31])
+      :
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_ld_bind_max(float* v, float* mx) {
+  asm volatile(
+      "tcgen05.wait::ld.sync.aligned;"
+      : "+f"(v[0]), "+f"(v[1]), "+f"(v[2]), "+f"(v[3]), "+f"(v[4]), "+f"(v[5]), "+f"(v[6]),
+        "+f"(v[7]), "+f"(v[8]), "+f"(v[9]), "+f"(v[10]), "+f"(v[11]), "+f"(v[12]), "+f"(v[13]),
+        "+f"(v[14]), "+f"(v[15]), "+f"(v[16]), "+f"(v[17]), "+f"(v[18]), "+f"(v[19]),
+        "+f"(v[20]), "+f"(v[21]), "+f"(v[22]), "+f"(v[23]), "+f"(v[24]), "+f"(v[25]),
+        "+f"(v[26]), "+f"(v[27]), "+f"(v[28]), "+f"(v[29]), "+f"(v[30]), "+f"(v[31]), "+f"(*mx)
       :
       : "memory");
 }
@@ -189,6 +220,17 @@ __device__ __forceinline__ void tma_load_rows(void* dst, const CUtensorMap* map,
       "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%2, %3, %2}], [%4];" ::"r"(smem_addr(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(row), "r"(smem_addr(bar))
+      : "memory");
+}
+
+// Copy the box at coordinates (0, head, token, 0) of a 4-D map
+// (make_token_head_map).
+__device__ __forceinline__ void tma_load_token_heads(void* dst, const CUtensorMap* map, int head,
+                                                     int token, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %2}], [%5];" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(head), "r"(token), "r"(smem_addr(bar))
       : "memory");
 }
 
@@ -326,6 +368,29 @@ inline bool make_rows_map(CUtensorMap* map, const void* base, int dtype, long lo
                         dtype == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                           : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
                         3, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// 4-D view of query (or output) rows [tokens, heads, head_dim] for TMA:
+// (64 columns, heads, tokens, head_dim / 64 atoms), 128-byte swizzle.  A box
+// of box_heads x box_tokens = 8 rows lands as one 8-row group of the tile
+// layout above, token-major, every atom of the group in one copy; rows past
+// the end read as zero.
+inline bool make_token_head_map(CUtensorMap* map, const void* base, int dtype, long long tokens,
+                                int heads, int head_dim, int box_heads, int box_tokens) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+  if (!fn) return false;
+  const int atoms = head_dim / 64;
+  const cuuint64_t dims[4] = {64, (cuuint64_t)heads, (cuuint64_t)tokens, (cuuint64_t)atoms};
+  const cuuint64_t strides[3] = {(cuuint64_t)head_dim * 2, (cuuint64_t)heads * head_dim * 2, 128};
+  const cuuint32_t box[4] = {64, (cuuint32_t)box_heads, (cuuint32_t)box_tokens, (cuuint32_t)atoms};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUresult r = fn(map,
+                        dtype == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                          : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                        4, const_cast<void*>(base), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;

@@ -166,7 +166,7 @@ def paged_attn_prefill(out, q, query_start, k_cache, v_cache, block_tables, cont
     if block_tables.shape[0] != S or query_start.shape[0] != S + 1:
         raise ValueError("block_tables / query_start must match context_lens")
     st = _lib.load().pkv_paged_attn_prefill(
-        out.data_ptr(), q.data_ptr(), query_start.data_ptr(), int(max_query_len),
+        out.data_ptr(), q.data_ptr(), T, query_start.data_ptr(), int(max_query_len),
         k_cache.data_ptr(), v_cache.data_ptr(), block_tables.data_ptr(), block_tables.shape[1],
         context_lens.data_ptr(), int(max_context_len), S, Hq, Hkv, D, B, NB, float(scale),
         _DTYPE_CODE[dtype], _stream_handle(q.device))

@@ -167,10 +167,10 @@ def test_append_and_copy_host_validation(lib):
 
 
 def _prefill(lib, **over):
-    a = dict(out=16, q=16, qs=16, mql=8, k=16, v=16, tables=16, mbps=4, lens=16, maxctx=64, S=2,
-             Hq=8, Hkv=2, D=128, B=16, NB=10, scale=0.1, dtype=1)
+    a = dict(out=16, q=16, T=16, qs=16, mql=8, k=16, v=16, tables=16, mbps=4, lens=16, maxctx=64,
+             S=2, Hq=8, Hkv=2, D=128, B=16, NB=10, scale=0.1, dtype=1)
     a.update(over)
-    return lib.pkv_paged_attn_prefill(a["out"], a["q"], a["qs"], a["mql"], a["k"], a["v"],
+    return lib.pkv_paged_attn_prefill(a["out"], a["q"], a["T"], a["qs"], a["mql"], a["k"], a["v"],
                                       a["tables"], a["mbps"], a["lens"], a["maxctx"], a["S"],
                                       a["Hq"], a["Hkv"], a["D"], a["B"], a["NB"], a["scale"],
                                       a["dtype"], None)
@@ -193,6 +193,8 @@ def _prefill(lib, **over):
     (dict(S=70000), 2),                 # grid limit
     (dict(S=0, q=None), 0),             # empty batch is a no-op
     (dict(mql=0, q=None), 0),           # no queries: a no-op
+    (dict(T=-1), 1),                    # negative row count of q and out
+    (dict(T=0, q=None), 0),             # no rows: a no-op
 ])
 def test_prefill_host_validation(lib, over, expect):
     assert _prefill(lib, **over) == expect

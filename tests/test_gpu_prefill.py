@@ -8,12 +8,15 @@ query (which must agree with decode), several 128-row query tiles and
 128-key tiles, ragged and NaN-poisoned block tails, every block size and
 grouped heads."""
 
+import ctypes
+
 import numpy as np
 import pytest
 import torch
 
 import oracle
 import paged_kv_cache_247_gb300 as pkv
+from paged_kv_cache_247_gb300 import _lib
 from paged_kv_cache_247_gb300 import workloads as W
 from _gpu_util import TOL, assert_within_tol, to_f64
 
@@ -140,3 +143,34 @@ def test_prefill_empty_chunks_and_bad_context(cuda_device):
                                           case.block_tables.cpu().numpy()[1:], ok_lens[1:],
                                           qs2[1:] - 41, case.scale)
     assert_within_tol(out2[41:], ref2, torch.bfloat16, "prefill next to a bad sequence")
+
+
+def test_rows_past_total_queries_untouched(lib, cuda_device):
+    """q and out hold total_queries rows; with total_queries below
+    query_start[S] the rows from total_queries on are neither read (the Q
+    copies read zeros there) nor written, and the rows before it are exact.
+    Only the kernel's own bounds keep the last sequence's tail rows out of
+    memory that q and out do not own."""
+    lens = [300, 200]
+    chunks = [150, 100]
+    case = W.make_decode_case(31, len(lens), 32, 8, 128, 16, "bf16", lens, pool_factor=1.2,
+                              device=cuda_device)
+    qs = np.concatenate([[0], np.cumsum(chunks)]).astype(np.int32)
+    gen = torch.Generator(device=cuda_device).manual_seed(8)
+    q = torch.randn((int(qs[-1]), 32, 128), generator=gen, device=cuda_device).to(torch.bfloat16)
+    out = torch.full_like(q, float("nan"))
+    total = 190  # 40 rows of sequence 1 are inside, 60 past the end
+    qs_dev = torch.from_numpy(qs).to(cuda_device)
+    st = lib.pkv_paged_attn_prefill(
+        out.data_ptr(), q.data_ptr(), total, qs_dev.data_ptr(), max(chunks),
+        case.k_cache.data_ptr(), case.v_cache.data_ptr(), case.block_tables.data_ptr(),
+        case.block_tables.shape[1], case.context_lens.data_ptr(), case.max_context_len, 2, 32,
+        8, 128, 16, case.k_cache.shape[0], case.scale, _lib.PKV_BF16,
+        ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert st == 0
+    torch.cuda.synchronize()
+    assert torch.isnan(out[total:]).all()
+    ref = oracle.paged_prefill_attention(to_f64(q), to_f64(case.k_cache), to_f64(case.v_cache),
+                                         case.block_tables.cpu().numpy(),
+                                         case.context_lens.cpu().numpy(), qs, case.scale)
+    assert_within_tol(out[:total], ref[:total], torch.bfloat16, "rows below total_queries")
