@@ -839,8 +839,9 @@ def run_ours(args, rank, world, local_rank):
         sh = shared_line(args, rank, world, local_rank)
         line["shared_prefix"] = {k: sh[k] for k in (
             "value", "unit", "ms_per_step", "steps_per_s", "steps", "device_ms_per_step",
-            "kernel_ms_last_step", "logical_gbs_kernel", "allocator_us_per_step", "first_step",
-            "held_kv_bytes", "logical_kv_bytes_per_step", "config", "clocks")}
+            "kernel_ms_last_step", "logical_gbs_kernel", "dram_bytes_kernel", "dram_gbs_kernel",
+            "allocator_us_per_step", "first_step", "held_kv_bytes", "logical_kv_bytes_per_step",
+            "config", "clocks")}
         pf = prefill_line(args, rank, world, local_rank, with_cpu=False)
         line["prefill"] = {k: pf[k] for k in (
             "metric", "value", "unit", "ms_per_step", "config", "roofline", "e2e", "clocks")}
@@ -1145,6 +1146,10 @@ def shared_line(args, rank, world, local_rank):
                                      D ** -0.5, int(lens.max()), workspace=ws)
     krn_ms = time_alone(last_launch, None, stream, 20)
     krn_bytes = int(lens.sum()) * 2 * H * D * e
+    # DRAM bytes of one fused launch from the committed ncu summary (a launch of
+    # the timed steps, contexts within a few tokens of this one): shared prompt
+    # blocks are read once per launch from DRAM and again from L2.
+    dram = ncu_traffic("paged_decode_kernel:fused", "shared")
     clock_rec = clocks.stop()
     if pkv.device_status(clear=True) != 0:
         raise RuntimeError("device status flags during the shared-prefix bench")
@@ -1171,6 +1176,10 @@ def shared_line(args, rank, world, local_rank):
             "logical_gbs_kernel": round(krn_bytes / (krn_ms * 1e-3) / 1e9, 1),
             "kernel_note": "the last step's fused append + decode launch timed alone (20 calls), "
                            "launch outside the event pair, L2 as the loop leaves it",
+            "dram_bytes_kernel": dram,
+            "dram_gbs_kernel": round(dram / (krn_ms * 1e-3) / 1e9, 1) if dram else None,
+            "dram_note": "ncu dram__bytes_read.sum + dram__bytes_write.sum of one fused launch "
+                         "(profiles/traffic.json, null unless taken on the current source)",
             "allocator_us_per_step": round(1e6 * stats["alloc_s"] / K, 2),
             "first_step": {"cow_pairs": cow_pairs, "ms": round(1e3 * t_cow, 3)},
             "pool": {k: st[k] for k in st},
