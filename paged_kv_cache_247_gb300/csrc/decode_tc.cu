@@ -597,21 +597,41 @@ __global__ void __launch_bounds__(TcShape<NH, D>::kThreads, 1)
         mbar_arrive(&o_free[ob]);
         if (ok) {
           const int d = t;
+          // Every head's sum is read from shared memory before the first
+          // store (a store through a plain pointer would otherwise make each
+          // later read wait for it), and each head divides by one
+          // reciprocal: IEEE divisions, each with its own slow-path branch,
+          // ran one after another and cost more than the item's last tile.
+          float l[NHW], inv[NHW];
 #pragma unroll
           for (int g = 0; g < NHW; ++g) {
-            if (hb + g >= G) continue;
-            const float l = (red[g] + red[NHW + g]) + (red[2 * NHW + g] + red[3 * NHW + g]);
-            const float val = o[g] / l;
-            const size_t row = (size_t)it.s * p.num_q_heads + h0 + hb + g;
-            if (it.nparts_seq == 1) {
-              static_cast<T*>(p.out)[row * D + d] = static_cast<T>(val);
-            } else {
-              const size_t r = row * p.num_parts + it.part;
-              p.ws_o[r * D + d] = val;
-              if (d == 0) {
-                p.ws_m[r] = mref[g];
-                p.ws_l[r] = l;
+            l[g] = (red[g] + red[NHW + g]) + (red[2 * NHW + g] + red[3 * NHW + g]);
+            inv[g] = __fdividef(1.f, l[g]);
+          }
+          const size_t row0 = (size_t)it.s * p.num_q_heads + h0 + hb;
+          if (it.nparts_seq == 1) {
+            T* dst = static_cast<T*>(p.out) + row0 * D + d;
+#pragma unroll
+            for (int g = 0; g < NHW; ++g)
+              if (hb + g < G) dst[(size_t)g * D] = static_cast<T>(o[g] * inv[g]);
+          } else {
+            const size_t r0 = row0 * p.num_parts + it.part;
+            float* dst = p.ws_o + r0 * D + d;
+#pragma unroll
+            for (int g = 0; g < NHW; ++g)
+              if (hb + g < G) dst[(size_t)g * p.num_parts * D] = o[g] * inv[g];
+            // Thread g writes head g's maximum and sum (one thread writing
+            // them all took longer than the whole tile).
+            float mg = 0.f, lg = 0.f;
+#pragma unroll
+            for (int g = 0; g < NHW; ++g)
+              if (d == g) {
+                mg = mref[g];
+                lg = l[g];
               }
+            if (d < NHW && hb + d < G) {
+              p.ws_m[r0 + (size_t)d * p.num_parts] = mg;
+              p.ws_l[r0 + (size_t)d * p.num_parts] = lg;
             }
           }
         }
