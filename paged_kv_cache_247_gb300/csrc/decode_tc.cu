@@ -114,8 +114,7 @@ struct TcShape {
   static constexpr int kQ = 2 * kStages * kKvTile;  // after the K and V rings
   static constexpr int kP = kQ + 2 * kQBytes;
   static constexpr int kRed = kP + kSB * kPBuf;     // [KG][4 warps][NHW] floats
-  static constexpr int kMref = kRed + KG * 4 * NHW * 4;
-  static constexpr int kBar = kMref + KG * NHW * 4;
+  static constexpr int kBar = kRed + KG * 4 * NHW * 4;
   static constexpr int kTmemSlot = kBar + kBarSlots * 8;
   static constexpr int kBytes = kTmemSlot + 16 + 1024;  // + alignment slack
   static_assert(kBytes <= 227 * 1024, "shared memory overflow");
@@ -431,7 +430,6 @@ __global__ void __launch_bounds__(TcShape<NH, D>::kThreads, 1)
     const int hb = kg * NHW;             // first head of this warpgroup within the group
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     float* red = reinterpret_cast<float*>(smem + L::kRed) + kg * 4 * NHW;
-    float* mref_s = reinterpret_cast<float*>(smem + L::kMref) + kg * NHW;
     const float qs = p.qscale;
     if constexpr (!L::kTrans) {
       // P's rows past the group are read by the P V product but never
@@ -458,10 +456,15 @@ __global__ void __launch_bounds__(TcShape<NH, D>::kThreads, 1)
         continue;
       }
       const int ob = k_item & 1;
-      if (t < NHW) mref_s[t] = -CUDART_INF_F;
+      // The running maxima per head are the same in every thread of the
+      // warpgroup: all start at -inf and all take each move from the same
+      // tile maxima, so they stay in registers.
       float mref[NHW], l_part[NHW];
 #pragma unroll
-      for (int g = 0; g < NHW; ++g) l_part[g] = 0.f;
+      for (int g = 0; g < NHW; ++g) {
+        mref[g] = -CUDART_INF_F;
+        l_part[g] = 0.f;
+      }
       for (int i = 0; i < it.n_tiles; ++i, ++kt) {
         const int nvalid = min(kKeys, it.t_end - (it.t_begin + i * kKeys));
         const bool valid = t < nvalid;
@@ -474,9 +477,6 @@ __global__ void __launch_bounds__(TcShape<NH, D>::kThreads, 1)
         tmem_load_small<NHW>(tmem + (kt % SB) * N + hb + lane_base, x);
         tc_fence_before();
         mbar_arrive(&s_free[kt % SB]);
-        group_sync(kg);  // mref_s: reset for the item or last moved
-#pragma unroll
-        for (int g = 0; g < NHW; ++g) mref[g] = mref_s[g];
         bool exceed = false;
 #pragma unroll
         for (int g = 0; g < NHW; ++g) {
@@ -506,11 +506,7 @@ __global__ void __launch_bounds__(TcShape<NH, D>::kThreads, 1)
             mref[g] = mn;
             l_part[g] *= alpha[g];
           }
-          group_sync(kg);  // every thread has read red[] and the old maxima
-          if (t == 0) {
-#pragma unroll
-            for (int g = 0; g < NHW; ++g) mref_s[g] = mref[g];
-          }
+          group_sync(kg);  // every thread has read red[] before it is written again
           if (i > 0 && moved) {
             // O holds this item's tiles so far: once their MMAs are done
             // (P^T buffer of the previous tile released), rescale it.
