@@ -1228,7 +1228,8 @@ def sweep_line(args, rank, world, local_rank, block_sizes=None):
                 case = W.sweep_decode(B, S, ctx, device=dev)
                 Sq, Hq, D = case.q.shape
                 Hkv = case.k_cache.shape[1]
-                part = pkv.decode_partition_size(Sq, Hq, Hkv, D, case.max_context_len)
+                part = args.partition or pkv.decode_partition_size(Sq, Hq, Hkv, D,
+                                                                   case.max_context_len)
                 ws = torch.empty(max(16, pkv.decode_workspace_size(Sq, Hq, Hkv, D,
                                                                    case.max_context_len, part)),
                                  dtype=torch.uint8, device=dev)

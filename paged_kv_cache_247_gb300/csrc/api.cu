@@ -142,35 +142,48 @@ int auto_partition(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim
 }
 
 // Partition of the tensor-core decode kernel.  Its CTAs are persistent (one
-// per SM) and take the work items (sequence, KV head, partition) in turn, so
-// a CTA's share is ceil(items / SMs) items.  The choice minimises that share
-// in 128-key tiles, counting about half a tile per item for the switch
-// between items and four tiles for the split reduction when there is one
-// (its launch and one round trip through the workspace: about 2 us on
-// GB300, against about 0.6 us per tile for a CTA streaming alone).
+// per SM) and take the work items (sequence, KV head, partition) in turn.
+// The choice minimises a model of the call's time in units of one 128-key
+// tile streamed at an SM's share of HBM:
+//   * every SM works through floor(items / SMs) items at its share;
+//   * the remaining items run on fewer SMs, each of which streams at most
+//     about twice its share (the bytes its copy rings keep in flight);
+//   * each item costs about half a tile more (its output and the switch to
+//     the next item), and a split about two tiles (the partials' round trip
+//     and the merge).
+// On GB300 this picks the fastest of the partitions measured on 8 and 64
+// sequences x 1k to 32k tokens (query-head group 4) and on 32 sequences x
+// 4k tokens with groups of 2 to 32: two partitions where the sequences x KV
+// heads are fewer than the SMs or a few times more, none for 4k tokens over
+// 256 of them, where splitting at 1k cost 5-10 %.
 int tc_partition(int num_seqs, int num_kv_heads, int max_context_len) {
-  const long long units = (long long)num_seqs * num_kv_heads;
-  const long long sms = device_sms();
+  const double units = (double)num_seqs * num_kv_heads;
+  const double sms = (double)device_sms();
   const long long tiles = ((long long)max_context_len + pkv::kTcPartitionQuantum - 1) /
                           pkv::kTcPartitionQuantum;
   if (tiles <= 1) return pkv::kTcPartitionQuantum;
-  const int max_tiles = kMaxAutoPartition / pkv::kTcPartitionQuantum;
-  long long best_cost = -1;
-  int best = 1;
-  for (int pt = 1; pt <= max_tiles; ++pt) {
-    const long long parts = (tiles + pt - 1) / pt;
-    const long long per_item = tiles < pt ? tiles : pt;
-    const long long items = units * parts;
-    // costs in half tiles
-    const long long cost =
-        (items + sms - 1) / sms * (2 * per_item + 1) + (parts > 1 ? 8 : 0);
-    if (best_cost < 0 || cost <= best_cost) {  // ties: the longer partition
+  constexpr double kMaxRate = 2.0;    // an SM alone streams about twice its share
+  constexpr double kItemCost = 0.5;   // tiles per work item
+  constexpr double kSplitCost = 2.0;  // tiles for a split call
+  double best_cost = 0.0;
+  long long best = tiles;
+  // more than about eight rounds of items never pays: the search stops there
+  const double most = ceil(8.0 * sms / units);
+  for (long long parts = 1; parts <= tiles && (double)parts <= most; ++parts) {
+    const long long pt = (tiles + parts - 1) / parts;  // tiles per partition
+    if ((tiles + pt - 1) / pt != parts) continue;      // the same partition as fewer parts
+    const double items = units * (double)parts;
+    const double avg = (double)tiles / (double)parts;  // tiles per item
+    const double rounds = floor(items / sms);
+    const double rest = items - rounds * sms;         // items of the last round
+    const double cost = rounds * avg + (rest > 0.0 ? avg / fmin(kMaxRate, sms / rest) : 0.0) +
+                        ceil(items / sms) * kItemCost + (parts > 1 ? kSplitCost : 0.0);
+    if (parts == 1 || cost < best_cost) {  // ties: fewer partitions
       best_cost = cost;
       best = pt;
     }
-    if (pt >= tiles) break;
   }
-  return best * pkv::kTcPartitionQuantum;
+  return (int)(best * pkv::kTcPartitionQuantum);
 }
 
 // Which decode kernel runs: 0 = chosen per call, 1 = CUDA cores, 2 = tensor
