@@ -9,39 +9,37 @@
 // a systems problem", section "Memory savings change the scheduling
 // question").  Unlike decode this is a dense contraction.
 //
-// One CTA owns (sequence, KV head, two tiles of 128 query rows).  Rows are
-// (query, head-of-group) pairs, so every head of a KV group shares each K/V
-// tile (grouped-query attention packs into the MMA's M dimension), and the
-// two row tiles share every K/V tile the CTA loads.
+// One CTA owns (sequence, KV head, a tile of 128 query rows), and two CTAs
+// share each SM: each holds half of the tensor memory (S/P in columns
+// [0, 128), O in [128, 128 + D)) and under 113 KiB of shared memory (Q, one
+// K tile, one V tile).  Rows are (query, head-of-group) pairs, so every head
+// of a KV group shares each K/V tile (grouped-query attention packs into
+// the MMA's M dimension).  The two CTAs' chains S -> softmax -> P V run
+// side by side on the SM's tensor core, and while one CTA starts or ends
+// (its first copies, its output, the launch of the next CTA) the other
+// keeps the SM busy.  One K and one V slot suffice: the next tile's K loads
+// while this tile's softmax runs, its V while the next S runs.
 //
-//   warps 8, 10  producers, alternate 128-key tiles: read the tile's block
-//            ids, then load every (block, head) run of K and of V with one
-//            4-D TMA copy each (cp.async.bulk.tensor, 128-byte swizzle);
-//            warp 8 first loads the Q rows of both row tiles, one 4-D TMA
-//            copy per 8-row group.
-//   warp 9   issues S_t = Q_t K^T for both row tiles t (Q from shared
-//            memory); allocates and frees the tensor memory.
-//   warp 11  issues O_t += P_t V (P from tensor memory, V as an MN-major
-//            operand); clears V rows past the context first.
-//   warps 0-3, 4-7  softmax, one warpgroup per row tile and one thread per
-//            row: per key tile it reads its S row for the row max (off the
-//            diagonal with tcgen05.ld.red, which returns each 32-column
-//            chunk's maximum with the values; on the diagonal with a masked
-//            pass), keeps the running max and sum in base 2 (lazy
-//            rescaling, O rescaled in place when the max moved), then
-//            computes the exponentials half a row at a time and writes each
-//            half of P over S in tensor memory, releasing it to P V at once;
-//            at the end it normalises and stores its O row.
+//   warp 4   producer: the Q rows (one 4-D TMA copy per 8-row group), then
+//            per key tile the tile's block ids and every (block, head) run
+//            of K and of V (one 4-D TMA copy each, 128-byte swizzle).
+//   warp 5   issues S = Q K^T (Q and K from shared memory) and O += P V (P
+//            from tensor memory, V as an MN-major operand, rows past the
+//            context cleared first); allocates and frees the tensor memory.
+//   warps 0-3  softmax, one thread per row: per key tile it reads its S row
+//            for the row max (off the diagonal with tcgen05.ld.red, which
+//            returns each 32-column chunk's maximum with the values; on the
+//            diagonal with a masked pass), keeps the running max and sum in
+//            base 2 (lazy rescaling, O rescaled in place when the max
+//            moved), then computes the exponentials half a row at a time and
+//            writes each half of P over S in tensor memory, releasing it to
+//            P V at once; at the end it normalises and stores its O row.
 //
 // Work items (one per CTA) are (query tile, KV head, sequence).  The (sequence,
-// KV head) pairs go in groups of about one wave of items, and within a group
-// the latest query tiles (the longest causal spans) start first: CTAs that
-// run together share K/V in L2, and the final wave holds short items.
-//
-// Tensor memory: row tile t has S/P in columns [128 t, 128 t + 128) and O
-// in [256 + D t, 256 + D (t + 1)).  While one row tile's softmax runs, the
-// tensor core computes the other tile's S or P V, so the two chains
-// S -> softmax -> P V interleave.
+// KV head) pairs go in groups of about one wave of items (two CTAs per SM),
+// and within a group the latest query tiles (the longest causal spans)
+// start first: CTAs that run together share K/V in L2, and the final wave
+// holds short items.
 
 #include <math_constants.h>
 
@@ -57,19 +55,16 @@ namespace {
 
 using namespace tc;
 
-constexpr int kBM = 128;     // rows of a row tile: MMA M
-constexpr int kRowTiles = 2; // row tiles per CTA, one softmax warpgroup each
+constexpr int kBM = 128;     // rows of the row tile: MMA M
+constexpr int kRowTiles = 1; // one row tile per CTA, two CTAs per SM
 constexpr int kBN = 128;     // keys per K/V tile: N of Q K^T, K of P V
 static_assert(kBN == kTileKeys, "TMA runs are capped at the tile length");
 constexpr int kSoftmaxWarps = 4 * kRowTiles;
-constexpr int kProducerWarp0 = kSoftmaxWarps;      // even K/V tiles
-constexpr int kMmaWarp = kSoftmaxWarps + 1;        // Q K^T; owns the tensor memory
-constexpr int kProducerWarp1 = kSoftmaxWarps + 2;  // odd K/V tiles
-constexpr int kPvWarp = kSoftmaxWarps + 3;         // P V
-constexpr int kPrefillThreads = (kSoftmaxWarps + 4) * 32;
-constexpr int kStages = 2;      // K ring and V ring depth: one slot per producer warp
-constexpr int kTmemCols = 512;
-constexpr int kBarSlots = 32;   // mbarriers reserved in shared memory
+constexpr int kProducerWarp = kSoftmaxWarps;  // Q, K and V copies
+constexpr int kMmaWarp = kSoftmaxWarps + 1;   // Q K^T and P V; owns the tensor memory
+constexpr int kPrefillThreads = (kSoftmaxWarps + 2) * 32;
+constexpr int kTmemCols = 256;
+constexpr int kBarSlots = 16;   // mbarriers reserved in shared memory
 
 // Shared-memory tiles (Q, K and V alike): groups of 8 rows, kGroup bytes
 // apart; within a group, one 1024-byte 128-byte-swizzled atom per 64
@@ -83,18 +78,14 @@ struct PrefillSmem {
   static constexpr int kQTile = (kBM / 8) * kGroup;
   static constexpr int kKvTile = (kBN / 8) * kGroup;
   static constexpr int kQ = 0;
-  static constexpr int kK = kQ + kRowTiles * kQTile;
-  static constexpr int kV = kK + kStages * kKvTile;
-  static constexpr int kBar = kV + kStages * kKvTile;
+  static constexpr int kK = kQ + kQTile;
+  static constexpr int kV = kK + kKvTile;
+  static constexpr int kBar = kV + kKvTile;
   static constexpr int kTmemSlot = kBar + kBarSlots * 8;
-  // + 1024-byte alignment slack; at least 116 KiB so that one CTA (which
-  // takes all of tensor memory) is resident per SM
-  static constexpr int kBytes =
-      kTmemSlot + 16 + 1024 > 116 * 1024 ? kTmemSlot + 16 + 1024 : 116 * 1024;
-  static_assert(kBytes <= 227 * 1024, "shared memory overflow");
-  // tensor-memory columns
-  static constexpr int kColO = kRowTiles * kBN;
-  static_assert(kColO + kRowTiles * D <= kTmemCols, "tensor memory overflow");
+  static constexpr int kBytes = kTmemSlot + 16 + 1024;  // + alignment slack
+  static_assert(kBytes <= 113 * 1024, "two CTAs per SM");
+  static constexpr int kColO = kBN;
+  static_assert(kColO + D <= kTmemCols, "tensor memory overflow");
 };
 
 struct PrefillParams {
@@ -128,7 +119,7 @@ __device__ __forceinline__ uint32_t tile_chunk_offset(int r, int c) {
 // ---- the kernel -----------------------------------------------------------
 
 template <typename T, int D>
-__global__ void __launch_bounds__(kPrefillThreads, 1)
+__global__ void __launch_bounds__(kPrefillThreads, 2)
     paged_prefill_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap qmap,
                          const __grid_constant__ CUtensorMap kmap,
                          const __grid_constant__ CUtensorMap vmap) {
@@ -140,26 +131,24 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
   unsigned char* sK = smem + L::kK;
   unsigned char* sV = smem + L::kV;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBar);
-  uint64_t* k_full = bars;                    // K slot landed (TMA transaction bytes)
-  uint64_t* k_empty = k_full + kStages;       // K slot consumed by both Q K^T (MMA commit)
-  uint64_t* v_full = k_empty + kStages;       // V slot landed
-  uint64_t* v_empty = v_full + kStages;       // V slot consumed by both P V
-  uint64_t* q_full = v_empty + kStages;       // [t] Q rows of tile t landed (TMA bytes)
-  uint64_t* s_full = q_full + kRowTiles;      // [t] S_t computed (MMA commit)
-  uint64_t* p_full = s_full + kRowTiles;      // [t][h] keys of half h of P_t written
-                                              // (after O_t was rescaled; softmax)
-  uint64_t* pv_done = p_full + 2 * kRowTiles; // [t] O_t += P_t V finished (MMA commit)
-  uint64_t* drain = pv_done + kRowTiles;      // [2] each issuer's last MMAs finished
-  static_assert(4 * kStages + 5 * kRowTiles + 2 <= kBarSlots, "barrier area too small");
+  uint64_t* k_full = bars;       // K slot landed (TMA transaction bytes)
+  uint64_t* k_empty = bars + 1;  // K slot read by S (MMA commit)
+  uint64_t* v_full = bars + 2;   // V slot landed
+  uint64_t* v_empty = bars + 3;  // V slot read by P V
+  uint64_t* q_full = bars + 4;   // Q rows landed
+  uint64_t* s_full = bars + 5;   // S computed (MMA commit)
+  uint64_t* p_full = bars + 6;   // [h] keys of half h of P written (after O was rescaled)
+  uint64_t* pv_done = bars + 8;  // O += P V finished (MMA commit)
+  uint64_t* drain = bars + 9;    // the issuer's last MMAs finished
+  static_assert(10 <= kBarSlots, "barrier area too small");
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kTmemSlot);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  // Work item -> (query tile, KV head, sequence).  The (sequence, head)
-  // pairs are taken in groups of about one wave of work items; within a
-  // group the hardware starts the latest query tiles (the longest causal
-  // spans) first and the shortest last.  CTAs running together then share
-  // a few pairs' K/V in L2, and the final wave holds short items.
+  // Work item -> (query tile, KV head, sequence): the (sequence, head) pairs
+  // are taken in groups of about one wave of work items, and within a group
+  // the hardware starts the latest query tiles (the longest causal spans)
+  // first.
   const int pairs = p.num_kv_heads * p.num_seqs;
   const int per_group = p.pairs_per_group * p.q_tiles;
   const int grp = (int)(blockIdx.x / per_group);
@@ -171,7 +160,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
   const int s = pair / p.num_kv_heads;
   const int G = p.group;
   const int Gp = p.group_pow2;
-  const int qpt = kBM / Gp;  // queries per row tile
+  const int qpt = kBM / Gp;
 
   const int q0 = p.query_start[s];
   const int nq = p.query_start[s + 1] - q0;
@@ -180,37 +169,27 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
                                (long long)p.max_blocks_per_seq * p.block_size);
   if (ctx < nq || ctx > cap_ll) {
     if (threadIdx.x == 0 && qt == 0) atomicOr(p.status, PKV_DEV_BAD_CONTEXT_LEN);
-    if (ctx < nq || nq <= 0) return;  // nothing sensible to attend to
+    if (ctx < nq || nq <= 0) return;
     ctx = (int)cap_ll;
   }
-  const int j0 = qt * kRowTiles * qpt;  // first query of the CTA
-  if (j0 >= nq) return;                         // no queries here
-  // Key tiles each row tile needs (up to its last query's position); row
-  // tile 1 ends later, or is empty.
+  const int j0 = qt * qpt;  // first query of the CTA
+  if (j0 >= nq) return;     // no queries here
+  // Key tiles up to the tile's last query's position.
   int n_t[kRowTiles];
-#pragma unroll
-  for (int t = 0; t < kRowTiles; ++t) {
-    const int jf = j0 + t * qpt;
-    n_t[t] = jf < nq ? (ctx - nq + min(nq, jf + qpt) - 1) / kBN + 1 : 0;
-  }
-  const int n_tiles = max(n_t[0], n_t[1]);
+  n_t[0] = (ctx - nq + min(nq, j0 + qpt) - 1) / kBN + 1;
+  const int n_tiles = n_t[0];
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kStages; ++i) {
-      mbar_init(&k_full[i], 1);
-      mbar_init(&k_empty[i], 1);
-      mbar_init(&v_full[i], 1);
-      mbar_init(&v_empty[i], 1);
-    }
-    for (int t = 0; t < kRowTiles; ++t) {
-      mbar_init(&q_full[t], 1);
-      mbar_init(&s_full[t], 1);
-      mbar_init(&p_full[2 * t], kBM);
-      mbar_init(&p_full[2 * t + 1], kBM);
-      mbar_init(&pv_done[t], 1);
-    }
-    mbar_init(&drain[0], 1);
-    mbar_init(&drain[1], 1);
+    mbar_init(k_full, 1);
+    mbar_init(k_empty, 1);
+    mbar_init(v_full, 1);
+    mbar_init(v_empty, 1);
+    mbar_init(q_full, 1);
+    mbar_init(s_full, 1);
+    mbar_init(&p_full[0], kBM);
+    mbar_init(&p_full[1], kBM);
+    mbar_init(pv_done, 1);
+    mbar_init(drain, 1);
     fence_barrier_init();
   }
   if (warp == kMmaWarp) {
@@ -224,168 +203,133 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == kProducerWarp0 || warp == kProducerWarp1) {
-    // ------------------------------------------------------------ producers
-    // Each warp loads K and then V of every other key tile into its slot of
-    // the two rings.  A tile's keys are runs of R rows that never cross a
-    // block boundary (R divides the block size and the tile); lane l copies
-    // run l with one TMA copy per operand.  The block-table entry of the
-    // warp's next tile is read before this tile's copies are issued, so its
-    // latency is spent while the warp waits for a free slot.
-    const int first = warp == kProducerWarp1 ? 1 : 0;
+  if (warp == kProducerWarp) {
+    // ------------------------------------------------------------- producer
+    // The Q rows, then K and V of each key tile into their slots.  A tile's
+    // keys are runs of R rows that never cross a block boundary (R divides
+    // the block size and the tile); lane l copies run l with one TMA copy
+    // per operand.  The block-table entry of the next tile is read before
+    // this tile's copies are issued, so its latency is spent while the warp
+    // waits for a free slot.
     const int B = p.block_size;
     const int R = B < kBN ? B : kBN;
     const int32_t* trow = p.block_tables + (size_t)s * p.max_blocks_per_seq;
-    const int seg = lane;
-    auto table_entry = [&](int t) -> int {
-      const int key = t * kBN + seg * R;
-      return (seg < kBN / R && t < n_tiles && key < ctx) ? __ldg(trow + key / B) : 0;
+    auto table_entry = [&](int i) -> int {
+      const int key = i * kBN + lane * R;
+      return (lane < kBN / R && i < n_tiles && key < ctx) ? __ldg(trow + key / B) : 0;
     };
-    int phys_next = table_entry(first);
-    int last_k = -1, last_v = -1;  // last tiles whose copies this warp issued
-    // Warp 8 first loads the Q rows of both row tiles: one copy per 8-row
-    // group, lane = group, box_heads heads x box_tokens queries.  Heads past
-    // the group and queries past the sequence are copied too (their rows are
-    // masked out and never written); rows past the end of q read as zero.
-    if (first == 0) {
+    int phys_next = table_entry(0);
+    {
+      // One copy per 8-row group, lane = group, box_heads heads x
+      // box_tokens queries.  Heads past the group and queries past the
+      // sequence are copied too (their rows are masked out and never
+      // written); rows past the end of q read as zero.
       const int hg = Gp > 8 ? Gp / 8 : 1;   // groups per query
       const int tpg = Gp > 8 ? 1 : 8 / Gp;  // queries per group
-#pragma unroll
-      for (int t = 0; t < kRowTiles; ++t) {
-        if (n_t[t] == 0) continue;
-        if (lane == 0) mbar_arrive_expect_tx(&q_full[t], L::kQTile);
-        __syncwarp();
-        if (lane < kBM / 8)
-          tma_load_token_heads(sQ + t * L::kQTile + lane * L::kGroup, &qmap,
-                               kvh * G + (lane % hg) * 8, q0 + j0 + t * qpt + (lane / hg) * tpg,
-                               &q_full[t]);
-      }
+      if (lane == 0) mbar_arrive_expect_tx(q_full, L::kQTile);
+      __syncwarp();
+      if (lane < kBM / 8)
+        tma_load_token_heads(sQ + lane * L::kGroup, &qmap, kvh * G + (lane % hg) * 8,
+                             q0 + j0 + (lane / hg) * tpg, q_full);
     }
-    for (int i = first; i < n_tiles; i += 2) {
-      const int st = i % kStages;
-      const uint32_t ph = ((i / kStages) - 1) & 1;
-      if (i >= kStages && !mbar_wait_warp(&k_empty[st], ph, p.status)) break;
+    int last_k = -1, last_v = -1;
+    for (int i = 0; i < n_tiles; ++i) {
+      const uint32_t ph = (i - 1) & 1;
+      if (i > 0 && !mbar_wait_warp(k_empty, ph, p.status)) break;
       const int key0 = i * kBN;
       const int nvalid = min(ctx, key0 + kBN) - key0;
       const int nseg = (nvalid + R - 1) / R;
       const uint32_t bytes = (uint32_t)nseg * R * D * (uint32_t)sizeof(T);
       int phys = phys_next;
-      phys_next = table_entry(i + 2);
+      phys_next = table_entry(i + 1);
       if ((unsigned)phys >= (unsigned)p.num_blocks) {
-        if (seg < nseg) atomicOr(p.status, PKV_DEV_BAD_BLOCK_ID);
+        if (lane < nseg) atomicOr(p.status, PKV_DEV_BAD_BLOCK_ID);
         phys = 0;
       }
-      const int key = key0 + seg * R;
-      const int g = ((phys * p.num_kv_heads + kvh) * B + key % B) / 8;  // 8-row group
-      const uint32_t dst = (uint32_t)(st * L::kKvTile + seg * (R / 8) * L::kGroup);
-      if (lane == 0) mbar_arrive_expect_tx(&k_full[st], bytes);
+      const int key = key0 + lane * R;
+      const int g8 = ((phys * p.num_kv_heads + kvh) * B + key % B) / 8;  // 8-row group
+      const uint32_t dst = (uint32_t)(lane * (R / 8) * L::kGroup);
+      if (lane == 0) mbar_arrive_expect_tx(k_full, bytes);
       __syncwarp();
-      if (seg < nseg) tma_load_group(sK + dst, &kmap, g, &k_full[st]);
+      if (lane < nseg) tma_load_group(sK + dst, &kmap, g8, k_full);
       last_k = i;
-      if (i >= kStages && !mbar_wait_warp(&v_empty[st], ph, p.status)) break;
-      if (lane == 0) mbar_arrive_expect_tx(&v_full[st], bytes);
+      if (i > 0 && !mbar_wait_warp(v_empty, ph, p.status)) break;
+      if (lane == 0) mbar_arrive_expect_tx(v_full, bytes);
       __syncwarp();
-      if (seg < nseg) tma_load_group(sV + dst, &vmap, g, &v_full[st]);
+      if (lane < nseg) tma_load_group(sV + dst, &vmap, g8, v_full);
       last_v = i;
     }
     // Copies still in flight at exit (only after a timeout) land before the
-    // CTA leaves: wait, bounded, for the last slots this warp filled.
-    if (last_k >= 0) mbar_drain(&k_full[last_k % kStages], (last_k / kStages) & 1);
-    if (last_v >= 0) mbar_drain(&v_full[last_v % kStages], (last_v / kStages) & 1);
-    if (first == 0) {
-#pragma unroll
-      for (int t = 0; t < kRowTiles; ++t)
-        if (n_t[t] > 0) mbar_drain(&q_full[t], 0);
-    }
+    // CTA leaves: wait, bounded, for the last ones this warp issued.
+    if (last_k >= 0) mbar_drain(k_full, last_k & 1);
+    if (last_v >= 0) mbar_drain(v_full, last_v & 1);
+    mbar_drain(q_full, 0);
     __syncwarp();
   } else if (warp == kMmaWarp) {
-    // ------------------------------------------------------ Q K^T issuer
-    // S_t of key tile i overwrites P_t of tile i - 1, so it waits for that
-    // P V; row tile 0 goes first and its softmax overlaps tile 1's MMAs.
+    // ---------------------------------------------------------- MMA issuer
+    // S of key tile i overwrites P of tile i - 1, so it waits for that P V.
     // The whole warp runs the loop and one elected lane issues.
     constexpr bool bf16 = std::is_same<T, __nv_bfloat16>::value;
     const uint32_t idesc_s = instr_desc(bf16, false, false, kBN, kBM);
-    const uint32_t aQ = smem_addr(sQ), aK = smem_addr(sK);
-    bool ok = true;
+    const uint32_t idesc_o = instr_desc(bf16, false, true, D, kBM);
+    const uint32_t aQ = smem_addr(sQ), aK = smem_addr(sK), aV = smem_addr(sV);
+    bool ok = mbar_wait_warp(q_full, 0, p.status);
     for (int i = 0; ok && i < n_tiles; ++i) {
-      const int st = i % kStages;
-      if (!mbar_wait_warp(&k_full[st], (i / kStages) & 1, p.status)) break;
+      if (!mbar_wait_warp(k_full, i & 1, p.status) ||
+          (i > 0 && !mbar_wait_warp(pv_done, (i - 1) & 1, p.status))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
 #pragma unroll
-      for (int t = 0; t < kRowTiles; ++t) {
-        if (i >= n_t[t]) continue;
-        const bool ready = i == 0 ? mbar_wait_warp(&q_full[t], 0, p.status)
-                                  : mbar_wait_warp(&pv_done[t], (i - 1) & 1, p.status);
-        if (!ready) {
+      for (int ks = 0; ks < D / 16; ++ks) {
+        const uint32_t koff = (ks / 4) * 1024 + (ks % 4) * 32;
+        mma_f16_ss_warp(tmem, smem_desc(aQ + koff, 16, L::kGroup),
+                        smem_desc(aK + koff, 16, L::kGroup), idesc_s, ks > 0);
+      }
+      mma_commit_warp(s_full);
+      mma_commit_warp(k_empty);
+      if (!mbar_wait_warp(v_full, i & 1, p.status)) {
+        ok = false;
+        break;
+      }
+      // Key rows past the context (the tail of the last block, or rows no
+      // run was loaded into) must not feed NaN or stale values into P V
+      // (their P is 0, but 0 * NaN is NaN): they are cleared first.
+      if (i * kBN + kBN > ctx) {
+        for (int r = max(ctx - i * kBN, 0) + lane; r < kBN; r += 32)
+#pragma unroll
+          for (int c = 0; c < D / 8; ++c)
+            *reinterpret_cast<uint4*>(sV + tile_chunk_offset<D>(r, c)) = make_uint4(0, 0, 0, 0);
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+      }
+      // P arrives in two halves of the keys; the first half's MMAs run while
+      // the softmax computes the second.  V as an MN-major operand: 8-key
+      // groups kGroup bytes apart, 64-column atoms 1024 bytes apart.
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        if (!mbar_wait_warp(&p_full[h], i & 1, p.status)) {
           ok = false;
           break;
         }
         tc_fence_after();
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t koff = (ks / 4) * 1024 + (ks % 4) * 32;
-          mma_f16_ss_warp(tmem + t * kBN, smem_desc(aQ + t * L::kQTile + koff, 16, L::kGroup),
-                          smem_desc(aK + st * L::kKvTile + koff, 16, L::kGroup), idesc_s,
-                          ks > 0);
-        }
-        mma_commit_warp(&s_full[t]);
+        for (int ks = h * kBN / 32; ks < (h + 1) * kBN / 32; ++ks)
+          mma_f16_ta_warp(tmem + L::kColO, tmem + ks * 8,
+                          smem_desc(aV + ks * 2 * L::kGroup, 1024, L::kGroup), idesc_o,
+                          (i > 0 || ks > 0) ? 1u : 0u);
       }
-      if (ok) mma_commit_warp(&k_empty[st]);
+      if (!ok) break;
+      mma_commit_warp(pv_done);
+      mma_commit_warp(v_empty);
     }
-    mma_commit_warp(&drain[0]);
-    mbar_drain(&drain[0], 0);
-    __syncwarp();
-  } else if (warp == kPvWarp) {
-    // --------------------------------------------------------- P V issuer
-    constexpr bool bf16 = std::is_same<T, __nv_bfloat16>::value;
-    const uint32_t idesc_o = instr_desc(bf16, false, true, D, kBM);
-    const uint32_t aV = smem_addr(sV);
-    bool ok = true;
-    for (int i = 0; ok && i < n_tiles; ++i) {
-      const int st = i % kStages;
-      if (!mbar_wait_warp(&v_full[st], (i / kStages) & 1, p.status)) break;
-      // Key rows past the context (the tail of the last block, or rows no
-      // run was loaded into) must not feed NaN or stale values into P V
-      // (their P is 0, but 0 * NaN is NaN): this warp clears them first.
-      if (i * kBN + kBN > ctx) {
-        for (int r = max(ctx - i * kBN, 0) + lane; r < kBN; r += 32)
-#pragma unroll
-          for (int c = 0; c < D / 8; ++c)
-            *reinterpret_cast<uint4*>(sV + st * L::kKvTile + tile_chunk_offset<D>(r, c)) =
-                make_uint4(0, 0, 0, 0);
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        __syncwarp();
-      }
-#pragma unroll
-      for (int t = 0; t < kRowTiles; ++t) {
-        if (i >= n_t[t]) continue;
-        // P arrives in two halves of the keys; the first half's MMAs run
-        // while the softmax computes the second.
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          if (!mbar_wait_warp(&p_full[2 * t + h], i & 1, p.status)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          // V as an MN-major operand: 8-key groups kGroup bytes apart,
-          // 64-column atoms 1024 bytes apart.
-#pragma unroll
-          for (int ks = h * kBN / 32; ks < (h + 1) * kBN / 32; ++ks)
-            mma_f16_ta_warp(tmem + L::kColO + t * D, tmem + t * kBN + ks * 8,
-                            smem_desc(aV + st * L::kKvTile + ks * 2 * L::kGroup, 1024, L::kGroup),
-                            idesc_o, (i > 0 || ks > 0) ? 1u : 0u);
-        }
-        if (!ok) break;
-        mma_commit_warp(&pv_done[t]);
-      }
-      if (ok) mma_commit_warp(&v_empty[st]);
-    }
-    mma_commit_warp(&drain[1]);
-    mbar_drain(&drain[1], 0);
+    mma_commit_warp(drain);
+    mbar_drain(drain, 0);
     __syncwarp();
   } else if (warp < kSoftmaxWarps) {
     // ------------------------------------------- softmax / epilogue (rows)
-    const int t = warp / 4;                 // row tile of this warpgroup
+    const int t = warp / 4;                 // row tile (the CTA's only one)
     const int r = threadIdx.x & (kBM - 1);  // row of the tile == TMEM lane
     const int nt = n_t[t];
     const int jq = j0 + t * qpt + r / Gp;
@@ -621,7 +565,7 @@ cudaError_t launch_paged_prefill(const PrefillArgs& a, cudaStream_t stream, bool
   // About one wave of CTAs (one per SM) per group; the count only shapes
   // the order, not the result.
   const int pairs = a.num_kv_heads * a.num_seqs;
-  p.pairs_per_group = std::max(1, std::min(pairs, a.sm_count / std::max(1, q_tiles)));
+  p.pairs_per_group = std::max(1, std::min(pairs, 2 * a.sm_count / std::max(1, q_tiles)));
   if (a.dtype == PKV_F16) {
     return a.head_dim == 64
                ? launch_prefill_typed<__half, 64>(p, qm, km, vm, q_tiles, a.num_seqs, stream)
