@@ -208,9 +208,9 @@ __global__ void __launch_bounds__(kPrefillThreads, 2)
     // The Q rows, then K and V of each key tile into their slots.  A tile's
     // keys are runs of R rows that never cross a block boundary (R divides
     // the block size and the tile); lane l copies run l with one TMA copy
-    // per operand.  The block-table entry of the next tile is read before
-    // this tile's copies are issued, so its latency is spent while the warp
-    // waits for a free slot.
+    // per operand.  The block-table entry of the next tile is read once this
+    // tile's copies are issued, so its latency is spent while the warp waits
+    // for a free slot.
     const int B = p.block_size;
     const int R = B < kBN ? B : kBN;
     const int32_t* trow = p.block_tables + (size_t)s * p.max_blocks_per_seq;
@@ -241,7 +241,6 @@ __global__ void __launch_bounds__(kPrefillThreads, 2)
       const int nseg = (nvalid + R - 1) / R;
       const uint32_t bytes = (uint32_t)nseg * R * D * (uint32_t)sizeof(T);
       int phys = phys_next;
-      phys_next = table_entry(i + 1);
       if ((unsigned)phys >= (unsigned)p.num_blocks) {
         if (lane < nseg) atomicOr(p.status, PKV_DEV_BAD_BLOCK_ID);
         phys = 0;
@@ -258,6 +257,9 @@ __global__ void __launch_bounds__(kPrefillThreads, 2)
       __syncwarp();
       if (lane < nseg) tma_load_group(sV + dst, &vmap, g8, v_full);
       last_v = i;
+      // The next tile's block ids, read after this tile's copies are out (read
+      // before them, the load held the copies back).
+      phys_next = table_entry(i + 1);
     }
     // Copies still in flight at exit (only after a timeout) land before the
     // CTA leaves: wait, bounded, for the last ones this warp issued.
