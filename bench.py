@@ -275,6 +275,15 @@ def time_alone(fn, flush, stream, iters):
     return total / iters
 
 
+def launch_floor_ms(flush, stream, iters):
+    """An empty kernel (a zero-cycle device-side wait) timed like the calls
+    of time_alone: the part of a lone call's time that no kernel avoids
+    (the launch leaving the queue, the CTAs starting, the end event)."""
+    for _ in range(3):
+        torch.cuda._sleep(0)
+    return time_alone(lambda: torch.cuda._sleep(0), flush, stream, iters)
+
+
 def pipelined_steps(stream, n_steps, copy_in, compute, copy_out, hold_ms=5.0, nbuf=2):
     """Mean ms per step of a multi-buffered serving loop, on the device
     clock.  copy_in(b) fills input buffer b on a copy stream, compute(b)
@@ -365,6 +374,24 @@ def cache_ops_bench(pkv, case, dev, stream, peak, iters=30, fill_blocks=400, cow
         dst = torch.empty_like(src)
         ref[name] = timed(lambda: dst.copy_(src))
         del src, dst
+    # The copy-on-write batch at other sizes, beside torch's copy of the same
+    # bytes: how the per-call latency weighs against the bytes moved.
+    batches = []
+    for n in (28, 224, 448):
+        if 2 * n > NB:
+            continue
+        pr = torch.stack([perm[:n], perm[n:2 * n]], dim=1).to(torch.int64).to(dev)
+        t_n = timed(lambda: pkv.block_copy(kc, vc, pr))
+        nbytes = 2 * n * Hkv * B * D * e
+        src = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        dst = torch.empty_like(src)
+        t_ref = timed(lambda: dst.copy_(src))
+        del src, dst, pr
+        gbs = 2 * nbytes / (t_n * 1e-3) / 1e9
+        batches.append({"pairs": n, "bytes_moved": 2 * nbytes, "ms": round(t_n, 5),
+                        "frac_of_peak": round(gbs / peak, 4),
+                        "torch_copy_same_bytes_ms": round(t_ref, 5)})
+    floor = launch_floor_ms(flush, stream, iters)
     if pkv.device_status(clear=True) != 0:
         raise RuntimeError("device status flags during the cache-operation bench")
     b_app = 2 * (2 * T * Hkv * D * e)          # K and V rows read, then written
@@ -382,6 +409,8 @@ def cache_ops_bench(pkv, case, dev, stream, peak, iters=30, fill_blocks=400, cow
                                          "random blocks", "kv_append_prompt_fill"),
             "block_copy_cow_batch": rec(t_cow, b_cow, f"{n_cow} block pairs, K and V",
                                         "block_copy_cow_batch"),
+            "block_copy_other_batches": batches,
+            "empty_kernel_ms": round(floor, 5),
             "l2": "flushed (256 MiB read) before every timed call",
             "launch": "queued behind a device-side wait, outside the timed region", "iters": iters}
 
@@ -835,7 +864,7 @@ def run_ours(args, rank, world, local_rank):
         # shared-prompt serving step, and chunked prefill on the tensor cores.
         sw = sweep_line(args, rank, world, local_rank, block_sizes=(16,))
         line["sweep_b16"] = {"rows": sw["sweep"], "l2": sw["config"]["l2"],
-                             "clocks": sw["clocks"]}
+                             "empty_kernel_ms": sw["empty_kernel_ms"], "clocks": sw["clocks"]}
         sh = shared_line(args, rank, world, local_rank)
         line["shared_prefix"] = {k: sh[k] for k in (
             "value", "unit", "ms_per_step", "steps_per_s", "steps", "device_ms_per_step",
@@ -1268,6 +1297,7 @@ def sweep_line(args, rank, world, local_rank, block_sizes=None):
                              "steady_frac": round(sgbs / peak, 4), "steady_copies": reps})
                 del case, ws, out, copies
                 torch.cuda.empty_cache()
+    floor = launch_floor_ms(flush, stream, max(5, min(args.steps, 30)))
     clock_rec = clocks.stop()
     if pkv.device_status(clear=True) != 0:
         raise RuntimeError("device status flags during the sweep")
@@ -1286,7 +1316,7 @@ def sweep_line(args, rank, world, local_rank, block_sizes=None):
                                  "region; steady_ms: back to back, as the layers of a step"},
             "roofline": {"bound": "hbm", "achieved": ref["GB/s"], "peak": peak, "unit": "GB/s",
                          "frac": ref["frac"], "peak_kind": peak_kind, "traffic": None},
-            "sweep": rows, "clocks": clock_rec}
+            "sweep": rows, "empty_kernel_ms": round(floor, 5), "clocks": clock_rec}
 
 
 def run_groups(args, rank, world, local_rank):
