@@ -9,37 +9,45 @@
 // a systems problem", section "Memory savings change the scheduling
 // question").  Unlike decode this is a dense contraction.
 //
-// One CTA owns (sequence, KV head, a tile of 128 query rows), and two CTAs
-// share each SM: each holds half of the tensor memory (S/P in columns
-// [0, 128), O in [128, 128 + D)) and under 113 KiB of shared memory (Q, one
-// K tile, one V tile).  Rows are (query, head-of-group) pairs, so every head
-// of a KV group shares each K/V tile (grouped-query attention packs into
-// the MMA's M dimension).  The two CTAs' chains S -> softmax -> P V run
-// side by side on the SM's tensor core, and while one CTA starts or ends
-// (its first copies, its output, the launch of the next CTA) the other
-// keeps the SM busy.  One K and one V slot suffice: the next tile's K loads
-// while this tile's softmax runs, its V while the next S runs.
+// One CTA owns (sequence, KV head, two tiles A and B of 128 query rows each)
+// and one SM: the tensor memory holds S_A, S_B (P written over them) and
+// O_A, O_B, 4 x 128 columns; shared memory holds both Q tiles and two slots
+// each of K and V (193 KiB at D = 128).  Rows are (query, head-of-group)
+// pairs, so every head of a KV group shares each K/V tile (grouped-query
+// attention packs into the MMA's M dimension).  Each tile's chain
+// S -> softmax -> P V is serial, and the single MMA issuer interleaves the
+// two: P V of A, S of A's next key tile, P V of B, S of B's next.  So while
+// one tile's softmax runs, the tensor core computes the other tile's
+// products, and the two softmax phases do not overlap (left to themselves,
+// two such chains on one tensor core fall into step, each softmax running
+// beside the other's instead of beside its MMAs).
 //
-//   warp 4   producer: the Q rows (one 4-D TMA copy per 8-row group), then
-//            per key tile the tile's block ids and every (block, head) run
-//            of K and of V (one 4-D TMA copy each, 128-byte swizzle).
-//   warp 5   issues S = Q K^T (Q and K from shared memory) and O += P V (P
+//   warp 8   producer: the Q rows of both tiles (one 4-D TMA copy per 8-row
+//            group), then per key tile the tile's block ids and every
+//            (block, head) run of K and of V (one 4-D TMA copy each, 128-byte
+//            swizzle) into the next free slot.
+//   warp 9   issues S = Q K^T (Q and K from shared memory) and O += P V (P
 //            from tensor memory, V as an MN-major operand, rows past the
 //            context cleared first); allocates and frees the tensor memory.
-//   warps 0-3  softmax, one thread per row: per key tile it reads its S row
-//            for the row max (off the diagonal with tcgen05.ld.red, which
-//            returns each 32-column chunk's maximum with the values; on the
-//            diagonal with a masked pass), keeps the running max and sum in
-//            base 2 (lazy rescaling, O rescaled in place when the max
-//            moved), then computes the exponentials half a row at a time and
-//            writes each half of P over S in tensor memory, releasing it to
-//            P V at once; at the end it normalises and stores its O row.
+//            S_t of a key tile overwrites P_t of the previous one, so it
+//            waits for that P V; the wait for the next V tile sits behind the
+//            last P V of a key tile, off the path from one tile's S to the
+//            other's P V.
+//   warps 0-3 (tile A), 4-7 (tile B)  softmax, one thread per row: per key
+//            tile it reads its S row for the row max (off the diagonal with
+//            tcgen05.ld.red, which returns each 32-column chunk's maximum with
+//            the values; on the diagonal with a masked pass), keeps the
+//            running max and sum in base 2 (lazy rescaling, O rescaled in
+//            place when the max moved), then computes the exponentials half a
+//            row at a time and writes each half of P over S in tensor memory,
+//            releasing it to P V at once; at the end it normalises and stores
+//            its O row.
 //
-// Work items (one per CTA) are (query tile, KV head, sequence).  The (sequence,
-// KV head) pairs go in groups of about one wave of items (two CTAs per SM),
-// and within a group the latest query tiles (the longest causal spans)
-// start first: CTAs that run together share K/V in L2, and the final wave
-// holds short items.
+// Work items (one per CTA) are (query tile pair, KV head, sequence).  The
+// (sequence, KV head) pairs go in groups of about one wave of items (one CTA
+// per SM), and within a group the latest query tiles (the longest causal
+// spans) start first: CTAs that run together share K/V in L2, and the final
+// wave holds short items.
 
 #include <math_constants.h>
 
@@ -56,15 +64,16 @@ namespace {
 using namespace tc;
 
 constexpr int kBM = 128;     // rows of the row tile: MMA M
-constexpr int kRowTiles = 1; // one row tile per CTA, two CTAs per SM
+constexpr int kRowTiles = 2; // two row tiles per CTA, their chains alternating
+constexpr int kStages = 2;   // K and V ring slots
 constexpr int kBN = 128;     // keys per K/V tile: N of Q K^T, K of P V
 static_assert(kBN == kTileKeys, "TMA runs are capped at the tile length");
 constexpr int kSoftmaxWarps = 4 * kRowTiles;
 constexpr int kProducerWarp = kSoftmaxWarps;  // Q, K and V copies
 constexpr int kMmaWarp = kSoftmaxWarps + 1;   // Q K^T and P V; owns the tensor memory
 constexpr int kPrefillThreads = (kSoftmaxWarps + 2) * 32;
-constexpr int kTmemCols = 256;
-constexpr int kBarSlots = 16;   // mbarriers reserved in shared memory
+constexpr int kTmemCols = 512;
+constexpr int kBarSlots = 24;   // mbarriers reserved in shared memory
 
 // Shared-memory tiles (Q, K and V alike): groups of 8 rows, kGroup bytes
 // apart; within a group, one 1024-byte 128-byte-swizzled atom per 64
@@ -78,14 +87,14 @@ struct PrefillSmem {
   static constexpr int kQTile = (kBM / 8) * kGroup;
   static constexpr int kKvTile = (kBN / 8) * kGroup;
   static constexpr int kQ = 0;
-  static constexpr int kK = kQ + kQTile;
-  static constexpr int kV = kK + kKvTile;
-  static constexpr int kBar = kV + kKvTile;
+  static constexpr int kK = kQ + kRowTiles * kQTile;
+  static constexpr int kV = kK + kStages * kKvTile;
+  static constexpr int kBar = kV + kStages * kKvTile;
   static constexpr int kTmemSlot = kBar + kBarSlots * 8;
   static constexpr int kBytes = kTmemSlot + 16 + 1024;  // + alignment slack
-  static_assert(kBytes <= 113 * 1024, "two CTAs per SM");
-  static constexpr int kColO = kBN;
-  static_assert(kColO + D <= kTmemCols, "tensor memory overflow");
+  static_assert(kBytes <= 227 * 1024, "shared memory per CTA");
+  static constexpr int kColO = kRowTiles * kBN;
+  static_assert(kColO + kRowTiles * D <= kTmemCols, "tensor memory overflow");
 };
 
 struct PrefillParams {
@@ -119,7 +128,7 @@ __device__ __forceinline__ uint32_t tile_chunk_offset(int r, int c) {
 // ---- the kernel -----------------------------------------------------------
 
 template <typename T, int D>
-__global__ void __launch_bounds__(kPrefillThreads, 2)
+__global__ void __launch_bounds__(kPrefillThreads, 1)
     paged_prefill_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap qmap,
                          const __grid_constant__ CUtensorMap kmap,
                          const __grid_constant__ CUtensorMap vmap) {
@@ -131,16 +140,16 @@ __global__ void __launch_bounds__(kPrefillThreads, 2)
   unsigned char* sK = smem + L::kK;
   unsigned char* sV = smem + L::kV;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBar);
-  uint64_t* k_full = bars;       // K slot landed (TMA transaction bytes)
-  uint64_t* k_empty = bars + 1;  // K slot read by S (MMA commit)
-  uint64_t* v_full = bars + 2;   // V slot landed
-  uint64_t* v_empty = bars + 3;  // V slot read by P V
-  uint64_t* q_full = bars + 4;   // Q rows landed
-  uint64_t* s_full = bars + 5;   // S computed (MMA commit)
-  uint64_t* p_full = bars + 6;   // [h] keys of half h of P written (after O was rescaled)
-  uint64_t* pv_done = bars + 8;  // O += P V finished (MMA commit)
-  uint64_t* drain = bars + 9;    // the issuer's last MMAs finished
-  static_assert(10 <= kBarSlots, "barrier area too small");
+  uint64_t* k_full = bars;        // [kStages] K slot landed (TMA transaction bytes)
+  uint64_t* k_empty = bars + 2;   // [kStages] K slot read by S (MMA commit)
+  uint64_t* v_full = bars + 4;    // [kStages] V slot landed
+  uint64_t* v_empty = bars + 6;   // [kStages] V slot read by P V
+  uint64_t* q_full = bars + 8;    // Q rows of both tiles landed
+  uint64_t* s_full = bars + 9;    // [t] S_t computed (MMA commit)
+  uint64_t* p_full = bars + 11;   // [2 t + h] half h of P_t written (after O_t was rescaled)
+  uint64_t* pv_done = bars + 15;  // [t] O_t += P_t V finished (MMA commit)
+  uint64_t* drain = bars + 17;    // the issuer's last MMAs finished
+  static_assert(18 <= kBarSlots, "barrier area too small");
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kTmemSlot);
 
   const int warp = threadIdx.x >> 5;
@@ -172,23 +181,32 @@ __global__ void __launch_bounds__(kPrefillThreads, 2)
     if (ctx < nq || nq <= 0) return;
     ctx = (int)cap_ll;
   }
-  const int j0 = qt * qpt;  // first query of the CTA
-  if (j0 >= nq) return;     // no queries here
-  // Key tiles up to the tile's last query's position.
+  const int j0 = qt * kRowTiles * qpt;  // first query of the CTA
+  if (j0 >= nq) return;                 // no queries here
+  // Key tiles up to each row tile's last query's position (none for a tile
+  // past the sequence's queries).
   int n_t[kRowTiles];
-  n_t[0] = (ctx - nq + min(nq, j0 + qpt) - 1) / kBN + 1;
-  const int n_tiles = n_t[0];
+#pragma unroll
+  for (int t = 0; t < kRowTiles; ++t) {
+    const int jt = j0 + t * qpt;
+    n_t[t] = jt < nq ? (ctx - nq + min(nq, jt + qpt) - 1) / kBN + 1 : 0;
+  }
+  const int n_tiles = max(n_t[0], n_t[1]);
 
   if (threadIdx.x == 0) {
-    mbar_init(k_full, 1);
-    mbar_init(k_empty, 1);
-    mbar_init(v_full, 1);
-    mbar_init(v_empty, 1);
+    for (int st = 0; st < kStages; ++st) {
+      mbar_init(&k_full[st], 1);
+      mbar_init(&k_empty[st], 1);
+      mbar_init(&v_full[st], 1);
+      mbar_init(&v_empty[st], 1);
+    }
     mbar_init(q_full, 1);
-    mbar_init(s_full, 1);
-    mbar_init(&p_full[0], kBM);
-    mbar_init(&p_full[1], kBM);
-    mbar_init(pv_done, 1);
+    for (int t = 0; t < kRowTiles; ++t) {
+      mbar_init(&s_full[t], 1);
+      mbar_init(&p_full[2 * t], kBM);
+      mbar_init(&p_full[2 * t + 1], kBM);
+      mbar_init(&pv_done[t], 1);
+    }
     mbar_init(drain, 1);
     fence_barrier_init();
   }
@@ -226,16 +244,17 @@ __global__ void __launch_bounds__(kPrefillThreads, 2)
       // written); rows past the end of q read as zero.
       const int hg = Gp > 8 ? Gp / 8 : 1;   // groups per query
       const int tpg = Gp > 8 ? 1 : 8 / Gp;  // queries per group
-      if (lane == 0) mbar_arrive_expect_tx(q_full, L::kQTile);
+      if (lane == 0) mbar_arrive_expect_tx(q_full, kRowTiles * L::kQTile);
       __syncwarp();
-      if (lane < kBM / 8)
+      if (lane < kRowTiles * kBM / 8)
         tma_load_token_heads(sQ + lane * L::kGroup, &qmap, kvh * G + (lane % hg) * 8,
                              q0 + j0 + (lane / hg) * tpg, q_full);
     }
     int last_k = -1, last_v = -1;
     for (int i = 0; i < n_tiles; ++i) {
-      const uint32_t ph = (i - 1) & 1;
-      if (i > 0 && !mbar_wait_warp(k_empty, ph, p.status)) break;
+      const int st = i % kStages;
+      const uint32_t ph = ((i / kStages) - 1) & 1;
+      if (i >= kStages && !mbar_wait_warp(&k_empty[st], ph, p.status)) break;
       const int key0 = i * kBN;
       const int nvalid = min(ctx, key0 + kBN) - key0;
       const int nseg = (nvalid + R - 1) / R;
@@ -247,15 +266,15 @@ __global__ void __launch_bounds__(kPrefillThreads, 2)
       }
       const int key = key0 + lane * R;
       const int g8 = ((phys * p.num_kv_heads + kvh) * B + key % B) / 8;  // 8-row group
-      const uint32_t dst = (uint32_t)(lane * (R / 8) * L::kGroup);
-      if (lane == 0) mbar_arrive_expect_tx(k_full, bytes);
+      const uint32_t dst = (uint32_t)(st * L::kKvTile + lane * (R / 8) * L::kGroup);
+      if (lane == 0) mbar_arrive_expect_tx(&k_full[st], bytes);
       __syncwarp();
-      if (lane < nseg) tma_load_group(sK + dst, &kmap, g8, k_full);
+      if (lane < nseg) tma_load_group(sK + dst, &kmap, g8, &k_full[st]);
       last_k = i;
-      if (i > 0 && !mbar_wait_warp(v_empty, ph, p.status)) break;
-      if (lane == 0) mbar_arrive_expect_tx(v_full, bytes);
+      if (i >= kStages && !mbar_wait_warp(&v_empty[st], ph, p.status)) break;
+      if (lane == 0) mbar_arrive_expect_tx(&v_full[st], bytes);
       __syncwarp();
-      if (lane < nseg) tma_load_group(sV + dst, &vmap, g8, v_full);
+      if (lane < nseg) tma_load_group(sV + dst, &vmap, g8, &v_full[st]);
       last_v = i;
       // The next tile's block ids, read after this tile's copies are out (read
       // before them, the load held the copies back).
@@ -263,38 +282,47 @@ __global__ void __launch_bounds__(kPrefillThreads, 2)
     }
     // Copies still in flight at exit (only after a timeout) land before the
     // CTA leaves: wait, bounded, for the last ones this warp issued.
-    if (last_k >= 0) mbar_drain(k_full, last_k & 1);
-    if (last_v >= 0) mbar_drain(v_full, last_v & 1);
+    if (last_k >= 0) mbar_drain(&k_full[last_k % kStages], (last_k / kStages) & 1);
+    if (last_v >= 0) mbar_drain(&v_full[last_v % kStages], (last_v / kStages) & 1);
     mbar_drain(q_full, 0);
     __syncwarp();
   } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------- MMA issuer
-    // S of key tile i overwrites P of tile i - 1, so it waits for that P V.
-    // The whole warp runs the loop and one elected lane issues.
+    // The two row tiles alternate: P V of tile A, S of A's next key tile, P V
+    // of tile B, S of B's next; so while one tile's softmax runs the tensor
+    // core works on the other's products.  S_t of key tile i + 1 overwrites
+    // P_t of tile i, so it waits for that P V.  The whole warp runs the loop
+    // and one elected lane issues.
     constexpr bool bf16 = std::is_same<T, __nv_bfloat16>::value;
     const uint32_t idesc_s = instr_desc(bf16, false, false, kBN, kBM);
     const uint32_t idesc_o = instr_desc(bf16, false, true, D, kBM);
     const uint32_t aQ = smem_addr(sQ), aK = smem_addr(sK), aV = smem_addr(sV);
-    bool ok = mbar_wait_warp(q_full, 0, p.status);
-    for (int i = 0; ok && i < n_tiles; ++i) {
-      if (!mbar_wait_warp(k_full, i & 1, p.status) ||
-          (i > 0 && !mbar_wait_warp(pv_done, (i - 1) & 1, p.status))) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
+    auto issue_s = [&](int t, int i) {
+      const uint32_t kb = aK + (uint32_t)((i % kStages) * L::kKvTile);
+      const uint32_t qb = aQ + (uint32_t)(t * L::kQTile);
 #pragma unroll
       for (int ks = 0; ks < D / 16; ++ks) {
         const uint32_t koff = (ks / 4) * 1024 + (ks % 4) * 32;
-        mma_f16_ss_warp(tmem, smem_desc(aQ + koff, 16, L::kGroup),
-                        smem_desc(aK + koff, 16, L::kGroup), idesc_s, ks > 0);
+        mma_f16_ss_warp(tmem + t * kBN, smem_desc(qb + koff, 16, L::kGroup),
+                        smem_desc(kb + koff, 16, L::kGroup), idesc_s, ks > 0);
       }
-      mma_commit_warp(s_full);
-      mma_commit_warp(k_empty);
-      if (!mbar_wait_warp(v_full, i & 1, p.status)) {
-        ok = false;
-        break;
-      }
+      mma_commit_warp(&s_full[t]);
+    };
+    bool ok = mbar_wait_warp(q_full, 0, p.status) && mbar_wait_warp(&k_full[0], 0, p.status);
+    if (ok) {
+      tc_fence_after();
+#pragma unroll
+      for (int t = 0; t < kRowTiles; ++t)
+        if (n_t[t] > 0) issue_s(t, 0);
+      mma_commit_warp(&k_empty[0]);
+    }
+    // V of key tile i is waited for while the last P V of tile i - 1 runs,
+    // off the path from one tile's S to the other's P V.
+    ok = ok && mbar_wait_warp(&v_full[0], 0, p.status);
+    for (int i = 0; ok && i < n_tiles; ++i) {
+      const int st = i % kStages;
+      const int last_t = i < n_t[1] ? 1 : 0;  // the last row tile with key tile i
+      unsigned char* sVs = sV + st * L::kKvTile;
       // Key rows past the context (the tail of the last block, or rows no
       // run was loaded into) must not feed NaN or stale values into P V
       // (their P is 0, but 0 * NaN is NaN): they are cleared first.
@@ -302,38 +330,68 @@ __global__ void __launch_bounds__(kPrefillThreads, 2)
         for (int r = max(ctx - i * kBN, 0) + lane; r < kBN; r += 32)
 #pragma unroll
           for (int c = 0; c < D / 8; ++c)
-            *reinterpret_cast<uint4*>(sV + tile_chunk_offset<D>(r, c)) = make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4*>(sVs + tile_chunk_offset<D>(r, c)) = make_uint4(0, 0, 0, 0);
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncwarp();
       }
-      // P arrives in two halves of the keys; the first half's MMAs run while
-      // the softmax computes the second.  V as an MN-major operand: 8-key
-      // groups kGroup bytes apart, 64-column atoms 1024 bytes apart.
+      const uint32_t aVs = aV + (uint32_t)(st * L::kKvTile);
+      bool k_next = false;  // K of key tile i + 1 has landed
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        if (!mbar_wait_warp(&p_full[h], i & 1, p.status)) {
-          ok = false;
-          break;
+      for (int t = 0; t < kRowTiles; ++t) {
+        if (i >= n_t[t]) continue;
+        // P arrives in two halves of the keys; the first half's MMAs run
+        // while the softmax computes the second.  V as an MN-major operand:
+        // 8-key groups kGroup bytes apart, 64-column atoms 1024 bytes apart.
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          if (!mbar_wait_warp(&p_full[2 * t + h], i & 1, p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int ks = h * kBN / 32; ks < (h + 1) * kBN / 32; ++ks)
+            mma_f16_ta_warp(tmem + L::kColO + t * D, tmem + t * kBN + ks * 8,
+                            smem_desc(aVs + ks * 2 * L::kGroup, 1024, L::kGroup), idesc_o,
+                            (i > 0 || ks > 0) ? 1u : 0u);
         }
-        tc_fence_after();
-#pragma unroll
-        for (int ks = h * kBN / 32; ks < (h + 1) * kBN / 32; ++ks)
-          mma_f16_ta_warp(tmem + L::kColO, tmem + ks * 8,
-                          smem_desc(aV + ks * 2 * L::kGroup, 1024, L::kGroup), idesc_o,
-                          (i > 0 || ks > 0) ? 1u : 0u);
+        if (!ok) break;
+        mma_commit_warp(&pv_done[t]);
+        if (t == last_t) {
+          mma_commit_warp(&v_empty[st]);
+          if (i + 1 < n_tiles &&
+              !mbar_wait_warp(&v_full[(i + 1) % kStages], ((i + 1) / kStages) & 1, p.status)) {
+            ok = false;
+            break;
+          }
+        }
+        if (i + 1 < n_t[t]) {
+          if (!k_next) {
+            if (!mbar_wait_warp(&k_full[(i + 1) % kStages], ((i + 1) / kStages) & 1, p.status)) {
+              ok = false;
+              break;
+            }
+            k_next = true;
+          }
+          if (!mbar_wait_warp(&pv_done[t], i & 1, p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          issue_s(t, i + 1);
+        }
       }
       if (!ok) break;
-      mma_commit_warp(pv_done);
-      mma_commit_warp(v_empty);
+      if (k_next) mma_commit_warp(&k_empty[(i + 1) % kStages]);
     }
     mma_commit_warp(drain);
     mbar_drain(drain, 0);
     __syncwarp();
   } else if (warp < kSoftmaxWarps) {
     // ------------------------------------------- softmax / epilogue (rows)
-    const int t = warp / 4;                 // row tile (the CTA's only one)
+    const int t = warp / 4;                 // row tile of this warpgroup
     const int r = threadIdx.x & (kBM - 1);  // row of the tile == TMEM lane
-    const int nt = n_t[t];
+    const int nt = t == 0 ? n_t[0] : n_t[1];  // (a select: no local-memory array)
     const int jq = j0 + t * qpt + r / Gp;
     const int g = r % Gp;
     const bool row_valid = jq < nq && g < G && q0 + jq < p.total_queries;
@@ -567,7 +625,7 @@ cudaError_t launch_paged_prefill(const PrefillArgs& a, cudaStream_t stream, bool
   // About one wave of CTAs (one per SM) per group; the count only shapes
   // the order, not the result.
   const int pairs = a.num_kv_heads * a.num_seqs;
-  p.pairs_per_group = std::max(1, std::min(pairs, 2 * a.sm_count / std::max(1, q_tiles)));
+  p.pairs_per_group = std::max(1, std::min(pairs, a.sm_count / std::max(1, q_tiles)));
   if (a.dtype == PKV_F16) {
     return a.head_dim == 64
                ? launch_prefill_typed<__half, 64>(p, qm, km, vm, q_tiles, a.num_seqs, stream)
