@@ -22,10 +22,11 @@
 // two such chains on one tensor core fall into step, each softmax running
 // beside the other's instead of beside its MMAs).
 //
-//   warp 8   producer: the Q rows of both tiles (one 4-D TMA copy per 8-row
-//            group), then per key tile the tile's block ids and every
-//            (block, head) run of K and of V (one 4-D TMA copy each, 128-byte
-//            swizzle) into the next free slot.
+//   warp 8   producer: the Q rows of each tile (one 4-D TMA copy per tile;
+//            tile A's, then the first K tile, then tile B's), then per key
+//            tile the tile's block ids and every (block, head) run of K and
+//            of V (one 4-D TMA copy each, 128-byte swizzle) into the next free
+//            slot.
 //   warp 9   issues S = Q K^T (Q and K from shared memory) and O += P V (P
 //            from tensor memory, V as an MN-major operand, rows past the
 //            context cleared first); allocates and frees the tensor memory.
@@ -75,11 +76,13 @@ constexpr int kPrefillThreads = (kSoftmaxWarps + 2) * 32;
 constexpr int kTmemCols = 512;
 constexpr int kBarSlots = 24;   // mbarriers reserved in shared memory
 
-// Shared-memory tiles (Q, K and V alike): groups of 8 rows, kGroup bytes
-// apart; within a group, one 1024-byte 128-byte-swizzled atom per 64
-// columns.  This is the K-major operand layout with SBO = kGroup, and, for
-// V, the MN-major one with LBO = 1024 and SBO = kGroup.  A single TMA copy
-// fills any number of whole groups with all their atoms.
+// Shared-memory K and V tiles: groups of 8 rows, kGroup bytes apart; within
+// a group, one 1024-byte 128-byte-swizzled atom per 64 columns.  This is the
+// K-major operand layout with SBO = kGroup, and, for V, the MN-major one with
+// LBO = 1024 and SBO = kGroup.  A single TMA copy fills any number of whole
+// groups with all their atoms.  A Q tile is written by one copy of all its
+// 128 rows: one 16 KiB block per 64 columns, 8-row groups 1024 bytes apart
+// in it (the K-major layout with SBO = 1024), so the same kQTile bytes.
 template <int D>
 struct PrefillSmem {
   static constexpr int kAtoms = D / 64;
@@ -144,12 +147,12 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
   uint64_t* k_empty = bars + 2;   // [kStages] K slot read by S (MMA commit)
   uint64_t* v_full = bars + 4;    // [kStages] V slot landed
   uint64_t* v_empty = bars + 6;   // [kStages] V slot read by P V
-  uint64_t* q_full = bars + 8;    // Q rows of both tiles landed
-  uint64_t* s_full = bars + 9;    // [t] S_t computed (MMA commit)
-  uint64_t* p_full = bars + 11;   // [2 t + h] half h of P_t written (after O_t was rescaled)
-  uint64_t* pv_done = bars + 15;  // [t] O_t += P_t V finished (MMA commit)
-  uint64_t* drain = bars + 17;    // the issuer's last MMAs finished
-  static_assert(18 <= kBarSlots, "barrier area too small");
+  uint64_t* q_full = bars + 8;    // [t] Q rows of tile t landed
+  uint64_t* s_full = bars + 10;   // [t] S_t computed (MMA commit)
+  uint64_t* p_full = bars + 12;   // [2 t + h] half h of P_t written (after O_t was rescaled)
+  uint64_t* pv_done = bars + 16;  // [t] O_t += P_t V finished (MMA commit)
+  uint64_t* drain = bars + 18;    // the issuer's last MMAs finished
+  static_assert(19 <= kBarSlots, "barrier area too small");
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kTmemSlot);
 
   const int warp = threadIdx.x >> 5;
@@ -200,8 +203,8 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       mbar_init(&v_full[st], 1);
       mbar_init(&v_empty[st], 1);
     }
-    mbar_init(q_full, 1);
     for (int t = 0; t < kRowTiles; ++t) {
+      mbar_init(&q_full[t], 1);
       mbar_init(&s_full[t], 1);
       mbar_init(&p_full[2 * t], kBM);
       mbar_init(&p_full[2 * t + 1], kBM);
@@ -237,19 +240,18 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       return (lane < kBN / R && i < n_tiles && key < ctx) ? __ldg(trow + key / B) : 0;
     };
     int phys_next = table_entry(0);
-    {
-      // One copy per 8-row group, lane = group, box_heads heads x
-      // box_tokens queries.  Heads past the group and queries past the
-      // sequence are copied too (their rows are masked out and never
-      // written); rows past the end of q read as zero.
-      const int hg = Gp > 8 ? Gp / 8 : 1;   // groups per query
-      const int tpg = Gp > 8 ? 1 : 8 / Gp;  // queries per group
-      if (lane == 0) mbar_arrive_expect_tx(q_full, kRowTiles * L::kQTile);
+    // Q rows of tile t: one copy of G' heads x 128 / G' queries.  Heads past
+    // the group and queries past the sequence are copied too (their rows are
+    // masked out and never written); rows past the end of q read as zero.
+    // Tile A's rows go first, then K of the first key tile, then tile B's.
+    auto load_q = [&](int t) {
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&q_full[t], L::kQTile);
+        tma_load_token_heads(sQ + t * L::kQTile, &qmap, kvh * G, q0 + j0 + t * qpt, &q_full[t]);
+      }
       __syncwarp();
-      if (lane < kRowTiles * kBM / 8)
-        tma_load_token_heads(sQ + lane * L::kGroup, &qmap, kvh * G + (lane % hg) * 8,
-                             q0 + j0 + (lane / hg) * tpg, q_full);
-    }
+    };
+    load_q(0);
     int last_k = -1, last_v = -1;
     for (int i = 0; i < n_tiles; ++i) {
       const int st = i % kStages;
@@ -271,6 +273,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       __syncwarp();
       if (lane < nseg) tma_load_group(sK + dst, &kmap, g8, &k_full[st]);
       last_k = i;
+      if (i == 0) load_q(1);
       if (i >= kStages && !mbar_wait_warp(&v_empty[st], ph, p.status)) break;
       if (lane == 0) mbar_arrive_expect_tx(&v_full[st], bytes);
       __syncwarp();
@@ -284,7 +287,8 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     // CTA leaves: wait, bounded, for the last ones this warp issued.
     if (last_k >= 0) mbar_drain(&k_full[last_k % kStages], (last_k / kStages) & 1);
     if (last_v >= 0) mbar_drain(&v_full[last_v % kStages], (last_v / kStages) & 1);
-    mbar_drain(q_full, 0);
+    mbar_drain(&q_full[0], 0);
+    if (last_k >= 0) mbar_drain(&q_full[1], 0);
     __syncwarp();
   } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------- MMA issuer
@@ -303,19 +307,21 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
 #pragma unroll
       for (int ks = 0; ks < D / 16; ++ks) {
         const uint32_t koff = (ks / 4) * 1024 + (ks % 4) * 32;
-        mma_f16_ss_warp(tmem + t * kBN, smem_desc(qb + koff, 16, L::kGroup),
+        const uint32_t qoff = (ks / 4) * (kBM * 128) + (ks % 4) * 32;
+        mma_f16_ss_warp(tmem + t * kBN, smem_desc(qb + qoff, 16, 1024),
                         smem_desc(kb + koff, 16, L::kGroup), idesc_s, ks > 0);
       }
       mma_commit_warp(&s_full[t]);
     };
-    bool ok = mbar_wait_warp(q_full, 0, p.status) && mbar_wait_warp(&k_full[0], 0, p.status);
-    if (ok) {
-      tc_fence_after();
+    bool ok = mbar_wait_warp(&k_full[0], 0, p.status);
 #pragma unroll
-      for (int t = 0; t < kRowTiles; ++t)
-        if (n_t[t] > 0) issue_s(t, 0);
-      mma_commit_warp(&k_empty[0]);
+    for (int t = 0; t < kRowTiles; ++t) {
+      if (!ok || n_t[t] == 0) continue;
+      ok = mbar_wait_warp(&q_full[t], 0, p.status);
+      tc_fence_after();
+      if (ok) issue_s(t, 0);
     }
+    if (ok) mma_commit_warp(&k_empty[0]);
     // V of key tile i is waited for while the last P V of tile i - 1 runs,
     // off the path from one tile's S to the other's P V.
     ok = ok && mbar_wait_warp(&v_full[0], 0, p.status);
@@ -590,10 +596,10 @@ cudaError_t launch_paged_prefill(const PrefillArgs& a, cudaStream_t stream, bool
   }
   int gp = 1;
   while (gp < a.num_q_heads / a.num_kv_heads) gp <<= 1;
-  // Q rows: 8-row groups of box_heads heads x box_tokens queries.
+  // Q rows: one copy per row tile, G' heads x 128 / G' queries (G' <= 128).
   CUtensorMap qm;
   if (!make_token_head_map(&qm, a.q, a.dtype, a.total_queries, a.num_q_heads, a.head_dim,
-                           gp < 8 ? gp : 8, gp < 8 ? 8 / gp : 1)) {
+                           gp, kBM / gp)) {
     *unsupported = true;
     return cudaErrorInvalidValue;
   }
