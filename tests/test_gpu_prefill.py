@@ -50,7 +50,10 @@ def _run(case, chunks, seed):
 @pytest.mark.parametrize("dtype,hq,hkv,D,B", [
     ("bf16", 8, 8, 128, 16), ("fp16", 8, 8, 128, 16), ("bf16", 32, 8, 128, 16),
     ("fp16", 16, 2, 64, 8), ("bf16", 12, 4, 128, 128), ("bf16", 6, 2, 64, 32),
-    ("fp16", 4, 4, 64, 64), ("bf16", 32, 1, 128, 16), ("fp16", 24, 4, 64, 32)])
+    ("fp16", 4, 4, 64, 64), ("bf16", 32, 1, 128, 16), ("fp16", 24, 4, 64, 32),
+    # groups of 5 (padded to 8 rows a query), 64 and 128 (one query per row tile):
+    # each row tile's Q is one copy of G' heads x 128 / G' queries
+    ("bf16", 10, 2, 128, 32), ("bf16", 64, 1, 64, 16), ("fp16", 128, 1, 128, 16)])
 def test_prefill_matches_oracle(cuda_device, dtype, hq, hkv, D, B):
     lens = [1, 17, 130, 300, 64, 257]
     chunks = [1, 17, 130, 45, 1, 200]   # whole prompt, partial chunks, single queries
