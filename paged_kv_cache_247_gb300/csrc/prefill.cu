@@ -120,7 +120,19 @@ struct PrefillParams {
   int q_tiles;          // CTAs per (sequence, KV head)
   int pairs_per_group;  // (sequence, KV head) pairs whose items are launched together
   int total_queries;    // rows of q and out
+  int prefetch_stride;  // work items between a CTA and the one likely to follow it on its SM
 };
+
+// A Q box (as tma_load_token_heads copies it) fetched into L2 only: no
+// shared memory, no barrier.
+__device__ __forceinline__ void tma_prefetch_token_heads(const CUtensorMap* map, int head,
+                                                         int token) {
+  asm volatile(
+      "cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %1}];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(0), "r"(head), "r"(token)
+      : "memory");
+}
 
 // Byte offset of 16-byte chunk c of row r in a tile of the layout above.
 template <int D>
@@ -273,7 +285,26 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       __syncwarp();
       if (lane < nseg) tma_load_group(sK + dst, &kmap, g8, &k_full[st]);
       last_k = i;
-      if (i == 0) load_q(1);
+      if (i == 0) {
+        load_q(1);
+        // The CTA that will most likely start on this SM when this one ends
+        // (one wave of CTAs later): its Q rows into L2 now, so that its first
+        // S does not wait for them from DRAM.
+        const int j2 = (int)blockIdx.x + p.prefetch_stride;
+        if (lane == 0 && j2 < (int)gridDim.x) {
+          const int grp2 = j2 / per_group;
+          const int gsize2 = min(p.pairs_per_group, pairs - grp2 * p.pairs_per_group);
+          const int rem2 = j2 - grp2 * per_group;
+          const int qt2 = p.q_tiles - 1 - rem2 / gsize2;
+          const int pair2 = grp2 * p.pairs_per_group + rem2 % gsize2;
+          const int q02 = __ldg(p.query_start + pair2 / p.num_kv_heads);
+#pragma unroll
+          for (int t = 0; t < kRowTiles; ++t)
+            tma_prefetch_token_heads(&qmap, (pair2 % p.num_kv_heads) * G,
+                                     q02 + qt2 * kRowTiles * qpt + t * qpt);
+        }
+        __syncwarp();
+      }
       if (i >= kStages && !mbar_wait_warp(&v_empty[st], ph, p.status)) break;
       if (lane == 0) mbar_arrive_expect_tx(&v_full[st], bytes);
       __syncwarp();
@@ -628,6 +659,7 @@ cudaError_t launch_paged_prefill(const PrefillArgs& a, cudaStream_t stream, bool
   p.num_seqs = a.num_seqs;
   p.q_tiles = q_tiles;
   p.total_queries = a.total_queries;
+  p.prefetch_stride = std::max(1, a.sm_count);
   // About one wave of CTAs (one per SM) per group; the count only shapes
   // the order, not the result.
   const int pairs = a.num_kv_heads * a.num_seqs;
