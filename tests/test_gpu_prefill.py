@@ -117,6 +117,37 @@ def test_prefill_full_size_sampled(cuda_device):
         assert_within_tol(out[row:row + 1], ref, torch.bfloat16, f"prefill seq {s} query {j}")
 
 
+def test_prefill_long_context_sampled(cuda_device):
+    """Chunks at the end of 32k-token contexts: 256 key tiles per row tile, so
+    the K and V rings wrap around many times, with a chunk that ends in a
+    partial row tile; checked on sampled queries against decode attention
+    over each query's visible prefix."""
+    lens = [32768, 30001]
+    chunks = [192, 77]
+    case = W.make_decode_case(31, len(lens), 32, 8, 128, 16, "bf16", lens, pool_factor=1.0,
+                              device=cuda_device)
+    qs = np.concatenate([[0], np.cumsum(chunks)]).astype(np.int32)
+    gen = torch.Generator(device=cuda_device).manual_seed(12)
+    q = torch.randn((int(qs[-1]), 32, 128), generator=gen, device=cuda_device).to(torch.bfloat16)
+    out = torch.full_like(q, float("nan"))
+    pkv.paged_attn_prefill(out, q, torch.from_numpy(qs).to(cuda_device), case.k_cache,
+                           case.v_cache, case.block_tables, case.context_lens, case.scale,
+                           case.max_context_len, max(chunks))
+    torch.cuda.synchronize()
+    assert not torch.isnan(out).any()
+    tables = case.block_tables.cpu().numpy()
+    B = 16
+    for s, j in [(0, 0), (0, 31), (0, 32), (0, 191), (1, 0), (1, 64), (1, 76)]:
+        p = lens[s] - chunks[s] + j
+        nb = -(-(p + 1) // B)
+        blocks = torch.from_numpy(tables[s, :nb].astype(np.int64)).to(cuda_device)
+        k_sub, v_sub = to_f64(case.k_cache[blocks]), to_f64(case.v_cache[blocks])
+        row = int(qs[s]) + j
+        ref = oracle.paged_decode_attention(to_f64(q[row:row + 1]), k_sub, v_sub,
+                                            np.arange(nb)[None, :], np.array([p + 1]), case.scale)
+        assert_within_tol(out[row:row + 1], ref, torch.bfloat16, f"long context seq {s} query {j}")
+
+
 def test_prefill_empty_chunks_and_bad_context(cuda_device):
     """Sequences without queries leave nothing to do; a context shorter than
     its chunk is flagged (PKV_DEV_BAD_CONTEXT_LEN = 2) and skipped, while the
