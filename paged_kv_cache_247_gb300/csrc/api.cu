@@ -3,6 +3,7 @@
 
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <math.h>
 #include <mutex>
 
@@ -379,7 +380,16 @@ pkv_status_t paged_decode_impl(void* out, const void* q, const void* k_new, cons
   if (err != cudaSuccess) return cuda_fail(err);
   if (plan.tc) {
     bool unsupported = false;
-    err = pkv::launch_paged_decode_tc(p, dtype, head_dim, device_sms(),
+    // CTAs for the persistent walk: as many as the SMs, or fewer so that
+    // every CTA walks the same number of items.  512 items on 152 SMs, say,
+    // run as 4 rounds of 128 CTAs instead of 3 rounds of 152 and a fourth of
+    // 56; each round still keeps HBM busy (one CTA streams about twice its
+    // share), and no CTA waits out a short last round.
+    const long long items = parts * num_kv_heads * (long long)num_seqs;
+    const long long sms = device_sms();
+    const long long rounds = (items + sms - 1) / sms;
+    const int ctas = (int)std::max(1LL, (items + rounds - 1) / rounds);
+    err = pkv::launch_paged_decode_tc(p, dtype, head_dim, ctas,
                                       reinterpret_cast<cudaStream_t>(stream), &unsupported);
     if (unsupported) return PKV_ERR_UNSUPPORTED;
   } else {
