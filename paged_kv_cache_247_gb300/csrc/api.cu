@@ -142,21 +142,24 @@ int auto_partition(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim
                        kPartitionQuantum);
 }
 
-// Partition of the tensor-core decode kernel.  Its CTAs are persistent (one
-// per SM) and take the work items (sequence, KV head, partition) in turn.
-// The choice minimises a model of the call's time in units of one 128-key
-// tile streamed at an SM's share of HBM:
-//   * every SM works through floor(items / SMs) items at its share;
-//   * the remaining items run on fewer SMs, each of which streams at most
-//     about twice its share (the bytes its copy rings keep in flight);
+// Partition of the tensor-core decode kernel.  Its CTAs are persistent and
+// take the work items (sequence, KV head, partition) in turn; the launch
+// uses ceil(items / rounds) CTAs for rounds = ceil(items / SMs), so every CTA
+// walks the same number of items.  The choice minimises a model of the
+// call's time in units of one 128-key tile streamed at an SM's share of HBM:
+//   * each round takes its items' tiles times the fraction of the SMs it
+//     occupies (HBM is shared), but no less than half a tile per tile, since
+//     one SM streams at most about twice its share (the bytes its copy rings
+//     keep in flight);
 //   * each item costs about half a tile more (its output and the switch to
 //     the next item), and a split about two tiles (the partials' round trip
 //     and the merge).
 // On GB300 this picks the fastest of the partitions measured on 8 and 64
-// sequences x 1k to 32k tokens (query-head group 4) and on 32 sequences x
-// 4k tokens with groups of 2 to 32: two partitions where the sequences x KV
-// heads are fewer than the SMs or a few times more, none for 4k tokens over
-// 256 of them, where splitting at 1k cost 5-10 %.
+// sequences x 1k to 8k tokens (query-head group 4) and on 32 sequences x 4k
+// tokens with groups of 4 and 32: two partitions for 8 x 8k and 8 x 32k
+// (64 sequence-heads, fewer than the SMs), none from 512 sequence-heads on
+// (64 x 8k: 1.04 of the copy peak unsplit against 1.00 in two), none for 4k
+// tokens over 256 of them, where splitting at 2k cost 4-10 %.
 int tc_partition(int num_seqs, int num_kv_heads, int max_context_len) {
   const double units = (double)num_seqs * num_kv_heads;
   const double sms = (double)device_sms();
@@ -175,10 +178,10 @@ int tc_partition(int num_seqs, int num_kv_heads, int max_context_len) {
     if ((tiles + pt - 1) / pt != parts) continue;      // the same partition as fewer parts
     const double items = units * (double)parts;
     const double avg = (double)tiles / (double)parts;  // tiles per item
-    const double rounds = floor(items / sms);
-    const double rest = items - rounds * sms;         // items of the last round
-    const double cost = rounds * avg + (rest > 0.0 ? avg / fmin(kMaxRate, sms / rest) : 0.0) +
-                        ceil(items / sms) * kItemCost + (parts > 1 ? kSplitCost : 0.0);
+    const double rounds = ceil(items / sms);
+    const double ctas = ceil(items / rounds);          // CTAs of the launch
+    const double cost = rounds * avg * fmax(ctas / sms, 1.0 / kMaxRate) + rounds * kItemCost +
+                        (parts > 1 ? kSplitCost : 0.0);
     if (parts == 1 || cost < best_cost) {  // ties: fewer partitions
       best_cost = cost;
       best = pt;

@@ -113,10 +113,11 @@ def test_auto_partition_policy(lib):
 def test_tensor_core_partition_policy(lib):
     """The tensor-core kernel's choice (grouped heads): whole 128-key tiles,
     minimising a model of the persistent kernel's time (152 SMs assumed) in
-    tiles at an SM's share of HBM: full rounds of items at that share, the
-    last round's items on fewer SMs at up to twice it, half a tile per item
-    and two tiles for a split.  The shapes below are the ones measured on
-    GB300, where the model picks the fastest partition."""
+    tiles at an SM's share of HBM: rounds of items on ceil(items / rounds)
+    CTAs, each round's tiles times the fraction of the SMs it occupies but
+    at least half, half a tile per item and two tiles for a split.  The
+    shapes below are the ones measured on GB300, where the model picks the
+    fastest partition."""
     import math
     part = lib.pkv_decode_partition_size
 
@@ -124,13 +125,12 @@ def test_tensor_core_partition_policy(lib):
         tiles = -(-ctx // 128)
         items = S * hkv * parts
         avg = tiles / parts
-        rounds = items // sms
-        rest = items - rounds * sms
-        return (rounds * avg + (avg / min(2.0, sms / rest) if rest else 0.0)
-                + math.ceil(items / sms) * 0.5 + (2.0 if parts > 1 else 0.0))
+        rounds = math.ceil(items / sms)
+        ctas = math.ceil(items / rounds)
+        return rounds * avg * max(ctas / sms, 0.5) + rounds * 0.5 + (2.0 if parts > 1 else 0.0)
 
     for S, ctx, want in [(8, 100, 128), (8, 1024, 1024), (64, 1024, 1024), (8, 8192, 4096),
-                         (64, 8192, 4096), (8, 32768, 16384), (64, 32768, 16384),
+                         (64, 8192, 8192), (8, 32768, 16384), (64, 32768, 32768),
                          (32, 4096, 4096), (256, 4096, 4096)]:
         p = part(S, 32, 8, 128, ctx)
         assert p == want, (S, ctx, p)
