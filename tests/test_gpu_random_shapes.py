@@ -20,7 +20,7 @@ from _gpu_util import assert_within_tol, oracle_decode, raw_bytes, to_f64
 
 pytestmark = pytest.mark.gpu
 
-N_CASES = 24
+N_CASES = 48
 
 
 def draw(seed):
