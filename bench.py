@@ -48,13 +48,14 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="opt13b",
-                    choices=["opt13b", "gqa4k", "prefill", "sweep", "shared", "groups"])
+                    choices=["opt13b", "gqa4k", "prefill", "prefill_shapes", "sweep", "shared",
+                             "groups"])
     ap.add_argument("--decode-path", type=int, default=0, choices=[0, 1, 2],
                     help="decode kernel: 0 = the library's choice, 1 = CUDA cores, "
                          "2 = tensor cores where supported")
     ap.add_argument("--only", default=None,
-                    help="--workload sweep: one case as block_size,batch,ctx (for profiler "
-                         "captures)")
+                    help="--workload sweep: one case as block_size,batch,ctx; --workload "
+                         "prefill_shapes: one case's index (for profiler captures)")
     ap.add_argument("--head-dim", type=int, default=128, choices=[64, 128],
                     help="--workload groups: head size")
     ap.add_argument("--block-size", type=int, default=16, choices=[8, 16, 32, 64, 128],
@@ -1319,6 +1320,93 @@ def sweep_line(args, rank, world, local_rank, block_sizes=None):
             "sweep": rows, "empty_kernel_ms": round(floor, 5), "clocks": clock_rec}
 
 
+def run_prefill_shapes(args, rank, world, local_rank):
+    """Chunked prefill across shapes: query-head groups (MHA to 8), head sizes,
+    chunk lengths (long chunks, short chunks at the end of long contexts,
+    whole prompts) and dtypes.  Each case is K launches back to back; TFLOP/s
+    of the causal attention's algorithmic work against the measured bf16
+    tensor peak.  `--only N` runs the N-th case alone (for profiler captures)."""
+    import paged_kv_cache_247_gb300 as pkv
+    from paged_kv_cache_247_gb300 import build as _build
+    from paged_kv_cache_247_gb300 import workloads as W
+    if rank == 0 or not os.path.exists(_build.LIB):
+        _build.build_library()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peak, kind = float(json.load(f)["bf16_tflops"]), "measured (MEASURED_PEAKS.json bf16_tflops, burst)"
+    except (OSError, KeyError, ValueError):
+        peak, kind = 1900.0, "fallback"
+    rng = np.random.default_rng(11)
+    prompts = [int(x) for x in rng.integers(100, 701, size=16)]
+    # (label, Hq, Hkv, D, B, dtype, context lengths, chunk lengths)
+    cases = [
+        ("GQA 32/8, D=128: 8 x 2048 queries over 4096", 32, 8, 128, 16, "bf16",
+         [4096] * 8, [2048] * 8),
+        ("MHA 40/40, D=128 (OPT-13B heads): 8 x 2048 over 4096", 40, 40, 128, 16, "fp16",
+         [4096] * 8, [2048] * 8),
+        ("group 8 (64/8), D=128: 8 x 2048 over 4096", 64, 8, 128, 16, "bf16",
+         [4096] * 8, [2048] * 8),
+        ("GQA 32/8, D=64: 8 x 2048 over 4096", 32, 8, 64, 16, "bf16",
+         [4096] * 8, [2048] * 8),
+        ("short chunks, GQA 32/8, D=128: 64 x 256 over 4096", 32, 8, 128, 16, "bf16",
+         [4096] * 64, [256] * 64),
+        ("long context, GQA 32/8, D=128: 2 x 8192 over 32768", 32, 8, 128, 16, "bf16",
+         [32768] * 2, [8192] * 2),
+        ("whole prompts, MHA 40/40, D=128: 16 prompts of 100-700 tokens", 40, 40, 128, 16,
+         "fp16", prompts, prompts),
+    ]
+    pick = [int(args.only)] if args.only else range(len(cases))
+    rows = []
+    clocks = ClockSampler(dev.index if dev.index is not None else 0)
+    clocks.start()
+    iters = max(5, min(args.steps, 20))
+    for ci in pick:
+        label, hq, hkv, D, B, dt, lens, chunks = cases[ci]
+        case = W.make_decode_case(700 + ci, len(lens), hq, hkv, D, B, dt, lens,
+                                  pool_factor=1.0, device=dev)
+        qs = torch.tensor(np.concatenate([[0], np.cumsum(chunks)]), dtype=torch.int32,
+                          device=dev)
+        gen = torch.Generator(device=dev).manual_seed(ci)
+        q = torch.randn((int(qs[-1]), hq, D), generator=gen, device=dev).to(case.q.dtype)
+        out = torch.empty_like(q)
+        max_chunk = max(chunks)
+
+        def call():
+            pkv.paged_attn_prefill(out, q, qs, case.k_cache, case.v_cache, case.block_tables,
+                                   case.context_lens, case.scale, case.max_context_len,
+                                   max_chunk)
+        t_host = 0.0
+        for i in range(max(3, args.warmup)):
+            t0 = time.perf_counter()
+            call()
+            t_host += time.perf_counter() - t0
+        torch.cuda.synchronize()
+        host_ms = 1e3 * t_host / max(3, args.warmup)
+        ms = timed_steps(call, iters, stream, host_ms) / iters
+        flops = prefill_flops(lens, chunks, hq, D)
+        tf = flops / (ms * 1e-3) / 1e12
+        rows.append({"case": label, "dtype": dt, "algorithmic_flops": flops,
+                     "ms": round(ms, 5), "TFLOP/s": round(tf, 1), "frac": round(tf / peak, 4)})
+        del case, q, out
+        torch.cuda.empty_cache()
+    clock_rec = clocks.stop()
+    if pkv.device_status(clear=True) != 0:
+        raise RuntimeError("device status flags during the prefill shape sweep")
+    if rank == 0:
+        print(json.dumps({
+            "metric": "paged chunked-prefill attention TFLOP/s across shapes (causal, algorithmic)",
+            "value": rows[0]["TFLOP/s"], "unit": "TFLOP/s", "n_gpus": world, "steps": iters,
+            "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16/fp16 (per case)", "data": "synthetic",
+            "config": {"workload": "chunked prefill shape sweep", "B": 16,
+                       "timing": "launches back to back between two events",
+                       "peak": peak, "peak_kind": kind},
+            "cases": rows, "clocks": clock_rec}), flush=True)
+
+
 def run_groups(args, rank, world, local_rank):
     """Decode across query-head group sizes over one KV cache shape (8 KV heads
     of 128, bf16, 4,096 tokens per sequence): each call timed alone after
@@ -1399,6 +1487,13 @@ def main():
                                       "the reference arm is timed on the decode workloads"}))
             else:
                 run_prefill(args, rank, world, local_rank)
+        elif args.workload == "prefill_shapes":
+            if args.impl == "reference":
+                if rank == 0:
+                    print(json.dumps({"impl": "reference", "unavailable":
+                                      "the reference arm is timed on the decode workloads"}))
+            else:
+                run_prefill_shapes(args, rank, world, local_rank)
         elif args.workload == "shared":
             if args.impl == "reference":
                 if rank == 0:
