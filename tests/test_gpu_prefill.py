@@ -148,6 +148,53 @@ def test_prefill_long_context_sampled(cuda_device):
         assert_within_tol(out[row:row + 1], ref, torch.bfloat16, f"long context seq {s} query {j}")
 
 
+@pytest.mark.parametrize("dtype,hq,D,lens,chunks", [
+    ("bf16", 32, 128, [1500, 1300], [1500, 1200]),  # 8 queries a CTA: 188 query tiles
+    ("fp16", 128, 64, [400, 150], [400, 150]),      # 2 queries a CTA: 200 query tiles
+])
+def test_prefill_more_query_tiles_than_sms(cuda_device, dtype, hq, D, lens, chunks):
+    """Large groups (one KV head): more query tiles per (sequence, KV head) than
+    the device has SMs, so each launch-order group holds one pair and the Q
+    rows fetched ahead for the next wave belong to the same sequence; every
+    output against the oracle."""
+    case = W.make_decode_case(hq + D, len(lens), hq, 1, D, 16, dtype, lens, pool_factor=1.2,
+                              poison=True, device=cuda_device)
+    q, out, ref, qs = _run(case, chunks, seed=hq)
+    assert_within_tol(out, ref, W.DTYPES[dtype], f"prefill {hq}/1 D={D} chunks {chunks}")
+
+
+def test_prefill_whole_prompts_sampled(cuda_device):
+    """The prefill shape sweep's whole-prompt case (16 prompts of 100-700
+    tokens, each queried whole, 40 MHA heads, fp16): 760 of its 1,920 CTAs
+    find no queries; sampled queries of every prompt against decode attention
+    over their visible prefix, on every head."""
+    rng = np.random.default_rng(11)
+    prompts = [int(x) for x in rng.integers(100, 701, size=16)]
+    case = W.make_decode_case(704, len(prompts), 40, 40, 128, 16, "fp16", prompts,
+                              pool_factor=1.0, device=cuda_device)
+    qs = np.concatenate([[0], np.cumsum(prompts)]).astype(np.int32)
+    gen = torch.Generator(device=cuda_device).manual_seed(4)
+    q = torch.randn((int(qs[-1]), 40, 128), generator=gen, device=cuda_device).half()
+    out = torch.full_like(q, float("nan"))
+    pkv.paged_attn_prefill(out, q, torch.from_numpy(qs).to(cuda_device), case.k_cache,
+                           case.v_cache, case.block_tables, case.context_lens, case.scale,
+                           case.max_context_len, max(prompts))
+    torch.cuda.synchronize()
+    assert not torch.isnan(out).any()
+    tables = case.block_tables.cpu().numpy()
+    pick = np.random.default_rng(5)
+    for s, n in enumerate(prompts):
+        for j in (0, n - 1, int(pick.integers(n))):
+            nb = -(-(j + 1) // 16)
+            blocks = torch.from_numpy(tables[s, :nb].astype(np.int64)).to(cuda_device)
+            k_sub, v_sub = to_f64(case.k_cache[blocks]), to_f64(case.v_cache[blocks])
+            row = int(qs[s]) + j
+            ref = oracle.paged_decode_attention(to_f64(q[row:row + 1]), k_sub, v_sub,
+                                                np.arange(nb)[None, :], np.array([j + 1]),
+                                                case.scale)
+            assert_within_tol(out[row:row + 1], ref, torch.float16, f"prompt {s} query {j}")
+
+
 def test_prefill_empty_chunks_and_bad_context(cuda_device):
     """Sequences without queries leave nothing to do; a context shorter than
     its chunk is flagged (PKV_DEV_BAD_CONTEXT_LEN = 2) and skipped, while the
