@@ -219,7 +219,10 @@ int pkv_decode_partition_size(int num_seqs, int num_q_heads, int num_kv_heads,
  * control; the default suits every shape measured):
  *   0  chosen per call (default): the tensor-core kernel for grouped heads
  *      (groups of 2 to 32 query heads, head_dim 64 or 128, partition_size 0
- *      or a multiple of 128), the CUDA-core kernel otherwise (MHA);
+ *      or a multiple of 128) and for single-head groups (MHA) with fewer
+ *      than 8 (sequence, KV head) pairs per SM; the CUDA-core kernel
+ *      otherwise (MHA with more pairs, or a partition the tensor-core
+ *      kernel cannot take);
  *   1  always the CUDA-core kernel;
  *   2  the tensor-core kernel wherever it can run (groups of 1 to 32, head_dim
  *      64 or 128, partition_size 0 or a multiple of 128), else the CUDA-core

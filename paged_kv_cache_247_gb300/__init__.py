@@ -4,8 +4,8 @@ Device calls (hand-written CUDA behind the C ABI of ``libpagedkv.so``):
 
 * :func:`paged_attn_decode` — single-query decode attention walking each
   sequence's block table, with split-context partitions and GQA grouping
-  (grouped heads of 128 on the tcgen05 tensor cores, single-head groups on
-  the CUDA cores);
+  (grouped heads and small single-head calls on the tcgen05 tensor cores,
+  single-head groups with many (sequence, head) pairs on the CUDA cores);
 * :func:`kv_append` — scatter of each step's new K/V into its slot;
 * :func:`paged_attn_decode_append` — both in one launch (the new token is
   written to its slot and used directly);

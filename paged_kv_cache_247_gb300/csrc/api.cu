@@ -202,9 +202,18 @@ int g_decode_path = 0;
 // faster than the CUDA-core one on every grouped shape of GB300 (groups of 2
 // to 32, head sizes 64 and 128, 8 to 256 sequences, 1k to 32k tokens, blocks
 // of 8 to 128), so it takes every grouped call it supports.  Single-head
-// groups (MHA) stay on the CUDA-core kernel: on the OPT-13B layer (64
-// sequences of lognormal lengths) it reaches the HBM roofline, 0.1172 ms,
-// where the tensor-core kernel's static walk of unequal items takes 0.1306.
+// groups (MHA) take the CUDA-core kernel once there are enough (sequence,
+// head) pairs to fill the GPU without splitting: on the OPT-13B layer (64
+// sequences of lognormal lengths, 2,560 pairs) it reaches the HBM roofline,
+// 0.1172 ms, where the tensor-core kernel's static walk of unequal items
+// takes 0.128-0.131.  With fewer pairs the CUDA-core kernel splits the
+// contexts and pays the reduction, and the tensor-core kernel measured
+// faster: 2 to 16 sequences of that layer 10-50 %, 4 and 16 sequences of 4k
+// tokens 7-13 %, 8 to 64 sequences of 4k tokens over 8 heads 3-16 %; the two
+// tie at 32 sequences of the layer (1,280 pairs) and at 128 of 4k tokens over
+// 8 heads (1,024).
+constexpr int kMhaTcPairsPerSm = 8;  // below this many pairs per SM: tensor cores
+
 struct DecodePlan {
   bool tc;
   int partition;
@@ -214,7 +223,9 @@ DecodePlan decode_plan(int num_seqs, int num_q_heads, int num_kv_heads, int head
                        int max_context_len, int partition_size) {
   const int group = num_q_heads / num_kv_heads;
   const int path = __atomic_load_n(&g_decode_path, __ATOMIC_RELAXED);
-  bool tc = path == 2 || (path == 0 && group >= 2);
+  const bool few_pairs =
+      (long long)num_seqs * num_kv_heads < (long long)kMhaTcPairsPerSm * device_sms();
+  bool tc = path == 2 || (path == 0 && (group >= 2 || few_pairs));
   if (tc && !pkv::decode_tc_supported(head_dim, group,
                                       partition_size ? partition_size
                                                      : pkv::kTcPartitionQuantum))

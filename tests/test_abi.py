@@ -137,11 +137,18 @@ def test_tensor_core_partition_policy(lib):
         tiles = -(-ctx // 128)
         parts = -(-tiles // (p // 128))
         assert model(S, 8, ctx, parts) <= min(model(S, 8, ctx, n) for n in range(1, 17)) + 1e-9
-    # groups of 2 to 32 share the policy; single-head groups do not (by default)
+    # groups of 2 to 32 share the policy, and so do single-head groups with
+    # fewer than 8 (sequence, KV head) pairs per SM; with more they take the
+    # CUDA-core kernel and its partitions (any multiple of 32)
     assert part(8, 16, 8, 128, 8192) == part(8, 256, 8, 128, 8192) == 4096
-    assert part(8, 8, 8, 128, 8192) % 128 != 0
-    assert lib.pkv_decode_uses_tensor_cores(8, 8, 8, 128, 8192, 0) == 0
+    assert part(8, 8, 8, 128, 8192) == 4096
+    assert lib.pkv_decode_uses_tensor_cores(8, 8, 8, 128, 8192, 0) == 1
     assert lib.pkv_decode_uses_tensor_cores(8, 16, 8, 64, 8192, 0) == 1
+    sms = 152  # no device here: the library assumes a GB300
+    assert lib.pkv_decode_uses_tensor_cores(8 * sms // 40 + 1, 40, 40, 128, 2048, 0) == 0
+    assert lib.pkv_decode_uses_tensor_cores(8 * sms // 40, 40, 40, 128, 2048, 0) == 1
+    assert lib.pkv_decode_uses_tensor_cores(64, 40, 40, 128, 2048, 0) == 0  # the OPT-13B layer
+    assert part(256, 8, 8, 128, 2000) % 128 != 0  # CUDA-core kernel: one partition, not whole tiles
 
 
 def test_auto_partition_properties(lib):

@@ -163,15 +163,14 @@ def test_long_contexts_sampled(cuda_device, group, head_dim):
 
 def test_default_path_takes_grouped_heads(lib, cuda_device):
     """By default grouped heads go to the tensor-core kernel (its partitions
-    are whole 128-key tiles) and single-head groups to the CUDA-core kernel;
-    both agree with the oracle."""
+    are whole 128-key tiles), and so do single-head groups with few (sequence,
+    KV head) pairs (8 x 8 here); both agree with the oracle."""
     lib.pkv_set_decode_path(0)
     assert lib.pkv_get_decode_path() == 0
     for hq, hkv in ((64, 8), (32, 8), (8, 8)):
         part = pkv.decode_partition_size(8, hq, hkv, 128, 8192)
-        assert part > 0 and part % 32 == 0
-        if hq // hkv >= 2:
-            assert part % 128 == 0
+        assert pkv.decode_uses_tensor_cores(8, hq, hkv, 128, 8192)
+        assert part > 0 and part % 128 == 0
         lens = [8192, 100, 5000, 7777, 1, 4096, 3000, 8000]
         case = W.make_decode_case(hq + 1, 8, hq, hkv, 128, 16, "bf16", lens, pool_factor=1.1,
                                   device=cuda_device)
