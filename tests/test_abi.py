@@ -244,8 +244,10 @@ def test_decode_path_switch(lib):
         assert lib.pkv_decode_partition_size(8, 256, 8, 128, 32768) % 128 == 0
         assert lib.pkv_set_decode_path(2) == 0
         assert lib.pkv_decode_partition_size(8, 32, 8, 128, 8192) % 128 == 0
-        # forced, single-head groups run on the tensor cores too; head size 64 has both
+        # forced, single-head groups run on the tensor cores whatever their number
+        # of (sequence, head) pairs; head size 64 has both
         assert lib.pkv_decode_uses_tensor_cores(8, 8, 8, 128, 8192, 0) == 1
+        assert lib.pkv_decode_uses_tensor_cores(256, 40, 40, 128, 2048, 0) == 1
         assert lib.pkv_decode_uses_tensor_cores(8, 64, 8, 64, 8192, 0) == 1
         assert lib.pkv_decode_uses_tensor_cores(8, 64, 8, 64, 8192, 96) == 0  # not whole tiles
         for args in ((8, 8, 8, 128, 8192), (8, 64, 8, 64, 8192)):
