@@ -209,7 +209,8 @@ int g_decode_path = 0;
 // takes 0.128-0.131.  With fewer pairs the CUDA-core kernel splits the
 // contexts and pays the reduction, and the tensor-core kernel measured
 // faster: 2 to 16 sequences of that layer 10-50 %, 4 and 16 sequences of 4k
-// tokens 7-13 %, 8 to 64 sequences of 4k tokens over 8 heads 3-16 %; the two
+// tokens over 40 heads 12 and 3 %, 8 to 64 sequences of 4k tokens over 8
+// heads 4-16 % (at head size 64 as well: 8-26 %); the two
 // tie at 32 sequences of the layer (1,280 pairs) and at 128 of 4k tokens over
 // 8 heads (1,024).
 constexpr int kMhaTcPairsPerSm = 8;  // below this many pairs per SM: tensor cores
